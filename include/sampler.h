@@ -1,0 +1,193 @@
+/*
+ * sampler.h -- C ABI of libsampler.so, the per-decode-step token sampler for
+ * GB300 (sm_103a).
+ *
+ * One call samples one token for each of N output rows of an LLM's [rows, V]
+ * logits tensor. Every row carries its own parameters, so one top-p or greedy
+ * request never changes what the other rows of the batch compute.
+ *
+ * The stages, in order, follow the xbrilliance.ai note "采样参数对解码开销的影响：
+ * temperature、top_p 与采样核路径" (Effect of sampling parameters on decode cost),
+ * section "解码一步里采样做什么" (what sampling does in one decode step):
+ *   penalties -> temperature -> top-k / top-p -> min-p -> fp32 softmax and
+ *   log_softmax -> pick.
+ * The parameters and their defaults follow its section
+ * "哪些参数会额外打开一趟全词表计算" (which parameters open an extra full-vocab
+ * pass): temperature 1.0, top_p 1.0, top_k -1, min_p 0, presence 0, frequency
+ * 0, repetition 1.0. Greedy below T = 1e-5 and the seeded type follow its
+ * section "采样类型与选路" (sampling type and routing). The random pick is the
+ * Gumbel-max rule of the dev.to claim check "SGLang's +75% sampler speedup
+ * skips Qwen3 chat requests", section "Nine lines, and exactly one call site":
+ * the token is argmax_v p_v / E_v with E_v ~ Exp(1). Returned logprobs are
+ * temperature-scaled, as in the SGLang manual "manual-sglang-101", section
+ * "Logprobs are temperature-scaled".
+ *
+ * Exact semantics (readings of the pages where they are silent):
+ *  - penalties, for a token v seen c_v > 0 times in the row's history:
+ *        x = x > 0 ? x / repetition : x * repetition;
+ *        x = x - frequency * c_v;     x = x - presence;
+ *    each step one IEEE fp32 operation, no fused multiply-add;
+ *  - T < 1e-5 picks the argmax of the penalised logits (lowest index on ties);
+ *    the outputs of such a row use T = 1;
+ *  - top_k keeps exactly k tokens in (value desc, index asc) order;
+ *    -1 or k >= V keeps all;
+ *  - top_p keeps, over the top-k set, the tokens whose exclusive prefix mass
+ *    (softmax at T over that set, same order) is < top_p; at least one stays;
+ *  - min_p keeps tokens with p_v >= min_p * p_max;
+ *  - the pick is argmax over the kept set of x_v / T - ln(E_v), ties to the
+ *    lowest index. E_v = -ln(u_v), u_v = (2 * (w >> 9) + 1) * 2^-24, where w is
+ *    word (v & 3) of Philox4x32-10 (Salmon et al., SC'11) with
+ *        key     = (lo32, hi32) of (has_seed[r] ? seed[r] : global_seed),
+ *        counter = (v >> 2, stream, lo32(offset), hi32(offset)),
+ *        stream  = (stream_id[r] & 0x7fffffff) | (has_seed[r] ? 0x80000000 : 0);
+ *    stream_id == NULL means stream_id[r] = r for unseeded rows and 0 for
+ *    seeded rows, so that a seeded row draws the same numbers wherever it sits
+ *    in the batch (give the forks of one seeded request distinct stream ids);
+ *  - probs = exp(x/T - lse) on the kept set and 0 elsewhere; logprobs =
+ *    x/T - lse on the kept set and -inf elsewhere; lse over the kept set.
+ *
+ * Threading: a handle is used by one host thread and one stream at a time.
+ */
+#ifndef DECODE_STEP_TOKEN_SAMPLER_H
+#define DECODE_STEP_TOKEN_SAMPLER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle. */
+typedef struct sampler_s* sampler_t;
+
+/* A cudaStream_t (CUstream). NULL is the legacy default stream. */
+typedef struct CUstream_st* sampler_stream_t;
+
+/* Logits element types. */
+enum {
+    SAMPLER_DTYPE_F32 = 0,  /* IEEE binary32 */
+    SAMPLER_DTYPE_BF16 = 1  /* bfloat16: the upper 16 bits of a binary32 */
+};
+
+/* Return codes of the calls (0 = success; negative = the call did nothing). */
+enum {
+    SAMPLER_OK = 0,
+    SAMPLER_ERR_NULL_ARG = -1,     /* a required pointer is NULL */
+    SAMPLER_ERR_BAD_SHAPE = -2,    /* n_rows < 0, vocab < 1, row_stride < vocab, ... */
+    SAMPLER_ERR_TOO_LARGE = -3,    /* n_rows > max_rows or vocab > max_vocab */
+    SAMPLER_ERR_BAD_DTYPE = -4,
+    SAMPLER_ERR_CUDA = -5,         /* a CUDA call failed (launch, copy, set-up) */
+    SAMPLER_ERR_NO_DEVICE = -6,    /* no usable sm_100-family device */
+    SAMPLER_ERR_NO_STAGING = -7    /* sampler_sample_host on a handle made without staging */
+};
+
+/* Per-row status codes written to out_status (when given). A row with a
+ * non-zero status gets token -1 and NaN probs / logprobs; the other rows are
+ * unaffected. When several apply, the first in this list is reported. */
+enum {
+    SAMPLER_ROW_OK = 0,
+    SAMPLER_ROW_BAD_PARAM = 3,      /* T < 0, NaN or inf; top_k == 0 or < -1; top_p not
+                                       in (0, 1]; min_p not in [0, 1]; repetition <= 0,
+                                       NaN or inf; presence / frequency NaN or inf */
+    SAMPLER_ROW_BAD_HISTORY = 4,    /* a history id outside [0, V), or more than 65535
+                                       ids in one row's history */
+    SAMPLER_ROW_NONFINITE = 1,      /* a NaN or +inf logit (after penalties) */
+    SAMPLER_ROW_ALL_NEG_INF = 2,    /* every logit is -inf */
+    SAMPLER_ROW_TIMEOUT = 5         /* an internal wait gave up (never expected) */
+};
+
+/* Create-time limits. */
+typedef struct {
+    int device;            /* CUDA device ordinal the handle is bound to */
+    int64_t max_rows;      /* largest n_rows a call may pass (>= 1) */
+    int64_t max_vocab;     /* largest vocab a call may pass (1 .. 262144) */
+    int64_t max_history;   /* sampler_sample_host only: largest total history length */
+    uint32_t flags;        /* SAMPLER_CREATE_* bits */
+} sampler_config_t;
+
+/* Reserve device staging buffers for sampler_sample_host (max_rows x max_vocab
+ * fp32 logits, probs, logprobs, and the per-row arrays). */
+#define SAMPLER_CREATE_HOST_STAGING 1u
+
+/*
+ * Arguments of one sampling call. For sampler_sample every pointer is a device
+ * pointer; for sampler_sample_host every pointer is a host pointer. The caller
+ * owns every buffer. Arrays marked [N] have n_rows entries; NULL optional
+ * arrays take the default given.
+ */
+typedef struct {
+    /* logits: rows of `vocab` elements, row i starting at element i * row_stride */
+    const void* logits;
+    int32_t dtype;                   /* SAMPLER_DTYPE_* */
+    int64_t n_rows;                  /* N output rows (0 = nothing to do) */
+    int64_t vocab;                   /* V */
+    int64_t row_stride;              /* elements between logits rows (>= V) */
+    int64_t n_logit_rows;            /* rows in `logits` (only read by sampler_sample_host;
+                                        0 = n_rows) */
+    const int32_t* logit_row;        /* [N] logits row of output row r (forks share
+                                        one); NULL = r */
+
+    const float* temperature;        /* [N] required */
+    const int32_t* top_k;            /* [N] NULL = -1 */
+    const float* top_p;              /* [N] NULL = 1 */
+    const float* min_p;              /* [N] NULL = 0 */
+    const float* presence_penalty;   /* [N] NULL = 0 */
+    const float* frequency_penalty;  /* [N] NULL = 0 */
+    const float* repetition_penalty; /* [N] NULL = 1 */
+    const uint64_t* seed;            /* [N] per-row seed, read where has_seed[r] != 0 */
+    const uint8_t* has_seed;         /* [N] NULL = no row seeded */
+    const uint32_t* stream_id;       /* [N] Philox stream of row r; NULL: see above */
+
+    /* ragged prior-token history, CSR: ids of row r are
+       hist_ids[hist_offsets[r] .. hist_offsets[r + 1]); NULL = no penalties */
+    const int32_t* hist_offsets;     /* [N + 1] */
+    const int32_t* hist_ids;
+
+    uint64_t global_seed;            /* key of unseeded rows */
+    uint64_t philox_offset;          /* counter words 2-3 ... */
+    const uint64_t* philox_offset_dev; /* ... or read from this device word when non-NULL
+                                          (a CUDA graph replays new offsets this way);
+                                          ignored by sampler_sample_host */
+
+    int32_t* out_tokens;             /* [N] required */
+    float* out_probs;                /* [N * V] row-major, NULL = not materialised */
+    float* out_logprobs;             /* [N * V] row-major, NULL = not materialised */
+    int32_t* out_status;             /* [N] NULL = not reported */
+} sampler_args_t;
+
+/* Create a handle on cfg->device. Returns SAMPLER_OK and sets *out, or a
+ * negative code and sets *out = NULL. Allocates device memory only with
+ * SAMPLER_CREATE_HOST_STAGING. */
+int sampler_create(sampler_t* out, const sampler_config_t* cfg);
+
+/* Enqueue one sampling step on `stream`. All pointers in args are device
+ * pointers on the handle's device. Validates only host-visible scalars and
+ * pointers, allocates nothing, never synchronizes and never reads device
+ * memory on the host; per-row data errors go to out_status. Returns SAMPLER_OK
+ * once the work is enqueued, or a negative code (nothing enqueued). The device
+ * must be current on the calling thread (the call sets it). */
+int sampler_sample(sampler_t h, const sampler_args_t* args, sampler_stream_t stream);
+
+/* The same step from host memory: copies the inputs (n_logit_rows rows of
+ * logits, the per-row arrays, the history) to the handle's staging buffers on
+ * `stream`, samples, copies the outputs back into the host arrays of `args`
+ * and synchronizes `stream` before returning. Needs a handle created with
+ * SAMPLER_CREATE_HOST_STAGING; history length <= cfg.max_history. Pinned host
+ * memory makes the copies asynchronous with respect to other streams. */
+int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_t stream);
+
+/* Release the handle and its device memory. NULL is a no-op. */
+void sampler_destroy(sampler_t h);
+
+/* A static string for a return code or a per-row status code. */
+const char* sampler_status_string(int code);
+
+/* ABI version of this header: (major << 16) | minor. */
+uint32_t sampler_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_STEP_TOKEN_SAMPLER_H */
