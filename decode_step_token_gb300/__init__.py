@@ -1,0 +1,124 @@
+"""GB300-native per-decode-step token sampler.
+
+The sampler itself is the CUDA library ``libsampler.so`` (C ABI in
+``include/sampler.h``); this package is its thin Python binding. ``Sampler``
+wraps a handle and takes torch tensors that already live on the GPU; PyTorch
+provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from . import _binding as abi
+from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_DTYPE_BF16,
+                       SAMPLER_DTYPE_F32, SAMPLER_OK, load_library, sampler_abi_version,
+                       sampler_args_t, sampler_config_t, sampler_create, sampler_destroy,
+                       sampler_sample, sampler_sample_host, sampler_status_string)
+
+__all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
+           "sampler_sample_host", "sampler_destroy", "sampler_status_string",
+           "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
+
+
+class SamplerError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {sampler_status_string(code)} ({code})")
+        self.code = code
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return int(t)
+
+
+class Sampler:
+    """One libsampler handle on a CUDA device.
+
+    ``sample`` takes device tensors: logits ``[rows, >= vocab]`` (bf16 or fp32, unit
+    inner stride) and per-row parameter tensors, and writes the caller's output
+    tensors. It enqueues on torch's current stream (or ``stream``) and returns
+    without synchronising.
+    """
+
+    def __init__(self, max_rows: int, max_vocab: int, device: int = 0, max_history: int = 0,
+                 host_staging: bool = False):
+        cfg = sampler_config_t(device, max_rows, max_vocab, max_history,
+                               SAMPLER_CREATE_HOST_STAGING if host_staging else 0)
+        rc, h = sampler_create(cfg)
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_create")
+        self._h = h
+        self.device = device
+        self.max_rows = max_rows
+        self.max_vocab = max_vocab
+
+    def close(self):
+        if getattr(self, "_h", None):
+            sampler_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @staticmethod
+    def make_args(*, logits, vocab=None, n_rows=None, temperature, dtype=None, top_k=None,
+                  top_p=None, min_p=None, presence_penalty=None, frequency_penalty=None,
+                  repetition_penalty=None, seed=None, has_seed=None, stream_id=None,
+                  logit_row=None, hist_offsets=None, hist_ids=None, global_seed=0,
+                  philox_offset=0, philox_offset_dev=None, out_tokens, out_probs=None,
+                  out_logprobs=None, out_status=None, n_logit_rows=None,
+                  row_stride=None) -> sampler_args_t:
+        if dtype is None:
+            import torch
+            if logits.dtype == torch.bfloat16:
+                dtype = SAMPLER_DTYPE_BF16
+            elif logits.dtype == torch.float32:
+                dtype = SAMPLER_DTYPE_F32
+            else:
+                raise TypeError(f"unsupported logits dtype {logits.dtype}")
+        if row_stride is None:
+            if logits.stride(-1) != 1:
+                raise ValueError("logits rows must be contiguous")
+            row_stride = logits.stride(0) if logits.dim() == 2 else logits.shape[-1]
+        if vocab is None:
+            vocab = logits.shape[-1]
+        if n_rows is None:
+            n_rows = temperature.shape[0]
+        if n_logit_rows is None:
+            n_logit_rows = logits.shape[0] if logits.dim() == 2 else 1
+        return sampler_args_t(
+            _ptr(logits), dtype, n_rows, vocab, row_stride, n_logit_rows, _ptr(logit_row),
+            _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(min_p), _ptr(presence_penalty),
+            _ptr(frequency_penalty), _ptr(repetition_penalty), _ptr(seed), _ptr(has_seed),
+            _ptr(stream_id), _ptr(hist_offsets), _ptr(hist_ids), global_seed, philox_offset,
+            _ptr(philox_offset_dev), _ptr(out_tokens), _ptr(out_probs), _ptr(out_logprobs),
+            _ptr(out_status))
+
+    def sample_args(self, args: sampler_args_t, stream: Optional[int] = None) -> None:
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        rc = sampler_sample(self._h, args, stream)
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_sample")
+
+    def sample(self, stream: Optional[int] = None, **kw) -> None:
+        self.sample_args(self.make_args(**kw), stream)
+
+    def sample_host_args(self, args: sampler_args_t, stream: int = 0) -> None:
+        rc = sampler_sample_host(self._h, args, stream)
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_sample_host")

@@ -1,0 +1,324 @@
+// sampler_api.cu -- the C ABI of libsampler.so (declared in include/sampler.h):
+// argument checks, launch geometry and the cluster launch of the row kernel,
+// plus the host-buffer entry that stages through the handle's device buffers.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "row_sampler_kernel.cuh"
+#include "sampler.h"
+
+namespace {
+
+constexpr int64_t kMaxVocabLimit = 262144;  // a row always fits one cluster's shared memory
+constexpr int kMaxSmem = 227 * 1024;
+
+struct Geometry {
+    int cluster;    // CTAs per row
+    int slice;      // elements per CTA
+    size_t smem;    // dynamic shared memory per CTA
+};
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+Geometry geometry(int64_t V, int esize, bool pen)
+{
+    Geometry g;
+    g.cluster = int(std::min<int64_t>(dst::kMaxCluster, std::max<int64_t>(1, (V + 16383) / 16384)));
+    int64_t l = (V + g.cluster - 1) / g.cluster;
+    l = (l + 7) & ~int64_t(7);
+    g.slice = int(l);
+    g.smem = align16(sizeof(dst::Shared)) + (pen ? align16(size_t(l) * 2 + 4) : 0) +
+             align16(size_t(l) * esize + 32);
+    return g;
+}
+
+template <typename InT, bool kPen>
+void* kernel_ptr()
+{
+    return reinterpret_cast<void*>(&dst::row_sampler_kernel<InT, kPen>);
+}
+
+void* pick_kernel(int dtype, bool pen)
+{
+    if (dtype == SAMPLER_DTYPE_BF16) return pen ? kernel_ptr<uint16_t, true>() : kernel_ptr<uint16_t, false>();
+    return pen ? kernel_ptr<float, true>() : kernel_ptr<float, false>();
+}
+
+int kernel_slot(int dtype, bool pen) { return (dtype == SAMPLER_DTYPE_BF16 ? 2 : 0) + (pen ? 1 : 0); }
+
+}  // namespace
+
+struct sampler_s {
+    int device;
+    int64_t max_rows, max_vocab, max_history;
+    uint32_t flags;
+    size_t smem_set[4];  // dynamic shared memory already granted per kernel variant
+    // staging for sampler_sample_host
+    unsigned char* stage_base;
+    size_t stage_bytes;
+};
+
+namespace {
+
+int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
+{
+    const bool pen = a->hist_offsets != nullptr;
+    const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
+    const Geometry g = geometry(a->vocab, esize, pen);
+    if (g.smem > size_t(kMaxSmem)) return SAMPLER_ERR_TOO_LARGE;
+    void* fn = pick_kernel(a->dtype, pen);
+    const int slot = kernel_slot(a->dtype, pen);
+    if (h->smem_set[slot] < g.smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(g.smem)) !=
+            cudaSuccess)
+            return SAMPLER_ERR_CUDA;
+        h->smem_set[slot] = g.smem;
+    }
+
+    dst::KernelParams p;
+    std::memset(&p, 0, sizeof p);
+    p.logits = a->logits;
+    p.vocab = a->vocab;
+    p.row_stride = a->row_stride;
+    p.n_logit_rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
+    p.logit_row = a->logit_row;
+    p.temperature = a->temperature;
+    p.top_k = a->top_k;
+    p.top_p = a->top_p;
+    p.min_p = a->min_p;
+    p.presence = a->presence_penalty;
+    p.frequency = a->frequency_penalty;
+    p.repetition = a->repetition_penalty;
+    p.seed = a->seed;
+    p.has_seed = a->has_seed;
+    p.stream_id = a->stream_id;
+    p.hist_offsets = a->hist_offsets;
+    p.hist_ids = a->hist_ids;
+    p.global_seed = a->global_seed;
+    p.philox_offset = a->philox_offset;
+    p.philox_offset_dev = a->philox_offset_dev;
+    p.out_tokens = a->out_tokens;
+    p.out_probs = a->out_probs;
+    p.out_logprobs = a->out_logprobs;
+    p.out_status = a->out_status;
+    p.slice_len = g.slice;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(unsigned(a->n_rows * g.cluster), 1, 1);
+    cfg.blockDim = dim3(dst::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(g.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&p};
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
+int check_args(sampler_t h, const sampler_args_t* a)
+{
+    if (!h || !a) return SAMPLER_ERR_NULL_ARG;
+    if (a->n_rows < 0 || a->vocab < 1 || a->row_stride < a->vocab || a->n_logit_rows < 0)
+        return SAMPLER_ERR_BAD_SHAPE;
+    if (a->dtype != SAMPLER_DTYPE_F32 && a->dtype != SAMPLER_DTYPE_BF16) return SAMPLER_ERR_BAD_DTYPE;
+    if (a->n_rows > h->max_rows || a->vocab > h->max_vocab) return SAMPLER_ERR_TOO_LARGE;
+    if (a->n_rows == 0) return SAMPLER_OK;
+    if (!a->logits || !a->temperature || !a->out_tokens) return SAMPLER_ERR_NULL_ARG;
+    if (a->has_seed && !a->seed) return SAMPLER_ERR_NULL_ARG;
+    if (a->hist_offsets && !a->hist_ids) return SAMPLER_ERR_NULL_ARG;
+    return SAMPLER_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t sampler_abi_version(void) { return (1u << 16) | 0u; }
+
+const char* sampler_status_string(int code)
+{
+    switch (code) {
+        case SAMPLER_OK: return "ok";
+        case SAMPLER_ERR_NULL_ARG: return "a required pointer is NULL";
+        case SAMPLER_ERR_BAD_SHAPE: return "bad shape (rows, vocab or row stride)";
+        case SAMPLER_ERR_TOO_LARGE: return "rows or vocab above the handle's limits";
+        case SAMPLER_ERR_BAD_DTYPE: return "unknown logits dtype";
+        case SAMPLER_ERR_CUDA: return "a CUDA call failed";
+        case SAMPLER_ERR_NO_DEVICE: return "no usable sm_103 device";
+        case SAMPLER_ERR_NO_STAGING: return "handle has no host staging buffers";
+        case SAMPLER_ROW_NONFINITE: return "row: NaN or +inf logit";
+        case SAMPLER_ROW_ALL_NEG_INF: return "row: every logit is -inf";
+        case SAMPLER_ROW_BAD_PARAM: return "row: parameter out of range";
+        case SAMPLER_ROW_BAD_HISTORY: return "row: history id out of range or history too long";
+        case SAMPLER_ROW_TIMEOUT: return "row: internal wait gave up";
+        default: return "unknown code";
+    }
+}
+
+int sampler_create(sampler_t* out, const sampler_config_t* cfg)
+{
+    if (!out) return SAMPLER_ERR_NULL_ARG;
+    *out = nullptr;
+    if (!cfg) return SAMPLER_ERR_NULL_ARG;
+    if (cfg->max_rows < 1 || cfg->max_vocab < 1 || cfg->max_vocab > kMaxVocabLimit ||
+        cfg->max_history < 0)
+        return SAMPLER_ERR_BAD_SHAPE;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device < 0 || cfg->device >= ndev)
+        return SAMPLER_ERR_NO_DEVICE;
+    if (cudaSetDevice(cfg->device) != cudaSuccess) return SAMPLER_ERR_NO_DEVICE;
+    // the kernels are built for sm_103a only: make sure the image loads here
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, pick_kernel(SAMPLER_DTYPE_F32, false)) != cudaSuccess) {
+        cudaGetLastError();
+        return SAMPLER_ERR_NO_DEVICE;
+    }
+    sampler_s* h = new (std::nothrow) sampler_s;
+    if (!h) return SAMPLER_ERR_CUDA;
+    std::memset(h, 0, sizeof *h);
+    h->device = cfg->device;
+    h->max_rows = cfg->max_rows;
+    h->max_vocab = cfg->max_vocab;
+    h->max_history = cfg->max_history;
+    h->flags = cfg->flags;
+    if (cfg->flags & SAMPLER_CREATE_HOST_STAGING) {
+        const size_t R = size_t(cfg->max_rows), V = size_t(cfg->max_vocab);
+        size_t bytes = 0;
+        bytes += align16(R * V * 4);          // logits (largest element type)
+        bytes += 2 * align16(R * V * 4);      // probs, logprobs
+        bytes += 16 * align16(R * 8);         // per-row arrays
+        bytes += align16((R + 1) * 4) + align16(size_t(cfg->max_history) * 4 + 4);
+        if (cudaMalloc(&h->stage_base, bytes) != cudaSuccess) {
+            delete h;
+            return SAMPLER_ERR_CUDA;
+        }
+        h->stage_bytes = bytes;
+    }
+    *out = h;
+    return SAMPLER_OK;
+}
+
+void sampler_destroy(sampler_t h)
+{
+    if (!h) return;
+    if (h->stage_base) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        cudaSetDevice(h->device);
+        cudaFree(h->stage_base);
+        if (cur >= 0) cudaSetDevice(cur);
+    }
+    delete h;
+}
+
+int sampler_sample(sampler_t h, const sampler_args_t* a, sampler_stream_t stream)
+{
+    int rc = check_args(h, a);
+    if (rc != SAMPLER_OK || a->n_rows == 0) return rc;
+    if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return launch(h, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sampler_sample_host(sampler_t h, const sampler_args_t* a, sampler_stream_t stream_)
+{
+    int rc = check_args(h, a);
+    if (rc != SAMPLER_OK || a->n_rows == 0) return rc;
+    if (!h->stage_base) return SAMPLER_ERR_NO_STAGING;
+    const int64_t N = a->n_rows, V = a->vocab;
+    const int64_t NL = a->n_logit_rows > 0 ? a->n_logit_rows : N;
+    if (NL > h->max_rows) return SAMPLER_ERR_TOO_LARGE;
+    int64_t hist_len = 0;
+    if (a->hist_offsets) {
+        hist_len = a->hist_offsets[N];
+        if (hist_len < 0 || hist_len > h->max_history) return SAMPLER_ERR_TOO_LARGE;
+    }
+    if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
+    const size_t R = size_t(h->max_rows), VM = size_t(h->max_vocab);
+    const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
+
+    unsigned char* cur = h->stage_base;
+    auto take = [&](size_t bytes) {
+        unsigned char* p = cur;
+        cur += align16(bytes);
+        return p;
+    };
+    unsigned char* d_logits = take(R * VM * 4);
+    float* d_probs = reinterpret_cast<float*>(take(R * VM * 4));
+    float* d_logprobs = reinterpret_cast<float*>(take(R * VM * 4));
+    sampler_args_t d = *a;
+    bool fail = false;
+    auto put = [&](const void* src, size_t elem) -> void* {
+        unsigned char* p = take(R * 8);
+        if (src && cudaMemcpyAsync(p, src, size_t(N) * elem, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            fail = true;
+        return src ? p : nullptr;
+    };
+    // logits: compact NL rows of V elements
+    if (cudaMemcpy2DAsync(d_logits, size_t(V) * esize, a->logits, size_t(a->row_stride) * esize,
+                          size_t(V) * esize, size_t(NL), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        fail = true;
+    d.logits = d_logits;
+    d.row_stride = V;
+    d.n_logit_rows = NL;
+    d.logit_row = static_cast<const int32_t*>(put(a->logit_row, 4));
+    d.temperature = static_cast<const float*>(put(a->temperature, 4));
+    d.top_k = static_cast<const int32_t*>(put(a->top_k, 4));
+    d.top_p = static_cast<const float*>(put(a->top_p, 4));
+    d.min_p = static_cast<const float*>(put(a->min_p, 4));
+    d.presence_penalty = static_cast<const float*>(put(a->presence_penalty, 4));
+    d.frequency_penalty = static_cast<const float*>(put(a->frequency_penalty, 4));
+    d.repetition_penalty = static_cast<const float*>(put(a->repetition_penalty, 4));
+    d.seed = static_cast<const uint64_t*>(put(a->seed, 8));
+    d.has_seed = static_cast<const uint8_t*>(put(a->has_seed, 1));
+    d.stream_id = static_cast<const uint32_t*>(put(a->stream_id, 4));
+    int32_t* d_tokens = static_cast<int32_t*>(static_cast<void*>(take(R * 8)));
+    int32_t* d_status = static_cast<int32_t*>(static_cast<void*>(take(R * 8)));
+    d.out_tokens = d_tokens;
+    d.out_status = a->out_status ? d_status : nullptr;
+    d.out_probs = a->out_probs ? d_probs : nullptr;
+    d.out_logprobs = a->out_logprobs ? d_logprobs : nullptr;
+    d.philox_offset_dev = nullptr;
+    unsigned char* d_hoff = take((R + 1) * 4);
+    unsigned char* d_hids = take(size_t(h->max_history) * 4 + 4);
+    if (a->hist_offsets) {
+        if (cudaMemcpyAsync(d_hoff, a->hist_offsets, size_t(N + 1) * 4, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess)
+            fail = true;
+        if (hist_len > 0 &&
+            cudaMemcpyAsync(d_hids, a->hist_ids, size_t(hist_len) * 4, cudaMemcpyHostToDevice, st) !=
+                cudaSuccess)
+            fail = true;
+        d.hist_offsets = reinterpret_cast<const int32_t*>(d_hoff);
+        d.hist_ids = reinterpret_cast<const int32_t*>(d_hids);
+    }
+    if (fail) return SAMPLER_ERR_CUDA;
+    rc = launch(h, &d, st);
+    if (rc != SAMPLER_OK) return rc;
+    if (cudaMemcpyAsync(a->out_tokens, d_tokens, size_t(N) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    if (a->out_status &&
+        cudaMemcpyAsync(a->out_status, d_status, size_t(N) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    if (a->out_probs && cudaMemcpyAsync(a->out_probs, d_probs, size_t(N * V) * 4,
+                                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    if (a->out_logprobs && cudaMemcpyAsync(a->out_logprobs, d_logprobs, size_t(N * V) * 4,
+                                           cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+"""The C ABI library builds, loads and exports what include/sampler.h declares (no GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sampler.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_step_token_gb300 import build
+    build.build_library()
+    import decode_step_token_gb300 as d
+    return d.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sampler_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ("sampler_create", "sampler_sample", "sampler_destroy", "sampler_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (sampler_\w+)", out.stdout))
+    assert set(declared_functions()) <= exported
+
+
+def test_python_binding_uses_the_abi_names(lib):
+    import decode_step_token_gb300 as d
+    assert set(d.EXPORTED) == set(declared_functions())
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    import decode_step_token_gb300 as d
+    src = tmp_path / "layout.c"
+    fields_a = [f[0] for f in d.sampler_args_t._fields_]
+    fields_c = [f[0] for f in d.sampler_config_t._fields_]
+    body = ['#include <stdio.h>', '#include <stddef.h>', '#include "sampler.h"', "int main(void){"]
+    body.append('printf("%zu %zu\\n", sizeof(sampler_args_t), sizeof(sampler_config_t));')
+    for f in fields_a:
+        body.append(f'printf("%zu\\n", offsetof(sampler_args_t, {f}));')
+    for f in fields_c:
+        body.append(f'printf("%zu\\n", offsetof(sampler_config_t, {f}));')
+    body.append("return 0;}")
+    src.write_text("\n".join(body))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", f"-I{os.path.dirname(HEADER)}", str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(d.sampler_args_t)
+    assert vals[1] == ctypes.sizeof(d.sampler_config_t)
+    offs = vals[2:]
+    for f, o in zip(fields_a, offs[:len(fields_a)]):
+        assert getattr(d.sampler_args_t, f).offset == o, f
+    for f, o in zip(fields_c, offs[len(fields_a):]):
+        assert getattr(d.sampler_config_t, f).offset == o, f
+
+
+def test_host_checks_without_a_gpu(lib):
+    import decode_step_token_gb300 as d
+    assert d.sampler_abi_version() >> 16 == 1
+    assert "limits" in d.sampler_status_string(-3)
+    # NULL handle / NULL config are rejected before any CUDA call
+    rc, h = d.sampler_create(d.sampler_config_t(0, 0, 10, 0, 0))
+    assert rc == d._binding.SAMPLER_ERR_BAD_SHAPE and not h.value
+    assert lib.sampler_sample(None, None, None) == d._binding.SAMPLER_ERR_NULL_ARG
+    d.sampler_destroy(None)
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "decode_step_token_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower().replace("oracle-free", ""), f

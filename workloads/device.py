@@ -1,0 +1,100 @@
+"""Move a ``SamplerBatch`` to the GPU and run it through the library's Python binding.
+
+Marshalling only (numpy -> torch device tensors -> ``Sampler.sample``); no
+sampler arithmetic lives here.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+
+def to_device(batch, device="cuda:0", want_probs: Optional[bool] = None, copies: int = 1,
+              logits_offset_elems: int = 0):
+    """Device tensors for `batch`; `copies` distinct logits buffers (for rotating past L2);
+    `logits_offset_elems` shifts the logits start (to exercise unaligned rows)."""
+    import torch
+
+    want = batch.want_probs if want_probs is None else want_probs
+    dev = torch.device(device)
+
+    def t(a, dt=None):
+        if a is None:
+            return None
+        arr = np.ascontiguousarray(a)
+        if arr.dtype == np.uint64:
+            arr = arr.view(np.int64)
+        x = torch.from_numpy(arr)
+        return x.to(dev) if dt is None else x.to(dev).view(dt)
+
+    if batch.dtype == "bf16":
+        host = torch.from_numpy(np.ascontiguousarray(batch.logits).view(np.int16)).view(torch.bfloat16)
+    else:
+        host = torch.from_numpy(np.ascontiguousarray(batch.logits))
+    logits = []
+    for _ in range(copies):
+        if logits_offset_elems:
+            flat = torch.empty(host.numel() + logits_offset_elems, dtype=host.dtype, device=dev)
+            view = flat[logits_offset_elems:].view(host.shape)
+            view.copy_(host)
+            logits.append(view)
+        else:
+            logits.append(host.to(dev))
+    N, V = batch.n_rows, batch.vocab
+    d = {
+        "logits": logits,
+        "temperature": t(batch.temperature),
+        "top_k": t(batch.top_k),
+        "top_p": t(batch.top_p),
+        "min_p": t(batch.min_p),
+        "presence_penalty": t(batch.presence),
+        "frequency_penalty": t(batch.frequency),
+        "repetition_penalty": t(batch.repetition),
+        "seed": t(batch.seed),
+        "has_seed": t(batch.has_seed),
+        "stream_id": t(batch.stream_id.view(np.int32) if batch.stream_id is not None else None),
+        "logit_row": t(batch.logit_row),
+        "hist_offsets": t(batch.hist_offsets),
+        "hist_ids": t(batch.hist_ids),
+        "out_tokens": torch.full((N,), -7, dtype=torch.int32, device=dev),
+        "out_status": torch.full((N,), -7, dtype=torch.int32, device=dev),
+        "out_probs": torch.empty((N, V), dtype=torch.float32, device=dev) if want else None,
+        "out_logprobs": torch.empty((N, V), dtype=torch.float32, device=dev) if want else None,
+    }
+    return d
+
+
+def sample_args(sampler, batch, d, copy_index: int = 0, philox_offset: Optional[int] = None,
+                philox_offset_dev=None):
+    """The ctypes argument block for one call on device buffers `d`."""
+    return sampler.make_args(
+        logits=d["logits"][copy_index], vocab=batch.vocab, n_rows=batch.n_rows,
+        row_stride=batch.row_stride, n_logit_rows=batch.n_logit_rows,
+        temperature=d["temperature"], top_k=d["top_k"], top_p=d["top_p"], min_p=d["min_p"],
+        presence_penalty=d["presence_penalty"], frequency_penalty=d["frequency_penalty"],
+        repetition_penalty=d["repetition_penalty"], seed=d["seed"], has_seed=d["has_seed"],
+        stream_id=d["stream_id"], logit_row=d["logit_row"], hist_offsets=d["hist_offsets"],
+        hist_ids=d["hist_ids"], global_seed=batch.global_seed,
+        philox_offset=batch.philox_offset if philox_offset is None else philox_offset,
+        philox_offset_dev=philox_offset_dev,
+        out_tokens=d["out_tokens"], out_probs=d["out_probs"], out_logprobs=d["out_logprobs"],
+        out_status=d["out_status"])
+
+
+class GpuResult:
+    def __init__(self, tokens, status, probs, logprobs):
+        self.tokens, self.status, self.probs, self.logprobs = tokens, status, probs, logprobs
+
+
+def run(sampler, batch, want_probs: Optional[bool] = None, device="cuda:0",
+        logits_offset_elems: int = 0) -> GpuResult:
+    """One synchronous call; results back on the host as numpy."""
+    import torch
+
+    d = to_device(batch, device, want_probs, logits_offset_elems=logits_offset_elems)
+    sampler.sample_args(sample_args(sampler, batch, d))
+    torch.cuda.synchronize()
+    get = lambda x: None if x is None else x.cpu().numpy()
+    return GpuResult(get(d["out_tokens"]), get(d["out_status"]), get(d["out_probs"]),
+                     get(d["out_logprobs"]))
