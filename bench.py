@@ -228,6 +228,7 @@ def run_ours(args):
     arg_blocks = [wdev.sample_args(sampler, batch, d, copy_index=i) for i in range(copies)]
 
     stream = torch.cuda.Stream(device=dev)
+    sampler.stat(0, reset=True)
     with torch.cuda.stream(stream):
         for i in range(copies):  # first launches outside capture set kernel attributes
             sampler.sample_args(arg_blocks[i], stream.cuda_stream)
@@ -272,9 +273,9 @@ def run_ours(args):
     ms_step = ms / steps
     value = world * batch.n_rows * steps / (ms / 1e3)
 
+    exact_rows = sampler.stat(0, reset=True)
     if rank != 0:
         return
-    # parity spot check of the timed configuration (not timed)
     tokens = d["out_tokens"].cpu().numpy()
 
     # e2e through the host-buffer entry point
@@ -309,6 +310,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": steps,
+        "exact_path_rows_per_step": exact_rows / (steps + (reps_w + 1) * copies),
         "clocks": clk,
         "kernel_hash": kernel_hash(),
         "first_tokens": tokens[:8].tolist(),

@@ -14,7 +14,8 @@ from . import _binding as abi
 from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_DTYPE_BF16,
                        SAMPLER_DTYPE_F32, SAMPLER_OK, load_library, sampler_abi_version,
                        sampler_args_t, sampler_config_t, sampler_create, sampler_destroy,
-                       sampler_sample, sampler_sample_host, sampler_status_string)
+                       sampler_sample, sampler_sample_host, sampler_status_string,
+                       sampler_get_stat)
 
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
            "sampler_sample_host", "sampler_destroy", "sampler_status_string",
@@ -117,6 +118,13 @@ class Sampler:
 
     def sample(self, stream: Optional[int] = None, **kw) -> None:
         self.sample_args(self.make_args(**kw), stream)
+
+    def stat(self, which: int = 0, reset: bool = False) -> int:
+        """A device diagnostic counter (synchronizes the device)."""
+        rc, v = sampler_get_stat(self._h, which, reset)
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_get_stat")
+        return v
 
     def sample_host_args(self, args: sampler_args_t, stream: int = 0) -> None:
         rc = sampler_sample_host(self._h, args, stream)

@@ -34,7 +34,8 @@ SAMPLER_ROW_TIMEOUT = 5
 SAMPLER_CREATE_HOST_STAGING = 1
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
-            "sampler_status_string", "sampler_abi_version")
+            "sampler_status_string", "sampler_abi_version", "sampler_get_stat")
+SAMPLER_STAT_EXACT_ROWS = 0
 
 
 class sampler_config_t(ctypes.Structure):
@@ -104,6 +105,9 @@ def load_library(path: str = LIB):
             lib.sampler_destroy.restype = None
             lib.sampler_status_string.argtypes = [ctypes.c_int]
             lib.sampler_status_string.restype = ctypes.c_char_p
+            lib.sampler_get_stat.argtypes = [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64),
+                                             ctypes.c_int]
+            lib.sampler_get_stat.restype = ctypes.c_int
             lib.sampler_abi_version.argtypes = []
             lib.sampler_abi_version.restype = ctypes.c_uint32
             _lib = lib
@@ -135,3 +139,10 @@ def sampler_status_string(code: int) -> str:
 
 def sampler_abi_version() -> int:
     return int(load_library().sampler_abi_version())
+
+
+def sampler_get_stat(h, which: int, reset: bool = False):
+    """Returns (code, value)."""
+    v = ctypes.c_uint64(0)
+    rc = load_library().sampler_get_stat(h, which, ctypes.byref(v), 1 if reset else 0)
+    return rc, int(v.value)

@@ -1,0 +1,390 @@
+// colsplit.cuh -- the column-split sampler kernel for small batches (sm_103a).
+//
+// Every CTA (one per SM, 512 threads) owns one vocabulary slice of EVERY row, so
+// each SM gets the same share of each row's work whatever the per-row mix of
+// greedy / plain-temperature / truncated rows is. A CTA stages its slices of all
+// rows into shared memory with one bulk (TMA-engine) copy per row, issued at
+// launch, so the whole batch is in flight at once. Each warp owns a
+// cost-balanced set of rows; for each (row, slice) it writes a small summary
+// record to global memory and bumps the row's arrival counter. The warp that
+// brings a counter to the slice count finishes that row from the records:
+//
+//   greedy rows     argmax of the per-slice maxima (lowest index on ties)
+//   plain rows      the best two Gumbel scores of every slice, settled in double
+//   truncated rows  per-slice top-8 candidates merged into the row's top list;
+//                   top-k / top-p / min-p cut in double, Gumbel-max over the cut
+//
+// A truncated row whose kept set reaches below what the candidates cover is
+// finished exactly by its finishing CTA, streaming the row from global memory
+// (radix select by count or fixed-point softmax mass, then a Gumbel pass). The
+// finishing warp resets the row's counter, so the workspace is clean for the
+// next launch. Nothing waits on another CTA: no co-residency is assumed.
+#pragma once
+
+#include "row_sampler.cuh"
+
+namespace dst {
+namespace col {
+
+constexpr int kT = 512;
+constexpr int kW = kT / 32;
+constexpr int kSliceCand = 8;
+constexpr int kMaxRows = 256;
+constexpr int kListCap = 256;  // finisher merge list per warp
+constexpr int kKeepCap = 64;   // kept tokens resolved by a finishing warp
+constexpr uint32_t kOverflow = 0xFFFFFFFFu;
+constexpr int kMaxGc = 256;                 // slices per row (CTAs of the grid)
+constexpr int kMaxGcPerLane = kMaxGc / 32;
+
+enum : uint8_t { kClsErr = 0, kClsGreedy = 1, kClsPlain = 2, kClsCand = 3 };
+
+struct alignas(16) ColRec {  // one (row, slice) summary
+    float mx;
+    int32_t amax;
+    uint32_t flags;
+    uint32_t nc;  // candidates submitted, kOverflow if the slice could not bound them
+    GRec g0, g1;
+    unsigned long long cand[kSliceCand];
+    float zs;     // sum of exp((x - mx) / T) over the slice (compensated)
+    float zc;     // its compensation term
+    float pad0, pad1;
+};
+
+struct ColParams {
+    KernelParams k;
+    int32_t n_rows;
+    int32_t gc;         // slices per row (= grid size)
+    int32_t w;          // elements per slice (multiple of 8)
+    int32_t row_bytes;  // staged bytes per row (multiple of 16)
+    ColRec* rec;        // [n_rows][gc]
+    uint32_t* counters; // [n_rows], zero between launches
+    unsigned long long* stats;  // [0] rows finished by the exact path (diagnostic)
+};
+
+struct alignas(16) RowInfo {
+    float T, Te, invT, p, minp;
+    int32_t k;
+    uint32_t stream, key_lo, key_hi, off_lo, off_hi;
+    int32_t lrow;
+    int32_t status;
+    int32_t hb;          // staged head pad in bytes
+    int32_t head_end;    // elements before the aligned interior
+    int32_t tail_begin;  // first element after it
+    uint8_t cls, do_topk, do_topp, do_minp;
+    uint8_t need_z, small_k, greedy, pad;
+};
+
+struct alignas(16) ColShared {
+    uint64_t mbar[kMaxRows];
+    RowInfo info[kMaxRows];
+    int16_t order[kMaxRows];      // rows in processing order
+    int16_t warp_of[kMaxRows];
+    int32_t cls_count[4];
+    int32_t fallback_rows[kMaxRows];
+    float fb_m[kMaxRows];
+    int32_t fb_amax[kMaxRows];
+    int32_t n_fallback;
+    int32_t pad;
+    unsigned long long buf[kW][kListCap];  // per-warp scratch
+    // CTA-wide scratch for the exact fallback
+    uint32_t hcnt[256];
+    unsigned long long hmass[256];
+    unsigned long long scan_w[kW];
+    int32_t red_i[kW];
+    float red_f[kW];
+    GTop2 red_g[kW];
+    unsigned long long sel_prefix;  // packed state of the fallback select
+    unsigned long long sel_wabove;
+    unsigned long long sel_target;
+    int32_t sel_idx;
+    int32_t sel_found;
+};
+
+__device__ __forceinline__ RowParams as_row_params(const RowInfo& ri)
+{
+    RowParams rp;
+    rp.T = ri.T;
+    rp.Te = ri.Te;
+    rp.invT = ri.invT;
+    rp.k = ri.k;
+    rp.p = ri.p;
+    rp.minp = ri.minp;
+    rp.pres = 0.0f;
+    rp.freq = 0.0f;
+    rp.rep = 1.0f;
+    rp.lrow = ri.lrow;
+    rp.hlo = rp.hhi = 0;
+    rp.stream = ri.stream;
+    rp.status = ri.status;
+    rp.greedy = ri.greedy;
+    rp.do_topk = ri.do_topk;
+    rp.do_topp = ri.do_topp;
+    rp.do_minp = ri.do_minp;
+    rp.want_out = 0;
+    rp.has_hist = 0;
+    rp.plain_single = ri.cls == kClsPlain;
+    rp.key_lo = ri.key_lo;
+    rp.key_hi = ri.key_hi;
+    rp.off_lo = ri.off_lo;
+    rp.off_hi = ri.off_hi;
+    return rp;
+}
+
+// Composite sort word of an fp32 value and its token.
+__device__ __forceinline__ unsigned long long comp_of(float x, int v) { return cand_word(f2key(x), v); }
+
+// ---------------------------------------------------------------- warp helpers
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+// Sort 64 words held two per lane (lane holds items lane and lane + 32) descending:
+// a bitonic network over the 64 positions using shuffles.
+__device__ __forceinline__ void warp_sort64_desc(unsigned long long& a, unsigned long long& b)
+{
+    const int lane = threadIdx.x & 31;
+    // position of a: lane, of b: lane + 32
+    for (int size = 2; size <= 64; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride == 32) {
+                // partner of position p is p ^ 32: a <-> b of the same lane
+                const bool desc = true;  // size == 64 here
+                if ((a < b) == desc) {
+                    const unsigned long long t = a;
+                    a = b;
+                    b = t;
+                }
+            } else {
+                const unsigned long long pa = __shfl_xor_sync(0xffffffffu, a, stride);
+                const unsigned long long pb = __shfl_xor_sync(0xffffffffu, b, stride);
+                const int posA = lane, posB = lane + 32;
+                const bool lowA = (posA & stride) == 0, lowB = (posB & stride) == 0;
+                const bool descA = (posA & size) == 0, descB = (posB & size) == 0;
+                // the lower position keeps the larger value when sorting descending
+                const bool keepMaxA = (lowA == descA);
+                const bool keepMaxB = (lowB == descB);
+                a = keepMaxA ? (a > pa ? a : pa) : (a < pa ? a : pa);
+                b = keepMaxB ? (b > pb ? b : pb) : (b < pb ? b : pb);
+            }
+        }
+    }
+}
+
+// Sort n <= kListCap words in warp-private shared memory, descending (bitonic).
+__device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n)
+{
+    const int lane = threadIdx.x & 31;
+    int np2 = 1;
+    while (np2 < n) np2 <<= 1;
+    for (int i = n + lane; i < np2; i += 32) a[i] = 0ull;
+    __syncwarp();
+    for (int size = 2; size <= np2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = lane; t < (np2 >> 1); t += 32) {
+                const int lo = 2 * stride * (t / stride) + (t % stride);
+                const int hi = lo + stride;
+                const bool desc = (lo & size) == 0;
+                const unsigned long long x = a[lo], y = a[hi];
+                if ((x < y) == desc) {
+                    a[lo] = y;
+                    a[hi] = x;
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
+}  // namespace col
+}  // namespace dst
+
+namespace dst {
+namespace col {
+
+// ---------------------------------------------------------------- CTA-wide helpers (fallback)
+__device__ __forceinline__ unsigned long long cta_suffix_scan(unsigned long long v, ColShared& sh)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned long long s = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_down_sync(0xffffffffu, s, off);
+        if (lane + off < 32) s += o;
+    }
+    if (lane == 0) sh.scan_w[wid] = s;
+    __syncthreads();
+    unsigned long long later = 0;
+    for (int w = wid + 1; w < kW; ++w) later += sh.scan_w[w];
+    __syncthreads();
+    return s + later;
+}
+
+__device__ __forceinline__ int cta_excl_scan(int v, int& total, ColShared& sh)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int s = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += o;
+    }
+    if (lane == 31) sh.red_i[wid] = s;
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w = 0; w < kW; ++w) {
+        if (w < wid) before += sh.red_i[w];
+        tot += sh.red_i[w];
+    }
+    __syncthreads();
+    total = tot;
+    return before + s - v;
+}
+
+template <typename InT>
+__device__ __forceinline__ float row_x(const KernelParams& kp, int lrow, int v)
+{
+    return ElemTraits<InT>::load(kp.logits, int64_t(lrow) * kp.row_stride + v);
+}
+
+// Exact kept-prefix selection over a whole row, streamed from global memory by
+// one CTA: the first token whose inclusive weight (count, or fixed-point mass)
+// reaches `target` closes the prefix. Tokens outside the domain prefix weigh 0.
+template <typename InT>
+__device__ void cta_select(ColShared& sh, const KernelParams& kp, const RowInfo& ri, int V,
+                           bool mass_mode, bool dom, uint32_t dkey, int didx, float m,
+                           unsigned long long count_target, uint32_t& out_key, int& out_idx)
+{
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        sh.sel_prefix = 0;
+        sh.sel_wabove = 0;
+        sh.sel_target = count_target;
+    }
+    __syncthreads();
+    uint32_t pbits = 0;
+    unsigned long long tie_J = 1;
+    for (int level = 0; level < 4; ++level) {
+        for (int i = tid; i < 256; i += kT) {
+            sh.hcnt[i] = 0;
+            sh.hmass[i] = 0;
+        }
+        __syncthreads();
+        const uint32_t prefix = uint32_t(sh.sel_prefix);
+        const int shift = 24 - 8 * level;
+        for (int v = tid; v < V; v += kT) {
+            const float x = row_x<InT>(kp, ri.lrow, v);
+            const uint32_t key = f2key(x);
+            if (dom && !in_prefix(key, v, dkey, didx)) continue;
+            if (pbits && (key >> (32 - pbits)) != prefix) continue;
+            const uint32_t d = (key >> shift) & 255u;
+            atomicAdd(&sh.hcnt[d], 1u);
+            if (mass_mode) atomicAdd(&sh.hmass[d], mass_q(x, m, ri.invT));
+        }
+        __syncthreads();
+        const int d = tid < 256 ? tid : 0;
+        const unsigned long long wgt = tid < 256 ? (mass_mode ? sh.hmass[d] : (unsigned long long)sh.hcnt[d]) : 0ull;
+        const unsigned long long incl = cta_suffix_scan(wgt, sh);
+        if (tid == 0 && mass_mode && level == 0) {
+            unsigned long long t = (unsigned long long)ceil(double(ri.p) * double(incl));
+            sh.sel_target = t < 1 ? 1 : t;
+        }
+        __syncthreads();
+        const unsigned long long target = sh.sel_target, wa = sh.sel_wabove;
+        __syncthreads();
+        if (tid < 256 && wgt > 0 && wa + incl >= target && wa + (incl - wgt) < target) {
+            sh.sel_prefix = (unsigned long long)((prefix << 8) | uint32_t(d));
+            sh.sel_wabove = wa + (incl - wgt);
+        }
+        __syncthreads();
+        pbits += 8;
+    }
+    const uint32_t K = uint32_t(sh.sel_prefix);
+    {
+        const unsigned long long wt = mass_mode ? mass_q(key2f(K), m, ri.invT) : 1ull;
+        tie_J = (sh.sel_target - sh.sel_wabove + wt - 1) / wt;
+    }
+    // the tie_J-th token (index order) holding key K
+    int base = 0;
+    int found = -1;
+    for (int v0 = 0; v0 < V; v0 += kT) {
+        const int v = v0 + tid;
+        int c = 0;
+        if (v < V) {
+            const float x = row_x<InT>(kp, ri.lrow, v);
+            const uint32_t key = f2key(x);
+            c = (key == K && (!dom || in_prefix(key, v, dkey, didx))) ? 1 : 0;
+        }
+        int total = 0;
+        const int excl = cta_excl_scan(c, total, sh);
+        if (c && (unsigned long long)(base + excl + 1) == tie_J) sh.sel_idx = v;
+        base += total;
+        if ((unsigned long long)base >= tie_J) break;
+    }
+    __syncthreads();
+    (void)found;
+    out_key = K;
+    out_idx = sh.sel_idx;
+    __syncthreads();
+}
+
+// Exact finish of one row by the whole CTA (rows the candidates could not settle).
+template <typename InT>
+__device__ void cta_exact_row(ColShared& sh, const ColParams& P, int r, float m, int amax)
+{
+    const KernelParams& kp = P.k;
+    const RowInfo ri = sh.info[r];
+    const int V = int(kp.vocab);
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t bk = 0;
+    int bi = 0;
+    bool hb = false;
+    if (ri.do_topk) {
+        cta_select<InT>(sh, kp, ri, V, false, false, 0u, 0, m, (unsigned long long)ri.k, bk, bi);
+        hb = true;
+    }
+    if (ri.do_topp) {
+        cta_select<InT>(sh, kp, ri, V, true, hb, bk, bi, m, 0ull, bk, bi);
+        hb = true;
+    }
+    float xthr = -INFINITY;
+    if (ri.do_minp) {
+        const double th = double(m) + double(ri.Te) * log(double(ri.minp));
+        float f = float(th);
+        if (double(f) < th) f = nextafterf(f, INFINITY);
+        xthr = f;
+    }
+    const RowParams rp = as_row_params(ri);
+    GumbelAcc g;
+    gumbel_init(g);
+    for (int v = tid; v < V; v += kT) {
+        const float x = row_x<InT>(kp, ri.lrow, v);
+        if (!(x > -INFINITY)) continue;
+        if (hb && !in_prefix(f2key(x), v, bk, bi)) continue;
+        if (ri.do_minp && !(x >= xthr)) continue;
+        gumbel_visit(g, rp, v, x);
+    }
+    top2_warp_reduce(g.t);
+    if (lane == 0) sh.red_g[wid] = g.t;
+    __syncthreads();
+    if (tid == 0) {
+        GTop2 t;
+        t.a = grec_empty();
+        t.b = grec_empty();
+        for (int w = 0; w < kW; ++w) {
+            top2_insert(t, sh.red_g[w].a);
+            top2_insert(t, sh.red_g[w].b);
+        }
+        kp.out_tokens[r] = ri.greedy ? amax : settle_top2(t, ri.T);
+        if (kp.out_status) kp.out_status[r] = kRowOk;
+    }
+    __syncthreads();
+}
+
+}  // namespace col
+}  // namespace dst

@@ -155,4 +155,26 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), tracked per thread.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
+// arrival is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Plain arrival (release semantics) on `bar`.
+__device__ __forceinline__ void mbar_arrive_release(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
 }  // namespace dst

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <new>
 
+#include "colsplit_kernel.cuh"
 #include "row_sampler_kernel.cuh"
 #include "sampler.h"
 
@@ -16,6 +17,7 @@ namespace {
 
 constexpr int64_t kMaxVocabLimit = 262144;  // a row always fits one cluster's shared memory
 constexpr int kMaxSmem = 227 * 1024;
+constexpr int kNumStats = 4;
 
 struct Geometry {
     int cluster;    // CTAs per row
@@ -55,9 +57,16 @@ int kernel_slot(int dtype, bool pen) { return (dtype == SAMPLER_DTYPE_BF16 ? 2 :
 
 struct sampler_s {
     int device;
+    int num_sms;
     int64_t max_rows, max_vocab, max_history;
     uint32_t flags;
     size_t smem_set[4];  // dynamic shared memory already granted per kernel variant
+    size_t col_smem_set[2];
+    // workspace of the column-split path: per-(row, slice) records and row counters
+    dst::col::ColRec* col_rec;
+    uint32_t* col_counters;
+    unsigned long long* stats;  // device counters (diagnostics)
+    int col_rows;
     // staging for sampler_sample_host
     unsigned char* stage_base;
     size_t stage_bytes;
@@ -65,8 +74,17 @@ struct sampler_s {
 
 namespace {
 
+struct ColGeometry {
+    int gc, w, row_bytes;  // slices per row, elements per slice, staged bytes per row
+    size_t smem;
+};
+bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g);
+int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream);
+
 int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
 {
+    ColGeometry cg;
+    if (col_eligible(h, a, &cg)) return launch_col(h, a, cg, stream);
     const bool pen = a->hist_offsets != nullptr;
     const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
     const Geometry g = geometry(a->vocab, esize, pen);
@@ -126,6 +144,76 @@ int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
     return SAMPLER_OK;
 }
 
+ColGeometry col_geometry(int64_t N, int64_t V, int esize, int sms)
+{
+    ColGeometry g;
+    int64_t w = (V + sms - 1) / sms;
+    w = std::max<int64_t>(512, (w + 7) & ~int64_t(7));
+    g.w = int(w);
+    g.gc = int((V + w - 1) / w);
+    g.row_bytes = int(align16(size_t(w) * esize + 32));
+    g.smem = ((sizeof(dst::col::ColShared) + 127) & ~size_t(127)) + size_t(N) * g.row_bytes;
+    return g;
+}
+
+// The column-split kernel serves small batches without penalties or outputs.
+bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g)
+{
+    if (!h->col_rec || a->n_rows > h->col_rows) return false;
+    if (a->hist_offsets || a->out_probs || a->out_logprobs) return false;
+    const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
+    *g = col_geometry(a->n_rows, a->vocab, esize, h->num_sms);
+    return g->smem <= size_t(kMaxSmem) && g->gc <= h->num_sms && g->gc <= dst::col::kMaxGc;
+}
+
+int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream)
+{
+    void* fn = a->dtype == SAMPLER_DTYPE_BF16
+                   ? reinterpret_cast<void*>(&dst::col::colsplit_kernel<uint16_t>)
+                   : reinterpret_cast<void*>(&dst::col::colsplit_kernel<float>);
+    const int slot = a->dtype == SAMPLER_DTYPE_BF16 ? 1 : 0;
+    if (h->col_smem_set[slot] < g.smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(g.smem)) !=
+            cudaSuccess)
+            return SAMPLER_ERR_CUDA;
+        h->col_smem_set[slot] = g.smem;
+    }
+    dst::col::ColParams p;
+    std::memset(&p, 0, sizeof p);
+    dst::KernelParams& k = p.k;
+    k.logits = a->logits;
+    k.vocab = a->vocab;
+    k.row_stride = a->row_stride;
+    k.n_logit_rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
+    k.logit_row = a->logit_row;
+    k.temperature = a->temperature;
+    k.top_k = a->top_k;
+    k.top_p = a->top_p;
+    k.min_p = a->min_p;
+    k.presence = a->presence_penalty;
+    k.frequency = a->frequency_penalty;
+    k.repetition = a->repetition_penalty;
+    k.seed = a->seed;
+    k.has_seed = a->has_seed;
+    k.stream_id = a->stream_id;
+    k.global_seed = a->global_seed;
+    k.philox_offset = a->philox_offset;
+    k.philox_offset_dev = a->philox_offset_dev;
+    k.out_tokens = a->out_tokens;
+    k.out_status = a->out_status;
+    p.n_rows = int(a->n_rows);
+    p.gc = g.gc;
+    p.w = g.w;
+    p.row_bytes = g.row_bytes;
+    p.rec = h->col_rec;
+    p.counters = h->col_counters;
+    p.stats = h->stats;
+    void* args[] = {&p};
+    if (cudaLaunchKernel(fn, dim3(g.gc), dim3(dst::col::kT), args, g.smem, stream) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
 int check_args(sampler_t h, const sampler_args_t* a)
 {
     if (!h || !a) return SAMPLER_ERR_NULL_ARG;
@@ -145,6 +233,19 @@ int check_args(sampler_t h, const sampler_args_t* a)
 extern "C" {
 
 uint32_t sampler_abi_version(void) { return (1u << 16) | 0u; }
+
+int sampler_get_stat(sampler_t h, int which, uint64_t* value, int reset)
+{
+    if (!h || !value) return SAMPLER_ERR_NULL_ARG;
+    if (which < 0 || which >= kNumStats) return SAMPLER_ERR_BAD_SHAPE;
+    if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    unsigned long long v = 0;
+    if (cudaMemcpy(&v, h->stats + which, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    if (reset && cudaMemset(h->stats + which, 0, sizeof v) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    *value = v;
+    return SAMPLER_OK;
+}
 
 const char* sampler_status_string(int code)
 {
@@ -192,6 +293,23 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
     h->max_vocab = cfg->max_vocab;
     h->max_history = cfg->max_history;
     h->flags = cfg->flags;
+    cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
+    h->col_rows = int(std::min<int64_t>(cfg->max_rows, dst::col::kMaxRows));
+    {
+        const size_t rec_bytes = size_t(h->col_rows) * size_t(h->num_sms) * sizeof(dst::col::ColRec);
+        if (cudaMalloc(&h->col_rec, rec_bytes) != cudaSuccess ||
+            cudaMalloc(&h->col_counters, size_t(h->col_rows) * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(h->col_counters, 0, size_t(h->col_rows) * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMalloc(&h->stats, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaMemset(h->stats, 0, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(h->col_rec);
+            cudaFree(h->col_counters);
+            cudaFree(h->stats);
+            delete h;
+            return SAMPLER_ERR_CUDA;
+        }
+    }
     if (cfg->flags & SAMPLER_CREATE_HOST_STAGING) {
         const size_t R = size_t(cfg->max_rows), V = size_t(cfg->max_vocab);
         size_t bytes = 0;
@@ -200,6 +318,9 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
         bytes += 16 * align16(R * 8);         // per-row arrays
         bytes += align16((R + 1) * 4) + align16(size_t(cfg->max_history) * 4 + 4);
         if (cudaMalloc(&h->stage_base, bytes) != cudaSuccess) {
+            cudaFree(h->col_rec);
+            cudaFree(h->col_counters);
+            cudaFree(h->stats);
             delete h;
             return SAMPLER_ERR_CUDA;
         }
@@ -212,13 +333,14 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
 void sampler_destroy(sampler_t h)
 {
     if (!h) return;
-    if (h->stage_base) {
-        int cur = -1;
-        cudaGetDevice(&cur);
-        cudaSetDevice(h->device);
-        cudaFree(h->stage_base);
-        if (cur >= 0) cudaSetDevice(cur);
-    }
+    int cur = -1;
+    cudaGetDevice(&cur);
+    cudaSetDevice(h->device);
+    if (h->stage_base) cudaFree(h->stage_base);
+    if (h->col_rec) cudaFree(h->col_rec);
+    if (h->col_counters) cudaFree(h->col_counters);
+    if (h->stats) cudaFree(h->stats);
+    if (cur >= 0) cudaSetDevice(cur);
     delete h;
 }
 

@@ -183,6 +183,14 @@ void sampler_destroy(sampler_t h);
 /* A static string for a return code or a per-row status code. */
 const char* sampler_status_string(int code);
 
+/* Diagnostic counters kept on the device (reading one synchronizes the device):
+ *   SAMPLER_STAT_EXACT_ROWS  rows whose kept set reached below what the per-slice
+ *                            candidates of the small-batch path cover, and which
+ *                            were therefore finished by its slower exact path.
+ * Writes the count to *value and clears it when reset != 0. */
+enum { SAMPLER_STAT_EXACT_ROWS = 0 };
+int sampler_get_stat(sampler_t h, int which, uint64_t* value, int reset);
+
 /* ABI version of this header: (major << 16) | minor. */
 uint32_t sampler_abi_version(void);
 

@@ -172,7 +172,7 @@ def test_host_rejections(sampler):
     t = torch.ones(2, device="cuda")
     out = torch.zeros(2, dtype=torch.int32, device="cuda")
     with pytest.raises(d.SamplerError) as e:
-        sampler.sample(logits=x, temperature=t, out_tokens=out, vocab=300000)
+        sampler.sample(logits=x, temperature=t, out_tokens=out, vocab=300000, row_stride=300000)
     assert e.value.code == d._binding.SAMPLER_ERR_TOO_LARGE
     with pytest.raises(d.SamplerError) as e:
         sampler.sample(logits=x, temperature=t, out_tokens=out, dtype=9)
