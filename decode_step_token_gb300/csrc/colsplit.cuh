@@ -75,17 +75,12 @@ struct alignas(16) RowInfo {
 };
 
 struct alignas(16) ColShared {
-    uint64_t mbar[kMaxRows];
-    RowInfo info[kMaxRows];
-    int16_t order[kMaxRows];      // rows in processing order
-    int16_t warp_of[kMaxRows];
-    int32_t cls_count[4];
     int32_t fallback_rows[kMaxRows];
     float fb_m[kMaxRows];
     int32_t fb_amax[kMaxRows];
     int32_t n_fallback;
-    int32_t pad;
-    unsigned long long buf[kW][kListCap];  // per-warp scratch
+    int32_t next_row;  // the CTA's row queue
+    unsigned long long offset;  // Philox counter words 2-3 for this launch
     // CTA-wide scratch for the exact fallback
     uint32_t hcnt[256];
     unsigned long long hmass[256];
@@ -93,12 +88,30 @@ struct alignas(16) ColShared {
     int32_t red_i[kW];
     float red_f[kW];
     GTop2 red_g[kW];
-    unsigned long long sel_prefix;  // packed state of the fallback select
+    unsigned long long sel_prefix;  // state of the fallback select
     unsigned long long sel_wabove;
     unsigned long long sel_target;
     int32_t sel_idx;
     int32_t sel_found;
 };
+
+// A staged row in a warp's ring: raw parameters (copied asynchronously with the
+// logits) followed by the slice's 16-byte vectors.
+struct alignas(16) SlotHdr {
+    float T;
+    int32_t k;
+    float p;
+    float minp;
+    uint32_t seed_lo, seed_hi;
+    uint32_t stream_id;
+    int32_t lrow;
+    int32_t r;
+    uint32_t has_seed;  // the aligned 4-byte word that holds the row's has_seed byte
+    float pres, freq, rep;
+    int32_t hs_shift;   // bit position of that byte within the word
+    int32_t pad[2];
+};
+constexpr int kSlots = 3;  // rows staged per warp: the current one and two ahead
 
 __device__ __forceinline__ RowParams as_row_params(const RowInfo& ri)
 {
@@ -335,10 +348,10 @@ __device__ void cta_select(ColShared& sh, const KernelParams& kp, const RowInfo&
 
 // Exact finish of one row by the whole CTA (rows the candidates could not settle).
 template <typename InT>
-__device__ void cta_exact_row(ColShared& sh, const ColParams& P, int r, float m, int amax)
+__device__ void cta_exact_row(ColShared& sh, const ColParams& P, int r, const RowInfo ri, float m,
+                              int amax)
 {
     const KernelParams& kp = P.k;
-    const RowInfo ri = sh.info[r];
     const int V = int(kp.vocab);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     uint32_t bk = 0;

@@ -61,7 +61,7 @@ struct sampler_s {
     int64_t max_rows, max_vocab, max_history;
     uint32_t flags;
     size_t smem_set[4];  // dynamic shared memory already granted per kernel variant
-    size_t col_smem_set[2];
+    size_t col_smem_set[6];
     // workspace of the column-split path: per-(row, slice) records and row counters
     dst::col::ColRec* col_rec;
     uint32_t* col_counters;
@@ -75,7 +75,8 @@ struct sampler_s {
 namespace {
 
 struct ColGeometry {
-    int gc, w, row_bytes;  // slices per row, elements per slice, staged bytes per row
+    int gc, w, row_bytes;  // slices per row, elements per slice, (unused)
+    int nv;                // 16-byte vectors per lane per row slice (kernel variant)
     size_t smem;
 };
 bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g);
@@ -151,8 +152,13 @@ ColGeometry col_geometry(int64_t N, int64_t V, int esize, int sms)
     w = std::max<int64_t>(512, (w + 7) & ~int64_t(7));
     g.w = int(w);
     g.gc = int((V + w - 1) / w);
-    g.row_bytes = int(align16(size_t(w) * esize + 32));
-    g.smem = ((sizeof(dst::col::ColShared) + 127) & ~size_t(127)) + size_t(N) * g.row_bytes;
+    const int64_t vecs = (w * esize + 15) / 16;  // 16-byte vectors per slice
+    g.nv = vecs <= 64 ? 2 : (vecs <= 128 ? 4 : (vecs <= 256 ? 8 : 0));
+    g.row_bytes = 0;
+    const int vec_bytes = std::max(g.nv * 32 * 16, dst::col::kListCap * 8);
+    g.smem = ((sizeof(dst::col::ColShared) + 127) & ~size_t(127)) +
+             size_t(dst::col::kW) * dst::col::kSlots * (sizeof(dst::col::SlotHdr) + vec_bytes);
+    (void)N;
     return g;
 }
 
@@ -163,15 +169,24 @@ bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g)
     if (a->hist_offsets || a->out_probs || a->out_logprobs) return false;
     const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
     *g = col_geometry(a->n_rows, a->vocab, esize, h->num_sms);
-    return g->smem <= size_t(kMaxSmem) && g->gc <= h->num_sms && g->gc <= dst::col::kMaxGc;
+    return g->nv > 0 && g->smem <= size_t(kMaxSmem) && g->gc <= h->num_sms &&
+           g->gc <= dst::col::kMaxGc;
 }
+
+template <typename InT, int NV>
+void* col_kernel() { return reinterpret_cast<void*>(&dst::col::colsplit_kernel<InT, NV>); }
 
 int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream)
 {
-    void* fn = a->dtype == SAMPLER_DTYPE_BF16
-                   ? reinterpret_cast<void*>(&dst::col::colsplit_kernel<uint16_t>)
-                   : reinterpret_cast<void*>(&dst::col::colsplit_kernel<float>);
-    const int slot = a->dtype == SAMPLER_DTYPE_BF16 ? 1 : 0;
+    const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
+    void* fn = nullptr;
+    int slot = 0;
+    switch (g.nv) {
+        case 2: fn = bf ? col_kernel<uint16_t, 2>() : col_kernel<float, 2>(); slot = 0; break;
+        case 4: fn = bf ? col_kernel<uint16_t, 4>() : col_kernel<float, 4>(); slot = 1; break;
+        default: fn = bf ? col_kernel<uint16_t, 8>() : col_kernel<float, 8>(); slot = 2; break;
+    }
+    slot = slot * 2 + (bf ? 1 : 0);
     if (h->col_smem_set[slot] < g.smem) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(g.smem)) !=
             cudaSuccess)
@@ -204,7 +219,7 @@ int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaS
     p.n_rows = int(a->n_rows);
     p.gc = g.gc;
     p.w = g.w;
-    p.row_bytes = g.row_bytes;
+    p.row_bytes = 0;
     p.rec = h->col_rec;
     p.counters = h->col_counters;
     p.stats = h->stats;
