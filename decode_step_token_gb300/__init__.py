@@ -12,13 +12,14 @@ from typing import Optional
 
 from . import _binding as abi
 from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_DTYPE_BF16,
-                       SAMPLER_DTYPE_F32, SAMPLER_OK, load_library, sampler_abi_version,
-                       sampler_args_t, sampler_config_t, sampler_create, sampler_destroy,
-                       sampler_sample, sampler_sample_host, sampler_status_string,
-                       sampler_get_stat)
+                       SAMPLER_DTYPE_F32, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK, load_library,
+                       sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
+                       sampler_destroy, sampler_sample, sampler_sample_host,
+                       sampler_sample_noalloc, sampler_status_string, sampler_get_stat)
 
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
-           "sampler_sample_host", "sampler_destroy", "sampler_status_string",
+           "sampler_sample_host", "sampler_sample_noalloc", "sampler_destroy",
+           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS",
            "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
 
 

@@ -23,6 +23,7 @@ SAMPLER_ERR_BAD_DTYPE = -4
 SAMPLER_ERR_CUDA = -5
 SAMPLER_ERR_NO_DEVICE = -6
 SAMPLER_ERR_NO_STAGING = -7
+SAMPLER_ERR_UNSUPPORTED = -8
 
 SAMPLER_ROW_OK = 0
 SAMPLER_ROW_NONFINITE = 1
@@ -34,8 +35,10 @@ SAMPLER_ROW_TIMEOUT = 5
 SAMPLER_CREATE_HOST_STAGING = 1
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
-            "sampler_status_string", "sampler_abi_version", "sampler_get_stat")
+            "sampler_status_string", "sampler_abi_version", "sampler_get_stat",
+            "sampler_sample_noalloc")
 SAMPLER_STAT_EXACT_ROWS = 0
+SAMPLER_NOALLOC_MAX_ROWS = 64
 
 
 class sampler_config_t(ctypes.Structure):
@@ -108,6 +111,8 @@ def load_library(path: str = LIB):
             lib.sampler_get_stat.argtypes = [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64),
                                              ctypes.c_int]
             lib.sampler_get_stat.restype = ctypes.c_int
+            lib.sampler_sample_noalloc.argtypes = [ctypes.POINTER(sampler_args_t), _P]
+            lib.sampler_sample_noalloc.restype = ctypes.c_int
             lib.sampler_abi_version.argtypes = []
             lib.sampler_abi_version.restype = ctypes.c_uint32
             _lib = lib
@@ -127,6 +132,10 @@ def sampler_sample(h, args: sampler_args_t, stream: int) -> int:
 
 def sampler_sample_host(h, args: sampler_args_t, stream: int) -> int:
     return load_library().sampler_sample_host(h, ctypes.byref(args), _P(stream))
+
+
+def sampler_sample_noalloc(args: sampler_args_t, stream: int) -> int:
+    return load_library().sampler_sample_noalloc(ctypes.byref(args), _P(stream))
 
 
 def sampler_destroy(h) -> None:

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "colsplit_kernel.cuh"
@@ -245,6 +246,74 @@ int check_args(sampler_t h, const sampler_args_t* a)
 
 }  // namespace
 
+// ---------------------------------------------------------------- allocation-free entry
+// The column-split kernel's workspace (row counters, then the per-(row, slice)
+// records) lives in this module's own device memory for sampler_sample_noalloc.
+namespace {
+
+constexpr int kNoAllocRows = SAMPLER_NOALLOC_MAX_ROWS;
+constexpr size_t kNoAllocCounterBytes = 256;  // kNoAllocRows 32-bit counters, padded
+constexpr size_t kNoAllocScratchBytes =
+    kNoAllocCounterBytes + size_t(kNoAllocRows) * dst::col::kMaxGc * sizeof(dst::col::ColRec);
+static_assert(kNoAllocRows * sizeof(uint32_t) <= kNoAllocCounterBytes, "counter area");
+static_assert(kNoAllocCounterBytes % alignof(dst::col::ColRec) == 0, "record alignment");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+    bool ready;
+    int num_sms;
+    unsigned char* scratch;  // device address of g_noalloc_scratch on this device
+    size_t smem_set[6];
+};
+
+std::mutex g_noalloc_mutex;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device (the device current): find the scratch array's address, read
+// the SM count and clear the row counters, which must start at zero (the kernel
+// leaves them at zero after every row it finishes).
+int noalloc_setup(int dev, cudaStream_t stream, NoAllocDevice* out)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, col_kernel<uint16_t, 8>()) != cudaSuccess) {
+            cudaGetLastError();
+            return SAMPLER_ERR_NO_DEVICE;
+        }
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SAMPLER_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            return SAMPLER_ERR_CUDA;
+        if (cudaMemsetAsync(ptr, 0, kNoAllocCounterBytes, stream) != cudaSuccess) return SAMPLER_ERR_CUDA;
+        d.scratch = static_cast<unsigned char*>(ptr);
+        d.num_sms = sms;
+        std::memset(d.smem_set, 0, sizeof d.smem_set);
+        d.ready = true;
+    }
+    *out = d;
+    return SAMPLER_OK;
+}
+
+int noalloc_grant_smem(int dev, int slot, void* fn, size_t smem)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (d.smem_set[slot] < smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+            return SAMPLER_ERR_CUDA;
+        d.smem_set[slot] = smem;
+    }
+    return SAMPLER_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 uint32_t sampler_abi_version(void) { return (1u << 16) | 0u; }
@@ -273,6 +342,7 @@ const char* sampler_status_string(int code)
         case SAMPLER_ERR_CUDA: return "a CUDA call failed";
         case SAMPLER_ERR_NO_DEVICE: return "no usable sm_103 device";
         case SAMPLER_ERR_NO_STAGING: return "handle has no host staging buffers";
+        case SAMPLER_ERR_UNSUPPORTED: return "not supported by this entry point";
         case SAMPLER_ROW_NONFINITE: return "row: NaN or +inf logit";
         case SAMPLER_ROW_ALL_NEG_INF: return "row: every logit is -inf";
         case SAMPLER_ROW_BAD_PARAM: return "row: parameter out of range";
@@ -365,6 +435,74 @@ int sampler_sample(sampler_t h, const sampler_args_t* a, sampler_stream_t stream
     if (rc != SAMPLER_OK || a->n_rows == 0) return rc;
     if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
     return launch(h, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
+{
+    if (!a) return SAMPLER_ERR_NULL_ARG;
+    if (a->n_rows < 0 || a->vocab < 1 || a->row_stride < a->vocab || a->n_logit_rows < 0)
+        return SAMPLER_ERR_BAD_SHAPE;
+    if (a->dtype != SAMPLER_DTYPE_F32 && a->dtype != SAMPLER_DTYPE_BF16) return SAMPLER_ERR_BAD_DTYPE;
+    if (a->n_rows > kNoAllocRows || a->vocab > kMaxVocabLimit) return SAMPLER_ERR_TOO_LARGE;
+    if (a->hist_offsets || a->hist_ids || a->out_probs || a->out_logprobs) return SAMPLER_ERR_UNSUPPORTED;
+    if (a->n_rows == 0) return SAMPLER_OK;
+    if (!a->logits || !a->temperature || !a->out_tokens) return SAMPLER_ERR_NULL_ARG;
+    if (a->has_seed && !a->seed) return SAMPLER_ERR_NULL_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return SAMPLER_ERR_NO_DEVICE;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    NoAllocDevice d;
+    int rc = noalloc_setup(dev, stream, &d);
+    if (rc != SAMPLER_OK) return rc;
+    const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
+    const ColGeometry g = col_geometry(a->n_rows, a->vocab, bf ? 2 : 4, d.num_sms);
+    if (g.nv == 0 || g.smem > size_t(kMaxSmem) || g.gc > d.num_sms || g.gc > dst::col::kMaxGc)
+        return SAMPLER_ERR_TOO_LARGE;
+    void* fn = nullptr;
+    int slot = 0;
+    switch (g.nv) {
+        case 2: fn = bf ? col_kernel<uint16_t, 2>() : col_kernel<float, 2>(); slot = 0; break;
+        case 4: fn = bf ? col_kernel<uint16_t, 4>() : col_kernel<float, 4>(); slot = 1; break;
+        default: fn = bf ? col_kernel<uint16_t, 8>() : col_kernel<float, 8>(); slot = 2; break;
+    }
+    slot = slot * 2 + (bf ? 1 : 0);
+    rc = noalloc_grant_smem(dev, slot, fn, g.smem);
+    if (rc != SAMPLER_OK) return rc;
+    dst::col::ColParams p;
+    std::memset(&p, 0, sizeof p);
+    dst::KernelParams& k = p.k;
+    k.logits = a->logits;
+    k.vocab = a->vocab;
+    k.row_stride = a->row_stride;
+    k.n_logit_rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
+    k.logit_row = a->logit_row;
+    k.temperature = a->temperature;
+    k.top_k = a->top_k;
+    k.top_p = a->top_p;
+    k.min_p = a->min_p;
+    k.presence = a->presence_penalty;
+    k.frequency = a->frequency_penalty;
+    k.repetition = a->repetition_penalty;
+    k.seed = a->seed;
+    k.has_seed = a->has_seed;
+    k.stream_id = a->stream_id;
+    k.global_seed = a->global_seed;
+    k.philox_offset = a->philox_offset;
+    k.philox_offset_dev = a->philox_offset_dev;
+    k.out_tokens = a->out_tokens;
+    k.out_status = a->out_status;
+    p.n_rows = int(a->n_rows);
+    p.gc = g.gc;
+    p.w = g.w;
+    p.row_bytes = 0;
+    p.counters = reinterpret_cast<uint32_t*>(d.scratch);
+    p.rec = reinterpret_cast<dst::col::ColRec*>(d.scratch + kNoAllocCounterBytes);
+    p.stats = nullptr;
+    void* args[] = {&p};
+    if (cudaLaunchKernel(fn, dim3(g.gc), dim3(dst::col::kT), args, g.smem, stream) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
 }
 
 int sampler_sample_host(sampler_t h, const sampler_args_t* a, sampler_stream_t stream_)

@@ -79,7 +79,8 @@ enum {
     SAMPLER_ERR_BAD_DTYPE = -4,
     SAMPLER_ERR_CUDA = -5,         /* a CUDA call failed (launch, copy, set-up) */
     SAMPLER_ERR_NO_DEVICE = -6,    /* no usable sm_100-family device */
-    SAMPLER_ERR_NO_STAGING = -7    /* sampler_sample_host on a handle made without staging */
+    SAMPLER_ERR_NO_STAGING = -7,   /* sampler_sample_host on a handle made without staging */
+    SAMPLER_ERR_UNSUPPORTED = -8   /* a feature sampler_sample_noalloc does not offer */
 };
 
 /* Per-row status codes written to out_status (when given). A row with a
@@ -176,6 +177,31 @@ int sampler_sample(sampler_t h, const sampler_args_t* args, sampler_stream_t str
  * SAMPLER_CREATE_HOST_STAGING; history length <= cfg.max_history. Pinned host
  * memory makes the copies asynchronous with respect to other streams. */
 int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_t stream);
+
+/*
+ * Allocation-free sampling step. None of the pages has a counterpart: the
+ * sampler they describe always owns its buffers. This entry point takes no
+ * handle and allocates nothing. Its workspace (row counters and per-(row,
+ * slice) records, about 2 MiB) is an array in the library's own device
+ * memory, one copy per device. It runs the same kernel sampler_sample uses for
+ * small batches and returns the same tokens.
+ *
+ * The first call on a device does a one-time set-up on the current device:
+ * it looks up that array's address, reads the SM count and clears the row
+ * counters on `stream`. Make that first call before any stream capture.
+ *
+ * Arguments as for sampler_sample (device pointers on the current device),
+ * with these limits:
+ *   n_rows <= SAMPLER_NOALLOC_MAX_ROWS, else SAMPLER_ERR_TOO_LARGE;
+ *   no history and no out_probs / out_logprobs, else SAMPLER_ERR_UNSUPPORTED;
+ *   vocab <= 2048 x SM count for bf16 and <= 1024 x SM count for fp32 (and
+ *   <= 262144), else SAMPLER_ERR_TOO_LARGE.
+ * Calls on one device share the workspace: two calls whose kernels can run at
+ * the same time (different streams, or different host threads without
+ * ordering) race and give wrong tokens. Order them on one stream.
+ */
+#define SAMPLER_NOALLOC_MAX_ROWS 64
+int sampler_sample_noalloc(const sampler_args_t* args, sampler_stream_t stream);
 
 /* Release the handle and its device memory. NULL is a no-op. */
 void sampler_destroy(sampler_t h);
