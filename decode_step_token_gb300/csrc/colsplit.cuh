@@ -1,21 +1,21 @@
-// colsplit.cuh -- the column-split sampler kernel for small batches (sm_103a).
+// colsplit.cuh -- the unit-split sampler kernel for small batches (sm_103a).
 //
-// Every CTA (one per SM, 512 threads) owns one vocabulary slice of EVERY row, so
-// each SM gets the same share of each row's work whatever the per-row mix of
-// greedy / plain-temperature / truncated rows is. A CTA stages its slices of all
-// rows into shared memory with one bulk (TMA-engine) copy per row, issued at
-// launch, so the whole batch is in flight at once. Each warp owns a
-// cost-balanced set of rows; for each (row, slice) it writes a small summary
-// record to global memory and bumps the row's arrival counter. The warp that
-// brings a counter to the slice count finishes that row from the records:
+// Each row is cut into G equal vocabulary units; the N x G units are spread
+// over every warp of the GPU (one CTA of 16 warps per SM), one unit per warp
+// when the batch allows. A warp copies its unit into its own shared-memory slot
+// with 16-byte asynchronous copies in four groups and starts on the first group
+// while the rest are in flight. It then writes a summary record of the unit to
+// global memory and bumps the row's arrival counter with a release atomic. The
+// warp that brings a counter to G finishes the row from the G records:
 //
-//   greedy rows     argmax of the per-slice maxima (lowest index on ties)
-//   plain rows      the best two Gumbel scores of every slice, settled in double
-//   truncated rows  per-slice top-8 candidates merged into the row's top list;
-//                   top-k / top-p / min-p cut in double, Gumbel-max over the cut
+//   greedy rows     argmax of the unit maxima (lowest index on ties)
+//   plain rows      the best two Gumbel scores of every unit, settled in double
+//   truncated rows  each unit's own top-C list (C = k when k <= 64, else 64),
+//                   merged into the row's sorted top list; top-k / top-p /
+//                   min-p cut in double, Gumbel-max over the kept tokens
 //
-// A truncated row whose kept set reaches below what the candidates cover is
-// finished exactly by its finishing CTA, streaming the row from global memory
+// A truncated row whose kept set reaches below what the lists cover is pushed
+// to its finishing CTA, which samples it exactly once all its units are done
 // (radix select by count or fixed-point softmax mass, then a Gumbel pass). The
 // finishing warp resets the row's counter, so the workspace is clean for the
 // next launch. Nothing waits on another CTA: no co-residency is assumed.
@@ -28,36 +28,37 @@ namespace col {
 
 constexpr int kT = 512;
 constexpr int kW = kT / 32;
-constexpr int kSliceCand = 8;
+constexpr int kSlotBytes = 9216;  // staged logits per warp: 4608 bf16 or 2304 fp32
+constexpr int kBufCap = 512;      // candidate words per warp
+constexpr int kCandCap = 64;      // candidates per unit record
+constexpr int kKeepCap = 64;      // kept tokens a finishing warp resolves
+constexpr int kStages = 4;        // copy groups per unit
 constexpr int kMaxRows = 256;
-constexpr int kListCap = 256;  // finisher merge list per warp
-constexpr int kKeepCap = 64;   // kept tokens resolved by a finishing warp
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
-constexpr int kMaxGc = 256;                 // slices per row (CTAs of the grid)
-constexpr int kMaxGcPerLane = kMaxGc / 32;
+constexpr int kUnitMinBytes = 4096;  // smallest unit, unless a row is narrower
 
 enum : uint8_t { kClsErr = 0, kClsGreedy = 1, kClsPlain = 2, kClsCand = 3 };
 
-struct alignas(16) ColRec {  // one (row, slice) summary
-    float mx;
-    int32_t amax;
+struct alignas(16) ColRec {  // one (row, unit) summary
+    float mx;      // unit maximum (NaN ignored)
+    int32_t amax;  // its lowest index
     uint32_t flags;
-    uint32_t nc;  // candidates submitted, kOverflow if the slice could not bound them
-    GRec g0, g1;
-    unsigned long long cand[kSliceCand];
-    float zs;     // sum of exp((x - mx) / T) over the slice (compensated)
-    float zc;     // its compensation term
+    uint32_t nc;   // candidates listed, kOverflow if the unit could not bound them
+    GRec g0, g1;   // plain rows: the unit's best two Gumbel scores
+    float zs;      // top-p rows without top-k: sum of exp((x - mx) / T), compensated
+    float zc;      // its compensation term
     float pad0, pad1;
+    unsigned long long cand[kCandCap];  // truncated rows: top list, descending
 };
 
 struct ColParams {
     KernelParams k;
     int32_t n_rows;
-    int32_t gc;         // slices per row (= grid size)
-    int32_t w;          // elements per slice (multiple of 8)
-    int32_t row_bytes;  // staged bytes per row (multiple of 16)
-    ColRec* rec;        // [n_rows][gc]
-    uint32_t* counters; // [n_rows], zero between launches
+    int32_t gc;       // units per row
+    int32_t w;        // elements per unit (a multiple of 16 bytes)
+    int32_t n_units;  // n_rows * gc
+    ColRec* rec;      // [n_rows][gc]
+    uint32_t* counters;  // [n_rows], zero between launches
     unsigned long long* stats;  // [0] rows finished by the exact path (diagnostic)
 };
 
@@ -67,9 +68,6 @@ struct alignas(16) RowInfo {
     uint32_t stream, key_lo, key_hi, off_lo, off_hi;
     int32_t lrow;
     int32_t status;
-    int32_t hb;          // staged head pad in bytes
-    int32_t head_end;    // elements before the aligned interior
-    int32_t tail_begin;  // first element after it
     uint8_t cls, do_topk, do_topp, do_minp;
     uint8_t need_z, small_k, greedy, pad;
 };
@@ -79,7 +77,7 @@ struct alignas(16) ColShared {
     float fb_m[kMaxRows];
     int32_t fb_amax[kMaxRows];
     int32_t n_fallback;
-    int32_t next_row;  // the CTA's row queue
+    int32_t pad_;
     unsigned long long offset;  // Philox counter words 2-3 for this launch
     // CTA-wide scratch for the exact fallback
     uint32_t hcnt[256];
@@ -95,23 +93,10 @@ struct alignas(16) ColShared {
     int32_t sel_found;
 };
 
-// A staged row in a warp's ring: raw parameters (copied asynchronously with the
-// logits) followed by the slice's 16-byte vectors.
-struct alignas(16) SlotHdr {
-    float T;
-    int32_t k;
-    float p;
-    float minp;
-    uint32_t seed_lo, seed_hi;
-    uint32_t stream_id;
-    int32_t lrow;
-    int32_t r;
-    uint32_t has_seed;  // the aligned 4-byte word that holds the row's has_seed byte
-    float pres, freq, rep;
-    int32_t hs_shift;   // bit position of that byte within the word
-    int32_t pad[2];
-};
-constexpr int kSlots = 3;  // rows staged per warp: the current one and two ahead
+constexpr size_t kSharedHead = (sizeof(ColShared) + 127) & ~size_t(127);
+constexpr size_t kWarpBytes = size_t(kSlotBytes) + size_t(kBufCap) * 8;
+constexpr size_t kSmemBytes = kSharedHead + kW * kWarpBytes;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ RowParams as_row_params(const RowInfo& ri)
 {
@@ -189,7 +174,7 @@ __device__ __forceinline__ void warp_sort64_desc(unsigned long long& a, unsigned
     }
 }
 
-// Sort n <= kListCap words in warp-private shared memory, descending (bitonic).
+// Sort n <= kBufCap words in warp-private shared memory, descending (bitonic).
 __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n)
 {
     const int lane = threadIdx.x & 31;

@@ -62,12 +62,13 @@ struct sampler_s {
     int64_t max_rows, max_vocab, max_history;
     uint32_t flags;
     size_t smem_set[4];  // dynamic shared memory already granted per kernel variant
-    size_t col_smem_set[6];
-    // workspace of the column-split path: per-(row, slice) records and row counters
+    size_t col_smem_set[2];
+    // workspace of the unit-split path: per-(row, unit) records and row counters
     dst::col::ColRec* col_rec;
     uint32_t* col_counters;
     unsigned long long* stats;  // device counters (diagnostics)
     int col_rows;
+    int64_t col_units;  // records in col_rec
     // staging for sampler_sample_host
     unsigned char* stage_base;
     size_t stage_bytes;
@@ -76,9 +77,10 @@ struct sampler_s {
 namespace {
 
 struct ColGeometry {
-    int gc, w, row_bytes;  // slices per row, elements per slice, (unused)
-    int nv;                // 16-byte vectors per lane per row slice (kernel variant)
-    size_t smem;
+    int gc;         // units per row
+    int w;          // elements per unit
+    int64_t units;  // n_rows * gc
+    int grid;       // CTAs
 };
 bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g);
 int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream);
@@ -146,55 +148,51 @@ int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
     return SAMPLER_OK;
 }
 
+// Units of one row: about one per warp of the GPU, between kUnitMinBytes (or the
+// whole row) and one warp's slot; a multiple of 16 bytes.
 ColGeometry col_geometry(int64_t N, int64_t V, int esize, int sms)
 {
     ColGeometry g;
-    int64_t w = (V + sms - 1) / sms;
-    w = std::max<int64_t>(512, (w + 7) & ~int64_t(7));
+    const int64_t epv = 16 / esize;
+    const int64_t w_min = dst::col::kUnitMinBytes / esize;
+    const int64_t w_max = dst::col::kSlotBytes / esize;
+    const int64_t warps = int64_t(sms) * dst::col::kW;
+    const int64_t g0 = std::max<int64_t>(1, warps / std::max<int64_t>(N, 1));
+    int64_t w = (V + g0 - 1) / g0;
+    w = (w + epv - 1) / epv * epv;
+    w = std::min(std::max(w, w_min), w_max);
+    w = std::min(w, (V + epv - 1) / epv * epv);
     g.w = int(w);
     g.gc = int((V + w - 1) / w);
-    const int64_t vecs = (w * esize + 15) / 16;  // 16-byte vectors per slice
-    g.nv = vecs <= 64 ? 2 : (vecs <= 128 ? 4 : (vecs <= 256 ? 8 : 0));
-    g.row_bytes = 0;
-    const int vec_bytes = std::max(g.nv * 32 * 16, dst::col::kListCap * 8);
-    g.smem = ((sizeof(dst::col::ColShared) + 127) & ~size_t(127)) +
-             size_t(dst::col::kW) * dst::col::kSlots * (sizeof(dst::col::SlotHdr) + vec_bytes);
-    (void)N;
+    g.units = N * g.gc;
+    g.grid = int(std::min<int64_t>(sms, std::max<int64_t>(g.units, 1)));
     return g;
 }
 
-// The column-split kernel serves small batches without penalties or outputs.
+// Largest unit count col_geometry gives for up to `rows` rows of up to `vocab`.
+int64_t col_max_units(int64_t rows, int64_t vocab, int sms)
+{
+    int64_t best = 0;
+    for (int esize = 2; esize <= 4; esize += 2)
+        for (int64_t n = 1; n <= rows; ++n) best = std::max(best, col_geometry(n, vocab, esize, sms).units);
+    return best;
+}
+
+// The unit-split kernel serves small batches without penalties or outputs.
 bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g)
 {
     if (!h->col_rec || a->n_rows > h->col_rows) return false;
     if (a->hist_offsets || a->out_probs || a->out_logprobs) return false;
     const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
     *g = col_geometry(a->n_rows, a->vocab, esize, h->num_sms);
-    return g->nv > 0 && g->smem <= size_t(kMaxSmem) && g->gc <= h->num_sms &&
-           g->gc <= dst::col::kMaxGc;
+    return g->units <= h->col_units;
 }
 
-template <typename InT, int NV>
-void* col_kernel() { return reinterpret_cast<void*>(&dst::col::colsplit_kernel<InT, NV>); }
+template <typename InT>
+void* col_kernel() { return reinterpret_cast<void*>(&dst::col::colsplit_kernel<InT>); }
 
-int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream)
+void fill_col_params(dst::col::ColParams& p, const sampler_args_t* a, const ColGeometry& g)
 {
-    const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
-    void* fn = nullptr;
-    int slot = 0;
-    switch (g.nv) {
-        case 2: fn = bf ? col_kernel<uint16_t, 2>() : col_kernel<float, 2>(); slot = 0; break;
-        case 4: fn = bf ? col_kernel<uint16_t, 4>() : col_kernel<float, 4>(); slot = 1; break;
-        default: fn = bf ? col_kernel<uint16_t, 8>() : col_kernel<float, 8>(); slot = 2; break;
-    }
-    slot = slot * 2 + (bf ? 1 : 0);
-    if (h->col_smem_set[slot] < g.smem) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(g.smem)) !=
-            cudaSuccess)
-            return SAMPLER_ERR_CUDA;
-        h->col_smem_set[slot] = g.smem;
-    }
-    dst::col::ColParams p;
     std::memset(&p, 0, sizeof p);
     dst::KernelParams& k = p.k;
     k.logits = a->logits;
@@ -220,12 +218,27 @@ int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaS
     p.n_rows = int(a->n_rows);
     p.gc = g.gc;
     p.w = g.w;
-    p.row_bytes = 0;
+    p.n_units = int(g.units);
+}
+
+int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream)
+{
+    const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
+    void* fn = bf ? col_kernel<uint16_t>() : col_kernel<float>();
+    const int slot = bf ? 1 : 0;
+    if (h->col_smem_set[slot] < dst::col::kSmemBytes) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dst::col::kSmemBytes)) !=
+            cudaSuccess)
+            return SAMPLER_ERR_CUDA;
+        h->col_smem_set[slot] = dst::col::kSmemBytes;
+    }
+    dst::col::ColParams p;
+    fill_col_params(p, a, g);
     p.rec = h->col_rec;
     p.counters = h->col_counters;
     p.stats = h->stats;
     void* args[] = {&p};
-    if (cudaLaunchKernel(fn, dim3(g.gc), dim3(dst::col::kT), args, g.smem, stream) != cudaSuccess)
+    if (cudaLaunchKernel(fn, dim3(g.grid), dim3(dst::col::kT), args, dst::col::kSmemBytes, stream) != cudaSuccess)
         return SAMPLER_ERR_CUDA;
     return SAMPLER_OK;
 }
@@ -253,8 +266,9 @@ namespace {
 
 constexpr int kNoAllocRows = SAMPLER_NOALLOC_MAX_ROWS;
 constexpr size_t kNoAllocCounterBytes = 256;  // kNoAllocRows 32-bit counters, padded
-constexpr size_t kNoAllocScratchBytes =
-    kNoAllocCounterBytes + size_t(kNoAllocRows) * dst::col::kMaxGc * sizeof(dst::col::ColRec);
+constexpr size_t kNoAllocScratchBytes = size_t(9) << 19;  // 4.5 MiB: 64 rows of up to 262144
+constexpr int64_t kNoAllocUnits =
+    int64_t((kNoAllocScratchBytes - kNoAllocCounterBytes) / sizeof(dst::col::ColRec));
 static_assert(kNoAllocRows * sizeof(uint32_t) <= kNoAllocCounterBytes, "counter area");
 static_assert(kNoAllocCounterBytes % alignof(dst::col::ColRec) == 0, "record alignment");
 
@@ -266,7 +280,7 @@ struct NoAllocDevice {
     bool ready;
     int num_sms;
     unsigned char* scratch;  // device address of g_noalloc_scratch on this device
-    size_t smem_set[6];
+    size_t smem_set[2];
 };
 
 std::mutex g_noalloc_mutex;
@@ -281,7 +295,7 @@ int noalloc_setup(int dev, cudaStream_t stream, NoAllocDevice* out)
     NoAllocDevice& d = g_noalloc_dev[dev];
     if (!d.ready) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, col_kernel<uint16_t, 8>()) != cudaSuccess) {
+        if (cudaFuncGetAttributes(&fa, col_kernel<uint16_t>()) != cudaSuccess) {
             cudaGetLastError();
             return SAMPLER_ERR_NO_DEVICE;
         }
@@ -380,8 +394,9 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
     h->flags = cfg->flags;
     cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
     h->col_rows = int(std::min<int64_t>(cfg->max_rows, dst::col::kMaxRows));
+    h->col_units = col_max_units(h->col_rows, cfg->max_vocab, h->num_sms);
     {
-        const size_t rec_bytes = size_t(h->col_rows) * size_t(h->num_sms) * sizeof(dst::col::ColRec);
+        const size_t rec_bytes = size_t(h->col_units) * sizeof(dst::col::ColRec);
         if (cudaMalloc(&h->col_rec, rec_bytes) != cudaSuccess ||
             cudaMalloc(&h->col_counters, size_t(h->col_rows) * sizeof(uint32_t)) != cudaSuccess ||
             cudaMemset(h->col_counters, 0, size_t(h->col_rows) * sizeof(uint32_t)) != cudaSuccess ||
@@ -457,50 +472,17 @@ int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
     if (rc != SAMPLER_OK) return rc;
     const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
     const ColGeometry g = col_geometry(a->n_rows, a->vocab, bf ? 2 : 4, d.num_sms);
-    if (g.nv == 0 || g.smem > size_t(kMaxSmem) || g.gc > d.num_sms || g.gc > dst::col::kMaxGc)
-        return SAMPLER_ERR_TOO_LARGE;
-    void* fn = nullptr;
-    int slot = 0;
-    switch (g.nv) {
-        case 2: fn = bf ? col_kernel<uint16_t, 2>() : col_kernel<float, 2>(); slot = 0; break;
-        case 4: fn = bf ? col_kernel<uint16_t, 4>() : col_kernel<float, 4>(); slot = 1; break;
-        default: fn = bf ? col_kernel<uint16_t, 8>() : col_kernel<float, 8>(); slot = 2; break;
-    }
-    slot = slot * 2 + (bf ? 1 : 0);
-    rc = noalloc_grant_smem(dev, slot, fn, g.smem);
+    if (g.units > kNoAllocUnits) return SAMPLER_ERR_TOO_LARGE;
+    void* fn = bf ? col_kernel<uint16_t>() : col_kernel<float>();
+    rc = noalloc_grant_smem(dev, bf ? 1 : 0, fn, dst::col::kSmemBytes);
     if (rc != SAMPLER_OK) return rc;
     dst::col::ColParams p;
-    std::memset(&p, 0, sizeof p);
-    dst::KernelParams& k = p.k;
-    k.logits = a->logits;
-    k.vocab = a->vocab;
-    k.row_stride = a->row_stride;
-    k.n_logit_rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
-    k.logit_row = a->logit_row;
-    k.temperature = a->temperature;
-    k.top_k = a->top_k;
-    k.top_p = a->top_p;
-    k.min_p = a->min_p;
-    k.presence = a->presence_penalty;
-    k.frequency = a->frequency_penalty;
-    k.repetition = a->repetition_penalty;
-    k.seed = a->seed;
-    k.has_seed = a->has_seed;
-    k.stream_id = a->stream_id;
-    k.global_seed = a->global_seed;
-    k.philox_offset = a->philox_offset;
-    k.philox_offset_dev = a->philox_offset_dev;
-    k.out_tokens = a->out_tokens;
-    k.out_status = a->out_status;
-    p.n_rows = int(a->n_rows);
-    p.gc = g.gc;
-    p.w = g.w;
-    p.row_bytes = 0;
+    fill_col_params(p, a, g);
     p.counters = reinterpret_cast<uint32_t*>(d.scratch);
     p.rec = reinterpret_cast<dst::col::ColRec*>(d.scratch + kNoAllocCounterBytes);
     p.stats = nullptr;
     void* args[] = {&p};
-    if (cudaLaunchKernel(fn, dim3(g.gc), dim3(dst::col::kT), args, g.smem, stream) != cudaSuccess)
+    if (cudaLaunchKernel(fn, dim3(g.grid), dim3(dst::col::kT), args, dst::col::kSmemBytes, stream) != cudaSuccess)
         return SAMPLER_ERR_CUDA;
     return SAMPLER_OK;
 }

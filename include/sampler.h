@@ -182,9 +182,9 @@ int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_
  * Allocation-free sampling step. None of the pages has a counterpart: the
  * sampler they describe always owns its buffers. This entry point takes no
  * handle and allocates nothing. Its workspace (row counters and per-(row,
- * slice) records, about 2 MiB) is an array in the library's own device
- * memory, one copy per device. It runs the same kernel sampler_sample uses for
- * small batches and returns the same tokens.
+ * unit) records, 4.5 MiB) is an array in the library's own device memory, one
+ * copy per device. It runs the same kernel sampler_sample uses for small
+ * batches and returns the same tokens.
  *
  * The first call on a device does a one-time set-up on the current device:
  * it looks up that array's address, reads the SM count and clears the row
@@ -192,10 +192,9 @@ int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_
  *
  * Arguments as for sampler_sample (device pointers on the current device),
  * with these limits:
- *   n_rows <= SAMPLER_NOALLOC_MAX_ROWS, else SAMPLER_ERR_TOO_LARGE;
- *   no history and no out_probs / out_logprobs, else SAMPLER_ERR_UNSUPPORTED;
- *   vocab <= 2048 x SM count for bf16 and <= 1024 x SM count for fp32 (and
- *   <= 262144), else SAMPLER_ERR_TOO_LARGE.
+ *   n_rows <= SAMPLER_NOALLOC_MAX_ROWS and vocab <= 262144, else
+ *   SAMPLER_ERR_TOO_LARGE;
+ *   no history and no out_probs / out_logprobs, else SAMPLER_ERR_UNSUPPORTED.
  * Calls on one device share the workspace: two calls whose kernels can run at
  * the same time (different streams, or different host threads without
  * ordering) race and give wrong tokens. Order them on one stream.

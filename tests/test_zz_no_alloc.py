@@ -98,11 +98,11 @@ def test_noalloc_rejections(lib):
     pen = workloads.random_batch(76, 4, 1000, "f32", penalties=True)
     dd = dev.to_device(pen, want_probs=False)
     assert _noalloc(dev.sample_args(s, pen, dd), stream) == d._binding.SAMPLER_ERR_UNSUPPORTED
-    # fp32 rows wider than 1024 elements per SM do not fit the kernel's slices
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    wide = workloads.random_batch(77, 1, min(1024 * sms + 8, 262144), "f32")
-    dd = dev.to_device(wide, want_probs=False)
-    assert _noalloc(dev.sample_args(s, wide, dd), stream) == d._binding.SAMPLER_ERR_TOO_LARGE
+    # a vocabulary above 262144 is refused before anything is read
+    dd = dev.to_device(small, want_probs=False)
+    wide = dev.sample_args(s, small, dd)
+    wide.vocab = wide.row_stride = 262145
+    assert _noalloc(wide, stream) == d._binding.SAMPLER_ERR_TOO_LARGE
     empty = workloads.random_batch(78, 0, 100, "f32")
     dd = dev.to_device(empty, want_probs=False)
     assert _noalloc(dev.sample_args(s, empty, dd), stream) == d.SAMPLER_OK
