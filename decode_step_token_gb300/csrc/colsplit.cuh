@@ -35,7 +35,9 @@ constexpr int kKeepCap = 64;      // kept tokens a finishing warp resolves
 constexpr int kStages = 4;        // copy groups per unit
 constexpr int kMaxRows = 256;
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
-constexpr int kUnitMinBytes = 4096;  // smallest unit, unless a row is narrower
+constexpr int kUnitMinElems = 2048;  // smallest unit, unless a row is narrower
+constexpr int kMaxUnits = 128;       // units per row: 262144 / kUnitMinElems
+constexpr int kLPL = kMaxUnits / 32; // a finishing warp's lists per lane
 
 enum : uint8_t { kClsErr = 0, kClsGreedy = 1, kClsPlain = 2, kClsCand = 3 };
 
@@ -142,33 +144,39 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Sort 64 words held two per lane (lane holds items lane and lane + 32) descending:
-// a bitonic network over the 64 positions using shuffles.
-__device__ __forceinline__ void warp_sort64_desc(unsigned long long& a, unsigned long long& b)
+// Bitonic sort, descending, of the 32 R words a warp holds in registers: word q
+// of lane l is element 32 q + l. Strides of 32 and more swap registers within a
+// lane; shorter ones exchange with a shuffle.
+template <int R>
+__device__ __forceinline__ void warp_sort_regs_desc(unsigned long long (&a)[R])
 {
     const int lane = threadIdx.x & 31;
-    // position of a: lane, of b: lane + 32
-    for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+    for (int size = 2; size <= 32 * R; size <<= 1) {
+#pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride == 32) {
-                // partner of position p is p ^ 32: a <-> b of the same lane
-                const bool desc = true;  // size == 64 here
-                if ((a < b) == desc) {
-                    const unsigned long long t = a;
-                    a = b;
-                    b = t;
+            if (stride >= 32) {
+                const int qs = stride >> 5;
+#pragma unroll
+                for (int q = 0; q < R; ++q) {
+                    if ((q & qs) == 0) {
+                        const int p = q | qs;
+                        const bool desc = ((q * 32) & size) == 0;
+                        const unsigned long long x = a[q], y = a[p];
+                        const bool sw = desc ? (x < y) : (x > y);
+                        a[q] = sw ? y : x;
+                        a[p] = sw ? x : y;
+                    }
                 }
             } else {
-                const unsigned long long pa = __shfl_xor_sync(0xffffffffu, a, stride);
-                const unsigned long long pb = __shfl_xor_sync(0xffffffffu, b, stride);
-                const int posA = lane, posB = lane + 32;
-                const bool lowA = (posA & stride) == 0, lowB = (posB & stride) == 0;
-                const bool descA = (posA & size) == 0, descB = (posB & size) == 0;
-                // the lower position keeps the larger value when sorting descending
-                const bool keepMaxA = (lowA == descA);
-                const bool keepMaxB = (lowB == descB);
-                a = keepMaxA ? (a > pa ? a : pa) : (a < pa ? a : pa);
-                b = keepMaxB ? (b > pb ? b : pb) : (b < pb ? b : pb);
+#pragma unroll
+                for (int q = 0; q < R; ++q) {
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, a[q], stride);
+                    const bool low = (lane & stride) == 0;
+                    const bool desc = ((q * 32 + lane) & size) == 0;
+                    const bool keep_max = low == desc;
+                    a[q] = keep_max ? (a[q] > o ? a[q] : o) : (a[q] < o ? a[q] : o);
+                }
             }
         }
     }
@@ -185,7 +193,7 @@ __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n
     for (int size = 2; size <= np2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             for (int t = lane; t < (np2 >> 1); t += 32) {
-                const int lo = 2 * stride * (t / stride) + (t % stride);
+                const int lo = ((t & ~(stride - 1)) << 1) | (t & (stride - 1));
                 const int hi = lo + stride;
                 const bool desc = (lo & size) == 0;
                 const unsigned long long x = a[lo], y = a[hi];
@@ -197,6 +205,32 @@ __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n
             __syncwarp();
         }
     }
+}
+
+// The largest key t with at least c of the warp's keys >= t (keys k[i] of lanes
+// where bit i of `valid` is set; the caller guarantees at least c of them).
+// Radix-4 from the top: three counts per step, 16 steps.
+template <int R>
+__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&k)[R], uint32_t valid, int c)
+{
+    uint32_t prefix = 0;
+#pragma unroll 1
+    for (int b = 30; b >= 0; b -= 2) {
+        const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
+        int n1 = 0, n2 = 0, n3 = 0;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const bool ok = (valid >> i) & 1u;
+            n1 += (ok && k[i] >= c1) ? 1 : 0;
+            n2 += (ok && k[i] >= c2) ? 1 : 0;
+            n3 += (ok && k[i] >= c3) ? 1 : 0;
+        }
+        n1 = __reduce_add_sync(0xffffffffu, n1);
+        n2 = __reduce_add_sync(0xffffffffu, n2);
+        n3 = __reduce_add_sync(0xffffffffu, n3);
+        prefix = n3 >= c ? c3 : (n2 >= c ? c2 : (n1 >= c ? c1 : prefix));
+    }
+    return prefix;
 }
 
 }  // namespace col

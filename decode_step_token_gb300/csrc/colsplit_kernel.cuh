@@ -355,22 +355,33 @@ __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const ui
 }
 
 // ---------------------------------------------------------------- word sorts
-// Sort buf[0, n) descending, n <= kBufCap: in registers when it fits 64 words.
-__device__ __forceinline__ void sort_buf(unsigned long long* buf, int n)
+// Sort buf[0, n) descending, n <= kBufCap: in registers up to 128 words.
+__device__ __noinline__ void sort_buf(unsigned long long* buf, int n)
 {
     const int lane = threadIdx.x & 31;
     if (n <= 1) return;
     if (n <= 64) {
-        unsigned long long a = lane < n ? buf[lane] : 0ull;
-        unsigned long long b = lane + 32 < n ? buf[lane + 32] : 0ull;
+        unsigned long long a[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) a[q] = q * 32 + lane < n ? buf[q * 32 + lane] : 0ull;
         __syncwarp();
-        warp_sort64_desc(a, b);
-        if (lane < n) buf[lane] = a;
-        if (lane + 32 < n) buf[lane + 32] = b;
+        warp_sort_regs_desc<2>(a);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (q * 32 + lane < n) buf[q * 32 + lane] = a[q];
+    } else if (n <= 128) {
+        unsigned long long a[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) a[q] = q * 32 + lane < n ? buf[q * 32 + lane] : 0ull;
         __syncwarp();
+        warp_sort_regs_desc<4>(a);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q * 32 + lane < n) buf[q * 32 + lane] = a[q];
     } else {
         warp_sort_smem_desc(buf, n);
     }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- truncated units
@@ -408,11 +419,8 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
     }
     const uint32_t flags = unit_flags(mx, nan);
     warp_maxidx(mx, am);
-    unsigned long long ga = (static_cast<unsigned long long>(f2key(gm0)) << 32) | uint32_t(lane);
-    unsigned long long gb = (static_cast<unsigned long long>(f2key(gm1)) << 32) | uint32_t(lane + 32);
-    warp_sort64_desc(ga, gb);
-    const unsigned long long tw = __shfl_sync(0xffffffffu, C <= 32 ? ga : gb, (C - 1) & 31);
-    const float tau = key2f(uint32_t(tw >> 32));
+    const uint32_t gk[2] = {f2key(gm0), f2key(gm1)};
+    const float tau = key2f(warp_kth_key<2>(gk, 3u, C));
     // gather x >= tau (finite) and, for top-p without top-k, the unit's softmax mass
     int cnt = 0;
     float zs = 0.0f, zc = 0.0f;
@@ -503,52 +511,247 @@ __device__ __forceinline__ GRec cand_grec(const RowInfo& ri, float x, int v)
     return GRec{x * ri.invT - fast_ln_exp1(w, __log2f(w), word), v, x, word};
 }
 
-// Append to buf[n, ...) every listed word >= t among the first `lim` entries of
-// each unit's list; returns the new count (which may pass kBufCap: then only
-// the first kBufCap words are stored). Lists are read 8 words at a time and a
-// list is left at its first word below t.
-__device__ __forceinline__ int gather_lists(const ColRec* rr, int G, int lim, unsigned long long t,
+// Append to buf[n, ...) every listed word whose value key is >= vt, reading
+// each list from its head 8 words at a time and leaving it at its first word
+// below vt; returns the new count (only the first kBufCap words are stored).
+__device__ __forceinline__ int gather_lists(const ColRec* rr, int G, const uint32_t (&nc)[kLPL], uint32_t vt,
                                             unsigned long long* buf, int n)
 {
     const int lane = threadIdx.x & 31;
+    int len[kLPL];
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) len[q] = int(nc[q]);
 #pragma unroll 1
-    for (int s0 = 0; s0 < G; s0 += 32) {
-        const int s = s0 + lane;
-        int len = s < G ? min(lim, int(__ldcg(&rr[s].nc))) : 0;
-#pragma unroll 1
-        for (int i0 = 0; __any_sync(0xffffffffu, i0 < len); i0 += 8) {
-            unsigned long long w[8];
-            if (i0 < len) {
+    for (int i0 = 0; i0 < kCandCap; i0 += 8) {
+        bool more = false;
+#pragma unroll
+        for (int q = 0; q < kLPL; ++q) more |= i0 < len[q];
+        if (!__any_sync(0xffffffffu, more)) break;
+        unsigned long long w[kLPL][8];
+#pragma unroll
+        for (int q = 0; q < kLPL; ++q) {
+            const int s = lane + 32 * q;
+            if (i0 < len[q]) {
                 const uint4* src = reinterpret_cast<const uint4*>(&rr[s].cand[i0]);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const uint4 x = __ldcg(src + h);
-                    w[2 * h] = (static_cast<unsigned long long>(x.y) << 32) | x.x;
-                    w[2 * h + 1] = (static_cast<unsigned long long>(x.w) << 32) | x.z;
+                    w[q][2 * h] = (static_cast<unsigned long long>(x.y) << 32) | x.x;
+                    w[q][2 * h + 1] = (static_cast<unsigned long long>(x.w) << 32) | x.z;
                 }
             } else {
 #pragma unroll
-                for (int h = 0; h < 8; ++h) w[h] = 0ull;
+                for (int h = 0; h < 8; ++h) w[q][h] = 0ull;
             }
+        }
+#pragma unroll
+        for (int q = 0; q < kLPL; ++q) {
+            if (!__any_sync(0xffffffffu, i0 < len[q])) continue;
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
-                const bool take = i0 + h < len && w[h] >= t;
+                const bool take = i0 + h < len[q] && cand_key(w[q][h]) >= vt;
                 const unsigned bt = __ballot_sync(0xffffffffu, take);
                 if (take) {
                     const int pos = n + __popc(bt & ((1u << lane) - 1u));
-                    if (pos < kBufCap) buf[pos] = w[h];
+                    if (pos < kBufCap) buf[pos] = w[q][h];
                 }
                 n += __popc(bt);
             }
-            if (!(w[7] >= t)) len = 0;  // sorted: the rest of this list is below t
+            if (!(cand_key(w[q][7]) >= vt)) len[q] = 0;  // sorted: the rest is below vt
         }
     }
     __syncwarp();
     return n;
 }
 
+// The kept set of a truncated row from its units' lists; returns the token, or
+// sets `fallback` when the lists cannot settle it. hd: the headers of the
+// lane's lists (list lane + 32 q).
+__device__ __noinline__ int finish_cand(const ColParams& P, unsigned long long* buf, const RowInfo ri,
+                                        const ColRec* rr, const uint32_t (&nc)[kLPL], float m, bool& fallback)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = P.gc;
+    const bool small_k = ri.small_k;
+    const int C = small_k ? ri.k : kCandCap;
+    int token = -1;
+    if (ri.do_topk && !small_k) {
+        fallback = true;
+        return -1;
+    }
+    // one round trip: the C-th word of every list, and a sample of h words from
+    // the head of every list (G h >= C of them when the lists hold that many)
+    const int h = min(C, (C + G - 1) / G);
+    const int ns = G * h;  // <= G + C - 1 <= 191
+    constexpr int kSPL = 6;
+    unsigned long long tail[kLPL];
+    uint32_t sk[kSPL];
+    uint32_t sok = 0;
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) {
+        const int s = lane + 32 * q;
+        tail[q] = (s < G && nc[q] == uint32_t(C)) ? __ldcg(&rr[s].cand[C - 1]) : 0ull;
+    }
+#pragma unroll
+    for (int t = 0; t < kSPL; ++t) {
+        const int j = lane + 32 * t;
+        sk[t] = 0u;
+        if (j < ns) {
+            const int s = j / h, i = j - s * h;
+            const uint32_t n_s = __ldcg(&rr[s].nc);
+            const unsigned long long w = __ldcg(&rr[s].cand[i]);
+            if (uint32_t(i) < n_s) {
+                sk[t] = cand_key(w);
+                sok |= 1u << t;
+            }
+        }
+    }
+    bool overflow = false;
+    unsigned long long tau_inc = 0ull;  // tokens missing from every list lie below it
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) {
+        overflow |= nc[q] == kOverflow;
+        tau_inc = tail[q] > tau_inc ? tail[q] : tau_inc;
+    }
+    if (__any_sync(0xffffffffu, overflow)) {
+        fallback = true;
+        return -1;
+    }
+    tau_inc = warp_max_u64(tau_inc);
+    const int nvalid = __reduce_add_sync(0xffffffffu, __popc(sok));
+    // every word whose value reaches the C-th sampled value: the row's top C and ties
+    const uint32_t vt = nvalid >= C ? warp_kth_key<kSPL>(sk, sok, C) : 0u;
+    const int n0 = gather_lists(rr, G, nc, vt, buf, 0);
+    if (n0 > kBufCap || n0 == 0) {
+        fallback = true;
+        return -1;
+    }
+    sort_buf(buf, n0);
+    const int lim = min(n0, kKeepCap);
+    const int nk = small_k ? min(ri.k, n0) : lim;
+    const int iA = lane, iB = lane + 32;
+    const unsigned long long cA = iA < lim ? buf[iA] : 0ull;
+    const unsigned long long cB = iB < lim ? buf[iB] : 0ull;
+    const float xA = key2f(cand_key(cA)), xB = key2f(cand_key(cB));
+    const int idxA = cand_idx(cA), idxB = cand_idx(cB);
+    auto complete = [&](int i) { return i < 0 || buf[i] >= tau_inc; };
+    int np = nk;
+    if (ri.do_topp) {
+        // prefix masses in fp32; redone in double when a prefix lies near the cut
+        const float eA = iA < nk ? __expf((xA - m) * ri.invT) : 0.0f;
+        const float eB = iB < nk ? __expf((xB - m) * ri.invT) : 0.0f;
+        float sA = eA, sB = eB;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float oA = __shfl_up_sync(0xffffffffu, sA, off);
+            const float oB = __shfl_up_sync(0xffffffffu, sB, off);
+            if (lane >= off) {
+                sA += oA;
+                sB += oB;
+            }
+        }
+        sB += __shfl_sync(0xffffffffu, sA, 31);
+        float Z;
+        if (small_k) {
+            Z = __shfl_sync(0xffffffffu, sB, 31);
+        } else {
+            float z = 0.0f;
+            for (int s = lane; s < G; s += 32) {
+                const float mxs = __ldcg(&rr[s].mx);
+                if (!(mxs > -INFINITY)) continue;
+                const float zs = __ldcg(&rr[s].zs) - __ldcg(&rr[s].zc);
+                z += zs * __expf((mxs - m) * ri.invT);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+            Z = z;
+        }
+        const float pz = ri.p * Z;
+        const float exA = sA - eA, exB = sB - eB;
+        const float tol = 1e-4f * Z;
+        const bool nearcut = __any_sync(0xffffffffu, (iA < nk && fabsf(exA - pz) < tol) ||
+                                                         (iB < nk && fabsf(exB - pz) < tol));
+        if (!nearcut) {
+            const bool kA = iA < nk && (exA < pz || iA == 0);
+            const bool kB = iB < nk && (exB < pz);
+            np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
+        } else {
+            // close to the cut: the same walk in double
+            const double Te = double(ri.Te);
+            const double y0 = double(m) / Te;
+            const double dA = iA < nk ? exp(double(xA) / Te - y0) : 0.0;
+            const double dB = iB < nk ? exp(double(xB) / Te - y0) : 0.0;
+            double qA = dA, qB = dB;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const double oA = __shfl_up_sync(0xffffffffu, qA, off);
+                const double oB = __shfl_up_sync(0xffffffffu, qB, off);
+                if (lane >= off) {
+                    qA += oA;
+                    qB += oB;
+                }
+            }
+            qB += __shfl_sync(0xffffffffu, qA, 31);
+            double ZD;
+            if (small_k) {
+                ZD = __shfl_sync(0xffffffffu, qB, 31);
+            } else {
+                double z = 0.0;
+                for (int s = lane; s < G; s += 32) {
+                    const float mxs = __ldcg(&rr[s].mx);
+                    if (!(mxs > -INFINITY)) continue;
+                    const double zs = double(__ldcg(&rr[s].zs)) - double(__ldcg(&rr[s].zc));
+                    z += zs * exp((double(mxs) - double(m)) / Te);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+                ZD = z;
+            }
+            const double pzd = double(ri.p) * ZD;
+            const bool kA = iA < nk && ((qA - dA) < pzd || iA == 0);
+            const bool kB = iB < nk && ((qB - dB) < pzd);
+            np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
+        }
+        if (!small_k && np >= lim) fallback = true;
+    } else if (!small_k) {
+        np = lim;
+    }
+    int nkept = np;
+    if (ri.do_minp) {
+        const double th = double(m) + double(ri.Te) * log(double(ri.minp));
+        float xthr = float(th);
+        if (double(xthr) < th) xthr = nextafterf(xthr, INFINITY);
+        const bool mA = iA < np && xA >= xthr;
+        const bool mB = iB < np && xB >= xthr;
+        nkept = __popc(__ballot_sync(0xffffffffu, mA)) + __popc(__ballot_sync(0xffffffffu, mB));
+        nkept = max(nkept, 1);
+        if (!small_k && !ri.do_topp && nkept >= lim) fallback = true;
+    } else if (!small_k && !ri.do_topp) {
+        fallback = true;
+    }
+    if (!fallback) {
+        // every kept token must be known exactly, and so must the first dropped
+        // one when min-p or top-p (not top-k) closed the set
+        if (!complete(nkept - 1)) fallback = true;
+        if (small_k && !complete(nk - 1)) fallback = true;
+        if (nkept < (small_k ? nk : lim) && !complete(nkept)) fallback = true;
+    }
+    if (!fallback) {
+        GTop2 t;
+        t.a = grec_empty();
+        t.b = grec_empty();
+        if (iA < nkept) top2_insert(t, cand_grec(ri, xA, idxA));
+        if (iB < nkept) top2_insert(t, cand_grec(ri, xB, idxB));
+        top2_warp_reduce(t);
+        token = settle_fast(t, ri.T);
+    }
+    __syncwarp();
+    return token;
+}
+
 // Finish row r from its records (one warp). Returns 1 when the row needs the
-// CTA-wide exact path (m and amax are returned for it), 0 otherwise.
+// CTA-wide exact path (m and amax are returned for it), 0 otherwise. Loads of
+// the G <= kMaxUnits records are issued together (kLPL per lane).
 __device__ __noinline__ int finish_row(const ColParams& P, unsigned long long* buf, const int r,
                                        const RowInfo ri, float* m_out, int* amax_out)
 {
@@ -558,17 +761,35 @@ __device__ __noinline__ int finish_row(const ColParams& P, unsigned long long* b
     const ColRec* rr = P.rec + int64_t(r) * G;
     __threadfence();
 
+    uint4 hd[kLPL];
+    GTop2 t;
+    t.a = grec_empty();
+    t.b = grec_empty();
+    const bool plain = ri.cls == kClsPlain;
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) {
+        const int s = lane + 32 * q;
+        hd[q] = s < G ? __ldcg(reinterpret_cast<const uint4*>(&rr[s]))  // mx, amax, flags, nc
+                      : make_uint4(0xFF800000u, uint32_t(INT_MAX), 0u, 0u);
+        if (plain && s < G) {
+            const uint4 ua = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g0));
+            const uint4 ub = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g1));
+            top2_insert(t, GRec{__uint_as_float(ua.x), int(ua.y), __uint_as_float(ua.z), ua.w});
+            top2_insert(t, GRec{__uint_as_float(ub.x), int(ub.y), __uint_as_float(ub.z), ub.w});
+        }
+    }
     float m = -INFINITY;
     int am = INT_MAX;
     uint32_t fl = 0;
-    for (int s = lane; s < G; s += 32) {
-        const uint4 h = __ldcg(reinterpret_cast<const uint4*>(&rr[s]));  // mx, amax, flags, nc
-        fl |= h.z;
-        maxidx_merge(m, am, __uint_as_float(h.x), int(h.y));
+    uint32_t nc[kLPL];
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) {
+        fl |= hd[q].z;
+        maxidx_merge(m, am, __uint_as_float(hd[q].x), int(hd[q].y));
+        nc[q] = hd[q].w;
     }
     warp_maxidx(m, am);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) fl |= __shfl_xor_sync(0xffffffffu, fl, off);
+    fl = __reduce_or_sync(0xffffffffu, fl);
     int status = ri.status;
     if (status == kRowOk) {
         if (fl & kFlagNonFinite) status = kRowNonFinite;
@@ -582,176 +803,11 @@ __device__ __noinline__ int finish_row(const ColParams& P, unsigned long long* b
         token = -1;
     } else if (ri.cls == kClsGreedy) {
         token = am;
-    } else if (ri.cls == kClsPlain) {
-        GTop2 t;
-        t.a = grec_empty();
-        t.b = grec_empty();
-        for (int s = lane; s < G; s += 32) {
-            const uint4 ua = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g0));
-            const uint4 ub = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g1));
-            top2_insert(t, GRec{__uint_as_float(ua.x), int(ua.y), __uint_as_float(ua.z), ua.w});
-            top2_insert(t, GRec{__uint_as_float(ub.x), int(ub.y), __uint_as_float(ub.z), ub.w});
-        }
+    } else if (plain) {
         top2_warp_reduce(t);
         token = settle_fast(t, ri.T);
     } else {
-        // ---- truncated row: merge the units' lists
-        const bool small_k = ri.small_k;
-        const int C = small_k ? ri.k : kCandCap;
-        if (ri.do_topk && !small_k) fallback = true;
-        // tokens missing from every list lie below tau_inc, the largest C-th entry
-        // of a full list
-        unsigned long long tau_inc = 0ull;
-        bool overflow = false;
-        for (int s = lane; s < G; s += 32) {
-            const uint32_t nc = __ldcg(&rr[s].nc);
-            if (nc == kOverflow) {
-                overflow = true;
-            } else if (nc == uint32_t(C)) {
-                const unsigned long long c = __ldcg(&rr[s].cand[C - 1]);
-                tau_inc = c > tau_inc ? c : tau_inc;
-            }
-        }
-        overflow = __any_sync(0xffffffffu, overflow);
-        tau_inc = warp_max_u64(tau_inc);
-        fallback = fallback || overflow;
-        int n0 = 0;
-        if (!fallback) {
-            // t1: the C-th largest of the lists' first h words; every word >= t1 of
-            // every list then holds the row's top C
-            const int h = min(C, (C + G - 1) / G);
-            const int ns = gather_lists(rr, G, h, 0ull, buf, 0);
-            unsigned long long t1 = 0ull;
-            if (ns >= C) {
-                sort_buf(buf, min(ns, kBufCap));
-                t1 = buf[C - 1];
-                __syncwarp();
-            }
-            n0 = gather_lists(rr, G, kCandCap, t1, buf, 0);
-            if (n0 > kBufCap || n0 == 0) fallback = true;
-        }
-        if (!fallback) {
-            sort_buf(buf, n0);
-            const int lim = min(n0, kKeepCap);
-            const int nk = small_k ? min(ri.k, n0) : lim;
-            const int iA = lane, iB = lane + 32;
-            const unsigned long long cA = iA < lim ? buf[iA] : 0ull;
-            const unsigned long long cB = iB < lim ? buf[iB] : 0ull;
-            const float xA = key2f(cand_key(cA)), xB = key2f(cand_key(cB));
-            const int idxA = cand_idx(cA), idxB = cand_idx(cB);
-            auto complete = [&](int i) { return i < 0 || buf[i] >= tau_inc; };
-            int np = nk;
-            if (ri.do_topp) {
-                // prefix masses in fp32; redone in double when a prefix lies near the cut
-                const float eA = iA < nk ? __expf((xA - m) * ri.invT) : 0.0f;
-                const float eB = iB < nk ? __expf((xB - m) * ri.invT) : 0.0f;
-                float sA = eA, sB = eB;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float oA = __shfl_up_sync(0xffffffffu, sA, off);
-                    const float oB = __shfl_up_sync(0xffffffffu, sB, off);
-                    if (lane >= off) {
-                        sA += oA;
-                        sB += oB;
-                    }
-                }
-                sB += __shfl_sync(0xffffffffu, sA, 31);
-                float Z;
-                if (small_k) {
-                    Z = __shfl_sync(0xffffffffu, sB, 31);
-                } else {
-                    float z = 0.0f;
-                    for (int s = lane; s < G; s += 32) {
-                        const float mxs = __ldcg(&rr[s].mx);
-                        if (!(mxs > -INFINITY)) continue;
-                        const float zs = __ldcg(&rr[s].zs) - __ldcg(&rr[s].zc);
-                        z += zs * __expf((mxs - m) * ri.invT);
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-                    Z = z;
-                }
-                const float pz = ri.p * Z;
-                const float exA = sA - eA, exB = sB - eB;
-                const float tol = 1e-4f * Z;
-                const bool nearcut = __any_sync(0xffffffffu, (iA < nk && fabsf(exA - pz) < tol) ||
-                                                                 (iB < nk && fabsf(exB - pz) < tol));
-                if (!nearcut) {
-                    const bool kA = iA < nk && (exA < pz || iA == 0);
-                    const bool kB = iB < nk && (exB < pz);
-                    np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
-                } else {
-                    // close to the cut: the same walk in double
-                    const double Te = double(ri.Te);
-                    const double y0 = double(m) / Te;
-                    const double dA = iA < nk ? exp(double(xA) / Te - y0) : 0.0;
-                    const double dB = iB < nk ? exp(double(xB) / Te - y0) : 0.0;
-                    double qA = dA, qB = dB;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const double oA = __shfl_up_sync(0xffffffffu, qA, off);
-                        const double oB = __shfl_up_sync(0xffffffffu, qB, off);
-                        if (lane >= off) {
-                            qA += oA;
-                            qB += oB;
-                        }
-                    }
-                    qB += __shfl_sync(0xffffffffu, qA, 31);
-                    double ZD;
-                    if (small_k) {
-                        ZD = __shfl_sync(0xffffffffu, qB, 31);
-                    } else {
-                        double z = 0.0;
-                        for (int s = lane; s < G; s += 32) {
-                            const float mxs = __ldcg(&rr[s].mx);
-                            if (!(mxs > -INFINITY)) continue;
-                            const double zs = double(__ldcg(&rr[s].zs)) - double(__ldcg(&rr[s].zc));
-                            z += zs * exp((double(mxs) - double(m)) / Te);
-                        }
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-                        ZD = z;
-                    }
-                    const double pzd = double(ri.p) * ZD;
-                    const bool kA = iA < nk && ((qA - dA) < pzd || iA == 0);
-                    const bool kB = iB < nk && ((qB - dB) < pzd);
-                    np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
-                }
-                if (!small_k && np >= lim) fallback = true;
-            } else if (!small_k) {
-                np = lim;
-            }
-            int nkept = np;
-            if (ri.do_minp) {
-                const double th = double(m) + double(ri.Te) * log(double(ri.minp));
-                float xthr = float(th);
-                if (double(xthr) < th) xthr = nextafterf(xthr, INFINITY);
-                const bool mA = iA < np && xA >= xthr;
-                const bool mB = iB < np && xB >= xthr;
-                nkept = __popc(__ballot_sync(0xffffffffu, mA)) + __popc(__ballot_sync(0xffffffffu, mB));
-                nkept = max(nkept, 1);
-                if (!small_k && !ri.do_topp && nkept >= lim) fallback = true;
-            } else if (!small_k && !ri.do_topp) {
-                fallback = true;
-            }
-            if (!fallback) {
-                // every kept token must be known exactly, and so must the first dropped
-                // one when min-p or top-p (not top-k) closed the set
-                if (!complete(nkept - 1)) fallback = true;
-                if (small_k && !complete(nk - 1)) fallback = true;
-                if (nkept < (small_k ? nk : lim) && !complete(nkept)) fallback = true;
-            }
-            if (!fallback) {
-                GTop2 t;
-                t.a = grec_empty();
-                t.b = grec_empty();
-                if (iA < nkept) top2_insert(t, cand_grec(ri, xA, idxA));
-                if (iB < nkept) top2_insert(t, cand_grec(ri, xB, idxB));
-                top2_warp_reduce(t);
-                token = settle_fast(t, ri.T);
-            }
-        }
-        __syncwarp();
+        token = finish_cand(P, buf, ri, rr, nc, m, fallback);
     }
     if (lane == 0) {
         if (!fallback) {

@@ -148,13 +148,13 @@ int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
     return SAMPLER_OK;
 }
 
-// Units of one row: about one per warp of the GPU, between kUnitMinBytes (or the
+// Units of one row: about one per warp of the GPU, between kUnitMinElems (or the
 // whole row) and one warp's slot; a multiple of 16 bytes.
 ColGeometry col_geometry(int64_t N, int64_t V, int esize, int sms)
 {
     ColGeometry g;
     const int64_t epv = 16 / esize;
-    const int64_t w_min = dst::col::kUnitMinBytes / esize;
+    const int64_t w_min = dst::col::kUnitMinElems;
     const int64_t w_max = dst::col::kSlotBytes / esize;
     const int64_t warps = int64_t(sms) * dst::col::kW;
     const int64_t g0 = std::max<int64_t>(1, warps / std::max<int64_t>(N, 1));
@@ -185,7 +185,7 @@ bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g)
     if (a->hist_offsets || a->out_probs || a->out_logprobs) return false;
     const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
     *g = col_geometry(a->n_rows, a->vocab, esize, h->num_sms);
-    return g->units <= h->col_units;
+    return g->units <= h->col_units && g->gc <= dst::col::kMaxUnits;
 }
 
 template <typename InT>
@@ -472,7 +472,7 @@ int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
     if (rc != SAMPLER_OK) return rc;
     const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
     const ColGeometry g = col_geometry(a->n_rows, a->vocab, bf ? 2 : 4, d.num_sms);
-    if (g.units > kNoAllocUnits) return SAMPLER_ERR_TOO_LARGE;
+    if (g.units > kNoAllocUnits || g.gc > dst::col::kMaxUnits) return SAMPLER_ERR_TOO_LARGE;
     void* fn = bf ? col_kernel<uint16_t>() : col_kernel<float>();
     rc = noalloc_grant_smem(dev, bf ? 1 : 0, fn, dst::col::kSmemBytes);
     if (rc != SAMPLER_OK) return rc;
