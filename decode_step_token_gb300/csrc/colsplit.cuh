@@ -1,24 +1,33 @@
 // colsplit.cuh -- the unit-split sampler kernel for small batches (sm_103a).
 //
-// Each row is cut into G equal vocabulary units; the N x G units are spread
-// over every warp of the GPU (one CTA of 16 warps per SM), one unit per warp
-// when the batch allows. A warp copies its unit into its own shared-memory slot
-// with 16-byte asynchronous copies in four groups and starts on the first group
-// while the rest are in flight. It then writes a summary record of the unit to
-// global memory and bumps the row's arrival counter with a release atomic. The
-// warp that brings a counter to G finishes the row from the G records:
+// Each row is cut into G equal vocabulary units, and the N x G units are spread
+// over every warp of a cooperative grid (one CTA of 16 warps per SM), one unit
+// per warp when the batch allows. The kernel runs in two phases split by one
+// grid-wide barrier:
 //
-//   greedy rows     argmax of the unit maxima (lowest index on ties)
-//   plain rows      the best two Gumbel scores of every unit, settled in double
-//   truncated rows  each unit's own top-C list (C = k when k <= 64, else 64),
-//                   merged into the row's sorted top list; top-k / top-p /
-//                   min-p cut in double, Gumbel-max over the kept tokens
+//   phase 1  a warp copies its unit into its own shared-memory slot (16-byte
+//            cp.async copies in four groups; work starts on the first while the
+//            rest land) and writes a summary record of the unit:
+//              greedy rows     the unit's maximum and its lowest index
+//              plain rows      the unit's best two Gumbel scores (fp32)
+//              truncated rows  tau, the C-th largest of 128 group maxima
+//                              (C = k when k <= 64, else 64), and every token
+//                              of the unit at or above it (unsorted; at least
+//                              C of them, so the unit's top C are among them)
+//   phase 2  rows are dealt round-robin to the CTAs. A greedy or plain row is
+//            finished by one warp from its G records (the best two Gumbel
+//            scores settled in double). A truncated row is finished by the whole
+//            CTA: every listed token at or above the largest tau of the row is
+//            gathered -- exactly the row's tokens above that value, which hold
+//            its top C -- ranked, then top-k / top-p / min-p are cut in double
+//            and the Gumbel-max pick is taken over the kept tokens.
 //
-// A truncated row whose kept set reaches below what the lists cover is pushed
-// to its finishing CTA, which samples it exactly once all its units are done
-// (radix select by count or fixed-point softmax mass, then a Gumbel pass). The
-// finishing warp resets the row's counter, so the workspace is clean for the
-// next launch. Nothing waits on another CTA: no co-residency is assumed.
+// A truncated row whose kept set reaches below what the lists cover is sampled
+// exactly by its phase-2 CTA, streaming the row from global memory (radix
+// select by count or fixed-point softmax mass, then a Gumbel pass). The grid
+// barrier is the only wait on other CTAs (the cooperative launch makes them
+// co-resident); it gives up after a bounded number of polls and marks the rows
+// SAMPLER_ROW_TIMEOUT.
 #pragma once
 
 #include "row_sampler.cuh"
@@ -28,16 +37,19 @@ namespace col {
 
 constexpr int kT = 512;
 constexpr int kW = kT / 32;
-constexpr int kSlotBytes = 9216;  // staged logits per warp: 4608 bf16 or 2304 fp32
-constexpr int kBufCap = 512;      // candidate words per warp
-constexpr int kCandCap = 64;      // candidates per unit record
-constexpr int kKeepCap = 64;      // kept tokens a finishing warp resolves
-constexpr int kStages = 4;        // copy groups per unit
+constexpr int kSlotBytes = 9216;   // staged logits per warp: 4608 bf16 or 2304 fp32
+constexpr int kSeg = 16;           // candidate words a lane may hold in phase 1
+constexpr int kBufCap = 32 * kSeg;
+constexpr int kUnitCands = 128;    // tokens a unit may gather at or above its tau
+constexpr int kCandCap = 64;       // top list of a row without a small top-k
+constexpr int kKeepCap = 64;       // kept tokens a finishing warp resolves
+constexpr int kSelCap = 512;       // tokens a phase-2 CTA gathers for one row
+constexpr int kStages = 4;         // copy groups per unit
 constexpr int kMaxRows = 256;
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
 constexpr int kUnitMinElems = 2048;  // smallest unit, unless a row is narrower
 constexpr int kMaxUnits = 128;       // units per row: 262144 / kUnitMinElems
-constexpr int kLPL = kMaxUnits / 32; // a finishing warp's lists per lane
+constexpr int kLPL = kMaxUnits / 32; // a finishing warp's records per lane
 
 enum : uint8_t { kClsErr = 0, kClsGreedy = 1, kClsPlain = 2, kClsCand = 3 };
 
@@ -45,12 +57,20 @@ struct alignas(16) ColRec {  // one (row, unit) summary
     float mx;      // unit maximum (NaN ignored)
     int32_t amax;  // its lowest index
     uint32_t flags;
-    uint32_t nc;   // candidates listed, kOverflow if the unit could not bound them
+    uint32_t nc;   // candidates listed, kOverflow if they did not fit
     GRec g0, g1;   // plain rows: the unit's best two Gumbel scores
     float zs;      // top-p rows without top-k: sum of exp((x - mx) / T), compensated
     float zc;      // its compensation term
-    float pad0, pad1;
-    unsigned long long cand[kCandCap];  // truncated rows: top list, descending
+    uint32_t tau;  // truncated rows: order key of the C-th largest group maximum
+    uint32_t pad;
+    unsigned long long cand[kCandCap];  // truncated rows: the unit's top list, descending
+};
+
+struct GridBar {      // grid barrier state, zero-initialised once
+    uint32_t count;   // CTAs arrived (back to 0 after every barrier)
+    uint32_t gen;     // bumped by the last arrival
+    uint32_t poison;  // set when a CTA gave up waiting: later barriers fail at once
+    uint32_t pad;
 };
 
 struct ColParams {
@@ -60,7 +80,7 @@ struct ColParams {
     int32_t w;        // elements per unit (a multiple of 16 bytes)
     int32_t n_units;  // n_rows * gc
     ColRec* rec;      // [n_rows][gc]
-    uint32_t* counters;  // [n_rows], zero between launches
+    GridBar* bar;
     unsigned long long* stats;  // [0] rows finished by the exact path (diagnostic)
 };
 
@@ -75,12 +95,18 @@ struct alignas(16) RowInfo {
 };
 
 struct alignas(16) ColShared {
-    int32_t fallback_rows[kMaxRows];
+    int32_t fallback_rows[kMaxRows];  // rows for the exact path, with their max / argmax
     float fb_m[kMaxRows];
     int32_t fb_amax[kMaxRows];
     int32_t n_fallback;
-    int32_t pad_;
-    unsigned long long offset;  // Philox counter words 2-3 for this launch
+    int32_t bar_ok;
+    // phase 2, the truncated row being finished
+    float fin_m;
+    int32_t fin_amax;
+    uint32_t fin_flags;
+    uint32_t fin_over;
+    int32_t n_sel;
+    unsigned long long fin_tinc;  // tokens missing from every list lie below it
     // CTA-wide scratch for the exact fallback
     uint32_t hcnt[256];
     unsigned long long hmass[256];
@@ -99,6 +125,9 @@ constexpr size_t kSharedHead = (sizeof(ColShared) + 127) & ~size_t(127);
 constexpr size_t kWarpBytes = size_t(kSlotBytes) + size_t(kBufCap) * 8;
 constexpr size_t kSmemBytes = kSharedHead + kW * kWarpBytes;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// phase 2 reuses the warps' slots: the records' lists, then the gathered tokens
+static_assert(size_t(kMaxUnits) * (kCandCap * 8 + 7 * 4) + size_t(kSelCap) * 20 <= kW * kWarpBytes,
+              "phase-2 area");
 
 __device__ __forceinline__ RowParams as_row_params(const RowInfo& ri)
 {
@@ -144,45 +173,43 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Bitonic sort, descending, of the 32 R words a warp holds in registers: word q
-// of lane l is element 32 q + l. Strides of 32 and more swap registers within a
-// lane; shorter ones exchange with a shuffle.
-template <int R>
-__device__ __forceinline__ void warp_sort_regs_desc(unsigned long long (&a)[R])
+// Bitonic sort, descending, of the 128 keys a warp holds four per lane (key q of
+// lane l is element 32 q + l). The stage loop stays rolled: one short body.
+__device__ __forceinline__ void warp_sort128_u32_desc(uint32_t (&a)[4])
 {
     const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int size = 2; size <= 32 * R; size <<= 1) {
-#pragma unroll
+#pragma unroll 1
+    for (int size = 2; size <= 128; size <<= 1) {
+#pragma unroll 1
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             if (stride >= 32) {
-                const int qs = stride >> 5;
+                const int qs = stride >> 5;  // 1 or 2
 #pragma unroll
-                for (int q = 0; q < R; ++q) {
-                    if ((q & qs) == 0) {
-                        const int p = q | qs;
+                for (int q = 0; q < 4; ++q) {
+                    const int p = q ^ qs;
+                    if (p > q) {
                         const bool desc = ((q * 32) & size) == 0;
-                        const unsigned long long x = a[q], y = a[p];
+                        const uint32_t x = a[q], y = a[p];
                         const bool sw = desc ? (x < y) : (x > y);
                         a[q] = sw ? y : x;
                         a[p] = sw ? x : y;
                     }
                 }
             } else {
+                const bool low = (lane & stride) == 0;
 #pragma unroll
-                for (int q = 0; q < R; ++q) {
-                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, a[q], stride);
-                    const bool low = (lane & stride) == 0;
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t o = __shfl_xor_sync(0xffffffffu, a[q], stride);
                     const bool desc = ((q * 32 + lane) & size) == 0;
-                    const bool keep_max = low == desc;
-                    a[q] = keep_max ? (a[q] > o ? a[q] : o) : (a[q] < o ? a[q] : o);
+                    a[q] = (low == desc) ? max(a[q], o) : min(a[q], o);
                 }
             }
         }
     }
 }
 
-// Sort n <= kBufCap words in warp-private shared memory, descending (bitonic).
+// Sort n <= kBufCap words in warp-private shared memory, descending (bitonic,
+// padded to a power of two with zeros; the array must hold that many words).
 __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n)
 {
     const int lane = threadIdx.x & 31;
@@ -190,7 +217,9 @@ __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n
     while (np2 < n) np2 <<= 1;
     for (int i = n + lane; i < np2; i += 32) a[i] = 0ull;
     __syncwarp();
+#pragma unroll 1
     for (int size = 2; size <= np2; size <<= 1) {
+#pragma unroll 1
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             for (int t = lane; t < (np2 >> 1); t += 32) {
                 const int lo = ((t & ~(stride - 1)) << 1) | (t & (stride - 1));
@@ -207,30 +236,28 @@ __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n
     }
 }
 
-// The largest key t with at least c of the warp's keys >= t (keys k[i] of lanes
-// where bit i of `valid` is set; the caller guarantees at least c of them).
-// Radix-4 from the top: three counts per step, 16 steps.
-template <int R>
-__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&k)[R], uint32_t valid, int c)
+// Sort n <= kSelCap words in shared memory, descending, with the whole CTA: each
+// word's rank is the number of words above it (words are distinct), found by
+// kT / n threads per word, then the words are scattered. rank[] and out[] hold n.
+__device__ __forceinline__ void cta_rank_sort_desc(const unsigned long long* in, int n, uint32_t* rank,
+                                                   unsigned long long* out)
 {
-    uint32_t prefix = 0;
-#pragma unroll 1
-    for (int b = 30; b >= 0; b -= 2) {
-        const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
-        int n1 = 0, n2 = 0, n3 = 0;
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const bool ok = (valid >> i) & 1u;
-            n1 += (ok && k[i] >= c1) ? 1 : 0;
-            n2 += (ok && k[i] >= c2) ? 1 : 0;
-            n3 += (ok && k[i] >= c3) ? 1 : 0;
-        }
-        n1 = __reduce_add_sync(0xffffffffu, n1);
-        n2 = __reduce_add_sync(0xffffffffu, n2);
-        n3 = __reduce_add_sync(0xffffffffu, n3);
-        prefix = n3 >= c ? c3 : (n2 >= c ? c2 : (n1 >= c ? c1 : prefix));
+    const int tid = threadIdx.x;
+    for (int i = tid; i < n; i += kT) rank[i] = 0u;
+    __syncthreads();
+    const int per = n > 0 ? max(1, kT / n) : 1;  // threads per word
+    const int chunk = (n + per - 1) / per;
+    for (int t = tid; t < n * per; t += kT) {
+        const int i = t % n, c = t / n;
+        const unsigned long long x = in[i];
+        uint32_t above = 0;
+        const int j1 = min(n, (c + 1) * chunk);
+        for (int j = c * chunk; j < j1; ++j) above += in[j] > x ? 1u : 0u;
+        if (above) atomicAdd(&rank[i], above);
     }
-    return prefix;
+    __syncthreads();
+    for (int i = tid; i < n; i += kT) out[rank[i]] = in[i];
+    __syncthreads();
 }
 
 }  // namespace col

@@ -3,9 +3,9 @@
 // Per warp and unit: the unit's logits go to the warp's shared-memory slot by
 // 16-byte cp.async copies in kStages commit groups, the row's parameters are
 // read while they fly, and the class pass (greedy / plain / truncated) starts on
-// the first group as soon as it has landed. Loops over a unit's vectors stay
-// rolled, and every pass, the finisher and the exact path are out-of-line, which
-// keeps the code each warp runs small.
+// the first group as soon as it has landed. Loops stay rolled and every pass is
+// out-of-line: code that a warp runs once per launch is fetched cold, so it is
+// kept short.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -17,11 +17,23 @@ namespace col {
 
 static_assert(kStages == 4, "wait_stage below spells out four stages");
 
-__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t* p, uint32_t v)
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v)
 {
     uint32_t old;
-    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -259,7 +271,7 @@ __device__ __forceinline__ float bar_of(float s)
     return -(s - (1e-4f + 1e-6f * fabsf(s))) * 1.4426950408889634f;
 }
 
-__device__ __forceinline__ void plain_take(PlainAcc& a, float invT, int v, float x, uint32_t word)
+__device__ __noinline__ void plain_take(PlainAcc& a, float invT, int v, float x, uint32_t word)
 {
     const float w = noise_one_minus_u(word);
     const float s = x * invT - fast_ln_exp1(w, __log2f(w), word);
@@ -267,15 +279,6 @@ __device__ __forceinline__ void plain_take(PlainAcc& a, float invT, int v, float
         a.best = GRec{s, v, x, word};
         a.c2 = bar_of(s);
     }
-}
-
-template <int E>
-__device__ __forceinline__ float pickf(const float (&a)[E], int e)
-{
-    float r = a[0];
-#pragma unroll
-    for (int i = 1; i < E; ++i) r = (e == i) ? a[i] : r;
-    return r;
 }
 
 template <int E>
@@ -287,9 +290,52 @@ __device__ __forceinline__ uint32_t picku(const uint32_t (&a)[E], int e)
     return r;
 }
 
+template <typename InT>
+__device__ __forceinline__ uint4 neg_inf_vec()
+{
+    const uint32_t w = sizeof(InT) == 2 ? 0xFF80FF80u : 0xFF800000u;
+    return make_uint4(w, w, w, w);
+}
+
+// Philox words and entry mask of one vector: bit q is set when token vb + q may
+// beat the bar, i.e. x/T - ln(1 - u) clears it.
+template <typename InT>
+__device__ __forceinline__ uint32_t plain_mask(const uint4& raw, int vb, float a2, float c2,
+                                               const PhiloxSchedule& ks, uint32_t stream, uint32_t olo,
+                                               uint32_t ohi, uint32_t (&ws)[Vec<InT>::E])
+{
+    constexpr int EPV = Vec<InT>::E;
+#pragma unroll
+    for (int b = 0; b < EPV / 4; ++b) {
+        const uint4 blk = philox4x32_10(make_uint4(uint32_t(vb >> 2) + b, stream, olo, ohi), ks);
+        ws[4 * b + 0] = blk.x;
+        ws[4 * b + 1] = blk.y;
+        ws[4 * b + 2] = blk.z;
+        ws[4 * b + 3] = blk.w;
+    }
+    uint32_t mask = 0;
+#pragma unroll
+    for (int q = 0; q < EPV; ++q) {
+        const float lg2w = __log2f(noise_one_minus_u(ws[q]));
+        mask |= (fmaf(Vec<InT>::get(raw, q), a2, c2) > lg2w) ? (1u << q) : 0u;
+    }
+    return mask;
+}
+
+template <typename InT>
+__device__ __forceinline__ void plain_takes(PlainAcc& a, float invT, const uint4& raw, int vb, uint32_t mask,
+                                            const uint32_t (&ws)[Vec<InT>::E])
+{
+    while (mask) {
+        const int q = __ffs(mask) - 1;
+        mask &= mask - 1;
+        plain_take(a, invT, vb + q, Vec<InT>::get(raw, q), picku<Vec<InT>::E>(ws, q));
+    }
+}
+
 // Gumbel-max over the unit: a token may win only if x/T - ln(1 - u) clears the
 // lane's bar (its best score so far, less a margin); the exact score is taken
-// only for those.
+// only for those. Two vectors per step, for independent work to overlap.
 template <typename InT>
 __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const uint4* slot, ColRec* rec)
 {
@@ -297,7 +343,7 @@ __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const ui
     const int lane = threadIdx.x & 31;
     const float invT = ri.invT;
     const float a2 = invT * 1.4426950408889634f;
-    const PhiloxKey key{ri.key_lo, ri.key_hi};
+    const PhiloxSchedule ks = philox_schedule(PhiloxKey{ri.key_lo, ri.key_hi});
     const uint32_t stream = ri.stream, olo = ri.off_lo, ohi = ri.off_hi;
     PlainAcc a;
     a.best = grec_empty();
@@ -309,34 +355,19 @@ __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const ui
         wait_stage(st);
         const int e = min((st + 1) * u.q, u.nvec);
 #pragma unroll 1
-        for (int j = st * u.q + lane; j < e; j += 32) {
-            const int vb = u.v0 + j * EPV;  // a multiple of 4
-            const uint4 raw = slot[j];
-            bool vn;
-            lm = fmaxf(lm, Vec<InT>::vmax(raw, vn));
-            nan |= vn;
-            float xs[EPV];
-            uint32_t ws[EPV];
-#pragma unroll
-            for (int b = 0; b < EPV / 4; ++b) {
-                const uint4 blk = philox4x32_10(make_uint4(uint32_t(vb >> 2) + b, stream, olo, ohi), key);
-                ws[4 * b + 0] = blk.x;
-                ws[4 * b + 1] = blk.y;
-                ws[4 * b + 2] = blk.z;
-                ws[4 * b + 3] = blk.w;
-            }
-            uint32_t mask = 0;
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                xs[q] = Vec<InT>::get(raw, q);
-                const float lg2w = __log2f(noise_one_minus_u(ws[q]));
-                mask |= (fmaf(xs[q], a2, a.c2) > lg2w) ? (1u << q) : 0u;
-            }
-            while (mask) {
-                const int q = __ffs(mask) - 1;
-                mask &= mask - 1;
-                plain_take(a, invT, vb + q, pickf<EPV>(xs, q), picku<EPV>(ws, q));
-            }
+        for (int j = st * u.q + lane; j < e; j += 64) {
+            const int j2 = j + 32;
+            const uint4 r1 = slot[j];
+            const uint4 r2 = j2 < e ? slot[j2] : neg_inf_vec<InT>();
+            const int vb1 = u.v0 + j * EPV, vb2 = u.v0 + j2 * EPV;  // multiples of 4
+            bool n1, n2;
+            lm = fmaxf(lm, fmaxf(Vec<InT>::vmax(r1, n1), Vec<InT>::vmax(r2, n2)));
+            nan |= n1 || n2;
+            uint32_t w1[EPV], w2[EPV];
+            const uint32_t m1 = plain_mask<InT>(r1, vb1, a2, a.c2, ks, stream, olo, ohi, w1);
+            const uint32_t m2 = plain_mask<InT>(r2, vb2, a2, a.c2, ks, stream, olo, ohi, w2);
+            plain_takes<InT>(a, invT, r1, vb1, m1, w1);
+            plain_takes<InT>(a, invT, r2, vb2, m2, w2);
         }
     }
     const uint32_t flags = unit_flags(lm, nan);
@@ -354,41 +385,11 @@ __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const ui
     }
 }
 
-// ---------------------------------------------------------------- word sorts
-// Sort buf[0, n) descending, n <= kBufCap: in registers up to 128 words.
-__device__ __noinline__ void sort_buf(unsigned long long* buf, int n)
-{
-    const int lane = threadIdx.x & 31;
-    if (n <= 1) return;
-    if (n <= 64) {
-        unsigned long long a[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) a[q] = q * 32 + lane < n ? buf[q * 32 + lane] : 0ull;
-        __syncwarp();
-        warp_sort_regs_desc<2>(a);
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-            if (q * 32 + lane < n) buf[q * 32 + lane] = a[q];
-    } else if (n <= 128) {
-        unsigned long long a[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) a[q] = q * 32 + lane < n ? buf[q * 32 + lane] : 0ull;
-        __syncwarp();
-        warp_sort_regs_desc<4>(a);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (q * 32 + lane < n) buf[q * 32 + lane] = a[q];
-    } else {
-        warp_sort_smem_desc(buf, n);
-    }
-    __syncwarp();
-}
-
 // ---------------------------------------------------------------- truncated units
-// The unit's top-C list (C = k for k <= 64, else 64) by (value desc, index asc):
-// every element at or above tau, the C-th largest of 64 group maxima (each lane
-// keeps one maximum for its even and one for its odd vectors), is gathered and
-// sorted. At least C elements reach tau, so the list is exact.
+// The unit's top-C list (C = k for k <= 64, else 64), sorted by (value desc,
+// index asc): tau = the C-th largest of 128 group maxima (each lane deals its
+// vectors to four groups in turn) is reached by at least C of the unit's tokens,
+// so its top C are among the tokens >= tau, which are gathered and sorted.
 template <typename InT>
 __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uint4* slot,
                                        unsigned long long* buf, ColRec* rec)
@@ -396,7 +397,7 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
     constexpr int EPV = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
     const int C = ri.small_k ? ri.k : kCandCap;
-    float mx = -INFINITY, gm0 = -INFINITY, gm1 = -INFINITY;
+    float mx = -INFINITY, g0 = -INFINITY, g1 = -INFINITY, g2 = -INFINITY, g3 = -INFINITY;
     int am = INT_MAX;
     bool nan = false;
 #pragma unroll 1
@@ -413,29 +414,33 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
                 mx = m;
                 am = u.v0 + j * EPV + vec_find<InT>(raw, m);
             }
-            if ((j >> 5) & 1) gm1 = fmaxf(gm1, m);
-            else gm0 = fmaxf(gm0, m);
+            const float g = fmaxf(g0, m);  // this vector joins group 0, then the groups rotate
+            g0 = g1;
+            g1 = g2;
+            g2 = g3;
+            g3 = g;
         }
     }
     const uint32_t flags = unit_flags(mx, nan);
     warp_maxidx(mx, am);
-    const uint32_t gk[2] = {f2key(gm0), f2key(gm1)};
-    const float tau = key2f(warp_kth_key<2>(gk, 3u, C));
-    // gather x >= tau (finite) and, for top-p without top-k, the unit's softmax mass
-    int cnt = 0;
+    uint32_t gk[4] = {f2key(g0), f2key(g1), f2key(g2), f2key(g3)};
+    warp_sort128_u32_desc(gk);
+    const uint32_t tauk = __shfl_sync(0xffffffffu, C <= 32 ? gk[0] : gk[1], (C - 1) & 31);
+    const float tau = key2f(tauk);
+    // tokens >= tau (finite), each lane into its own kSeg words of buf (word i of
+    // lane l at buf[32 i + l]); and, for top-p without top-k, the unit's mass
+    int my = 0;
     float zs = 0.0f, zc = 0.0f;
     const bool need_z = ri.need_z;
     const float invT = ri.invT;
 #pragma unroll 1
-    for (int j0 = 0; j0 < u.nvec; j0 += 32) {
-        const int j = j0 + lane;
-        const bool in = j < u.nvec;
-        const uint4 raw = in ? slot[j] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    for (int j = lane; j < u.nvec; j += 32) {
+        const uint4 raw = slot[j];
         const int vb = u.v0 + j * EPV;
         uint32_t mask = 0;
 #pragma unroll
         for (int q = 0; q < EPV; ++q) {
-            const float x = in ? Vec<InT>::get(raw, q) : -INFINITY;
+            const float x = Vec<InT>::get(raw, q);
             mask |= (x >= tau && x > -INFINITY) ? (1u << q) : 0u;
             if (need_z && x > -INFINITY) {
                 const float y = __expf((x - mx) * invT) - zc;
@@ -444,20 +449,13 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
                 zs = s2;
             }
         }
-        if (__any_sync(0xffffffffu, mask != 0)) {
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                const bool take = (mask >> q) & 1u;
-                const unsigned bt = __ballot_sync(0xffffffffu, take);
-                if (take) {
-                    const int pos = cnt + __popc(bt & ((1u << lane) - 1u));
-                    if (pos < kBufCap) buf[pos] = comp_of(Vec<InT>::get(raw, q), vb + q);
-                }
-                cnt += __popc(bt);
-            }
+        while (mask) {
+            const int q = __ffs(mask) - 1;
+            mask &= mask - 1;
+            if (my < kSeg) buf[32 * my + lane] = comp_of(Vec<InT>::get(raw, q), vb + q);
+            ++my;
         }
     }
-    __syncwarp();
     if (need_z) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -469,13 +467,26 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
             zs = s2;
         }
     }
+    int pre = my;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, pre, off);
+        if (lane >= off) pre += o;
+    }
+    const int cnt = __shfl_sync(0xffffffffu, pre, 31);
+    pre -= my;
     uint32_t nc;
-    if (cnt > kBufCap) {
-        nc = kOverflow;
+    if (__any_sync(0xffffffffu, my > kSeg) || cnt > kUnitCands) {
+        nc = kOverflow;  // the row takes the exact path
     } else {
-        sort_buf(buf, cnt);
+        // the unit's logits are no longer needed: pack the words into the slot, sort
+        unsigned long long* dst = reinterpret_cast<unsigned long long*>(const_cast<uint4*>(slot));
+        __syncwarp();
+        for (int i = 0; i < my; ++i) dst[pre + i] = buf[32 * i + lane];
+        __syncwarp();
+        warp_sort_smem_desc(dst, cnt);
         nc = uint32_t(min(cnt, C));
-        for (int i = lane; i < int(nc); i += 32) rec->cand[i] = buf[i];
+        for (int i = lane; i < int(nc); i += 32) rec->cand[i] = dst[i];
     }
     if (lane == 0) {
         rec->mx = mx;
@@ -484,345 +495,14 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
         rec->nc = nc;
         rec->zs = zs;
         rec->zc = zc;
-    }
-}
-
-// ---------------------------------------------------------------- finishing a row
-__device__ __noinline__ int settle_slow(const GTop2 t, float T) { return settle_top2(t, T); }
-
-// Pick between the two best fp32 Gumbel candidates; double precision only when
-// they are within fp32 reach of each other.
-__device__ __forceinline__ int settle_fast(const GTop2& t, float T)
-{
-    if (t.a.idx == INT_MAX) return -1;
-    if (t.b.idx == INT_MAX) return t.a.idx;
-    const float tol = 1e-4f + 1e-5f * fmaxf(fabsf(t.a.s), fabsf(t.b.s));
-    if (t.a.s - t.b.s > tol) return t.a.idx;
-    return settle_slow(t, T);
-}
-
-// Fast fp32 Gumbel record of a kept candidate.
-__device__ __forceinline__ GRec cand_grec(const RowInfo& ri, float x, int v)
-{
-    const uint4 blk = philox4x32_10(make_uint4(uint32_t(v) >> 2, ri.stream, ri.off_lo, ri.off_hi),
-                                    PhiloxKey{ri.key_lo, ri.key_hi});
-    const uint32_t word = lane_of(blk, uint32_t(v) & 3u);
-    const float w = noise_one_minus_u(word);
-    return GRec{x * ri.invT - fast_ln_exp1(w, __log2f(w), word), v, x, word};
-}
-
-// Append to buf[n, ...) every listed word whose value key is >= vt, reading
-// each list from its head 8 words at a time and leaving it at its first word
-// below vt; returns the new count (only the first kBufCap words are stored).
-__device__ __forceinline__ int gather_lists(const ColRec* rr, int G, const uint32_t (&nc)[kLPL], uint32_t vt,
-                                            unsigned long long* buf, int n)
-{
-    const int lane = threadIdx.x & 31;
-    int len[kLPL];
-#pragma unroll
-    for (int q = 0; q < kLPL; ++q) len[q] = int(nc[q]);
-#pragma unroll 1
-    for (int i0 = 0; i0 < kCandCap; i0 += 8) {
-        bool more = false;
-#pragma unroll
-        for (int q = 0; q < kLPL; ++q) more |= i0 < len[q];
-        if (!__any_sync(0xffffffffu, more)) break;
-        unsigned long long w[kLPL][8];
-#pragma unroll
-        for (int q = 0; q < kLPL; ++q) {
-            const int s = lane + 32 * q;
-            if (i0 < len[q]) {
-                const uint4* src = reinterpret_cast<const uint4*>(&rr[s].cand[i0]);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint4 x = __ldcg(src + h);
-                    w[q][2 * h] = (static_cast<unsigned long long>(x.y) << 32) | x.x;
-                    w[q][2 * h + 1] = (static_cast<unsigned long long>(x.w) << 32) | x.z;
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 8; ++h) w[q][h] = 0ull;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < kLPL; ++q) {
-            if (!__any_sync(0xffffffffu, i0 < len[q])) continue;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const bool take = i0 + h < len[q] && cand_key(w[q][h]) >= vt;
-                const unsigned bt = __ballot_sync(0xffffffffu, take);
-                if (take) {
-                    const int pos = n + __popc(bt & ((1u << lane) - 1u));
-                    if (pos < kBufCap) buf[pos] = w[q][h];
-                }
-                n += __popc(bt);
-            }
-            if (!(cand_key(w[q][7]) >= vt)) len[q] = 0;  // sorted: the rest is below vt
-        }
+        rec->tau = tauk;
     }
     __syncwarp();
-    return n;
 }
 
-// The kept set of a truncated row from its units' lists; returns the token, or
-// sets `fallback` when the lists cannot settle it. hd: the headers of the
-// lane's lists (list lane + 32 q).
-__device__ __noinline__ int finish_cand(const ColParams& P, unsigned long long* buf, const RowInfo ri,
-                                        const ColRec* rr, const uint32_t (&nc)[kLPL], float m, bool& fallback)
-{
-    const int lane = threadIdx.x & 31;
-    const int G = P.gc;
-    const bool small_k = ri.small_k;
-    const int C = small_k ? ri.k : kCandCap;
-    int token = -1;
-    if (ri.do_topk && !small_k) {
-        fallback = true;
-        return -1;
-    }
-    // one round trip: the C-th word of every list, and a sample of h words from
-    // the head of every list (G h >= C of them when the lists hold that many)
-    const int h = min(C, (C + G - 1) / G);
-    const int ns = G * h;  // <= G + C - 1 <= 191
-    constexpr int kSPL = 6;
-    unsigned long long tail[kLPL];
-    uint32_t sk[kSPL];
-    uint32_t sok = 0;
-#pragma unroll
-    for (int q = 0; q < kLPL; ++q) {
-        const int s = lane + 32 * q;
-        tail[q] = (s < G && nc[q] == uint32_t(C)) ? __ldcg(&rr[s].cand[C - 1]) : 0ull;
-    }
-#pragma unroll
-    for (int t = 0; t < kSPL; ++t) {
-        const int j = lane + 32 * t;
-        sk[t] = 0u;
-        if (j < ns) {
-            const int s = j / h, i = j - s * h;
-            const uint32_t n_s = __ldcg(&rr[s].nc);
-            const unsigned long long w = __ldcg(&rr[s].cand[i]);
-            if (uint32_t(i) < n_s) {
-                sk[t] = cand_key(w);
-                sok |= 1u << t;
-            }
-        }
-    }
-    bool overflow = false;
-    unsigned long long tau_inc = 0ull;  // tokens missing from every list lie below it
-#pragma unroll
-    for (int q = 0; q < kLPL; ++q) {
-        overflow |= nc[q] == kOverflow;
-        tau_inc = tail[q] > tau_inc ? tail[q] : tau_inc;
-    }
-    if (__any_sync(0xffffffffu, overflow)) {
-        fallback = true;
-        return -1;
-    }
-    tau_inc = warp_max_u64(tau_inc);
-    const int nvalid = __reduce_add_sync(0xffffffffu, __popc(sok));
-    // every word whose value reaches the C-th sampled value: the row's top C and ties
-    const uint32_t vt = nvalid >= C ? warp_kth_key<kSPL>(sk, sok, C) : 0u;
-    const int n0 = gather_lists(rr, G, nc, vt, buf, 0);
-    if (n0 > kBufCap || n0 == 0) {
-        fallback = true;
-        return -1;
-    }
-    sort_buf(buf, n0);
-    const int lim = min(n0, kKeepCap);
-    const int nk = small_k ? min(ri.k, n0) : lim;
-    const int iA = lane, iB = lane + 32;
-    const unsigned long long cA = iA < lim ? buf[iA] : 0ull;
-    const unsigned long long cB = iB < lim ? buf[iB] : 0ull;
-    const float xA = key2f(cand_key(cA)), xB = key2f(cand_key(cB));
-    const int idxA = cand_idx(cA), idxB = cand_idx(cB);
-    auto complete = [&](int i) { return i < 0 || buf[i] >= tau_inc; };
-    int np = nk;
-    if (ri.do_topp) {
-        // prefix masses in fp32; redone in double when a prefix lies near the cut
-        const float eA = iA < nk ? __expf((xA - m) * ri.invT) : 0.0f;
-        const float eB = iB < nk ? __expf((xB - m) * ri.invT) : 0.0f;
-        float sA = eA, sB = eB;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float oA = __shfl_up_sync(0xffffffffu, sA, off);
-            const float oB = __shfl_up_sync(0xffffffffu, sB, off);
-            if (lane >= off) {
-                sA += oA;
-                sB += oB;
-            }
-        }
-        sB += __shfl_sync(0xffffffffu, sA, 31);
-        float Z;
-        if (small_k) {
-            Z = __shfl_sync(0xffffffffu, sB, 31);
-        } else {
-            float z = 0.0f;
-            for (int s = lane; s < G; s += 32) {
-                const float mxs = __ldcg(&rr[s].mx);
-                if (!(mxs > -INFINITY)) continue;
-                const float zs = __ldcg(&rr[s].zs) - __ldcg(&rr[s].zc);
-                z += zs * __expf((mxs - m) * ri.invT);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-            Z = z;
-        }
-        const float pz = ri.p * Z;
-        const float exA = sA - eA, exB = sB - eB;
-        const float tol = 1e-4f * Z;
-        const bool nearcut = __any_sync(0xffffffffu, (iA < nk && fabsf(exA - pz) < tol) ||
-                                                         (iB < nk && fabsf(exB - pz) < tol));
-        if (!nearcut) {
-            const bool kA = iA < nk && (exA < pz || iA == 0);
-            const bool kB = iB < nk && (exB < pz);
-            np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
-        } else {
-            // close to the cut: the same walk in double
-            const double Te = double(ri.Te);
-            const double y0 = double(m) / Te;
-            const double dA = iA < nk ? exp(double(xA) / Te - y0) : 0.0;
-            const double dB = iB < nk ? exp(double(xB) / Te - y0) : 0.0;
-            double qA = dA, qB = dB;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const double oA = __shfl_up_sync(0xffffffffu, qA, off);
-                const double oB = __shfl_up_sync(0xffffffffu, qB, off);
-                if (lane >= off) {
-                    qA += oA;
-                    qB += oB;
-                }
-            }
-            qB += __shfl_sync(0xffffffffu, qA, 31);
-            double ZD;
-            if (small_k) {
-                ZD = __shfl_sync(0xffffffffu, qB, 31);
-            } else {
-                double z = 0.0;
-                for (int s = lane; s < G; s += 32) {
-                    const float mxs = __ldcg(&rr[s].mx);
-                    if (!(mxs > -INFINITY)) continue;
-                    const double zs = double(__ldcg(&rr[s].zs)) - double(__ldcg(&rr[s].zc));
-                    z += zs * exp((double(mxs) - double(m)) / Te);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-                ZD = z;
-            }
-            const double pzd = double(ri.p) * ZD;
-            const bool kA = iA < nk && ((qA - dA) < pzd || iA == 0);
-            const bool kB = iB < nk && ((qB - dB) < pzd);
-            np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
-        }
-        if (!small_k && np >= lim) fallback = true;
-    } else if (!small_k) {
-        np = lim;
-    }
-    int nkept = np;
-    if (ri.do_minp) {
-        const double th = double(m) + double(ri.Te) * log(double(ri.minp));
-        float xthr = float(th);
-        if (double(xthr) < th) xthr = nextafterf(xthr, INFINITY);
-        const bool mA = iA < np && xA >= xthr;
-        const bool mB = iB < np && xB >= xthr;
-        nkept = __popc(__ballot_sync(0xffffffffu, mA)) + __popc(__ballot_sync(0xffffffffu, mB));
-        nkept = max(nkept, 1);
-        if (!small_k && !ri.do_topp && nkept >= lim) fallback = true;
-    } else if (!small_k && !ri.do_topp) {
-        fallback = true;
-    }
-    if (!fallback) {
-        // every kept token must be known exactly, and so must the first dropped
-        // one when min-p or top-p (not top-k) closed the set
-        if (!complete(nkept - 1)) fallback = true;
-        if (small_k && !complete(nk - 1)) fallback = true;
-        if (nkept < (small_k ? nk : lim) && !complete(nkept)) fallback = true;
-    }
-    if (!fallback) {
-        GTop2 t;
-        t.a = grec_empty();
-        t.b = grec_empty();
-        if (iA < nkept) top2_insert(t, cand_grec(ri, xA, idxA));
-        if (iB < nkept) top2_insert(t, cand_grec(ri, xB, idxB));
-        top2_warp_reduce(t);
-        token = settle_fast(t, ri.T);
-    }
-    __syncwarp();
-    return token;
-}
-
-// Finish row r from its records (one warp). Returns 1 when the row needs the
-// CTA-wide exact path (m and amax are returned for it), 0 otherwise. Loads of
-// the G <= kMaxUnits records are issued together (kLPL per lane).
-__device__ __noinline__ int finish_row(const ColParams& P, unsigned long long* buf, const int r,
-                                       const RowInfo ri, float* m_out, int* amax_out)
-{
-    const int lane = threadIdx.x & 31;
-    const KernelParams& kp = P.k;
-    const int G = P.gc;
-    const ColRec* rr = P.rec + int64_t(r) * G;
-    __threadfence();
-
-    uint4 hd[kLPL];
-    GTop2 t;
-    t.a = grec_empty();
-    t.b = grec_empty();
-    const bool plain = ri.cls == kClsPlain;
-#pragma unroll
-    for (int q = 0; q < kLPL; ++q) {
-        const int s = lane + 32 * q;
-        hd[q] = s < G ? __ldcg(reinterpret_cast<const uint4*>(&rr[s]))  // mx, amax, flags, nc
-                      : make_uint4(0xFF800000u, uint32_t(INT_MAX), 0u, 0u);
-        if (plain && s < G) {
-            const uint4 ua = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g0));
-            const uint4 ub = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g1));
-            top2_insert(t, GRec{__uint_as_float(ua.x), int(ua.y), __uint_as_float(ua.z), ua.w});
-            top2_insert(t, GRec{__uint_as_float(ub.x), int(ub.y), __uint_as_float(ub.z), ub.w});
-        }
-    }
-    float m = -INFINITY;
-    int am = INT_MAX;
-    uint32_t fl = 0;
-    uint32_t nc[kLPL];
-#pragma unroll
-    for (int q = 0; q < kLPL; ++q) {
-        fl |= hd[q].z;
-        maxidx_merge(m, am, __uint_as_float(hd[q].x), int(hd[q].y));
-        nc[q] = hd[q].w;
-    }
-    warp_maxidx(m, am);
-    fl = __reduce_or_sync(0xffffffffu, fl);
-    int status = ri.status;
-    if (status == kRowOk) {
-        if (fl & kFlagNonFinite) status = kRowNonFinite;
-        else if (!(fl & kFlagAnyFinite)) status = kRowAllNegInf;
-    }
-    *m_out = m;
-    *amax_out = am;
-    int token = -1;
-    bool fallback = false;
-    if (status != kRowOk) {
-        token = -1;
-    } else if (ri.cls == kClsGreedy) {
-        token = am;
-    } else if (plain) {
-        top2_warp_reduce(t);
-        token = settle_fast(t, ri.T);
-    } else {
-        token = finish_cand(P, buf, ri, rr, nc, m, fallback);
-    }
-    if (lane == 0) {
-        if (!fallback) {
-            kp.out_tokens[r] = token;
-            if (kp.out_status) kp.out_status[r] = status;
-        }
-        P.counters[r] = 0u;
-    }
-    return fallback ? 1 : 0;
-}
-
-// ---------------------------------------------------------------- one unit
+// ---------------------------------------------------------------- one unit (phase 1)
 template <typename InT>
-__device__ __forceinline__ void unit_step(const ColParams& P, ColShared& sh, int uid, uint4* slot,
-                                          unsigned long long* buf)
+__device__ __forceinline__ void unit_step(const ColParams& P, int uid, uint4* slot, unsigned long long* buf)
 {
     const KernelParams& kp = P.k;
     const int lane = threadIdx.x & 31;
@@ -852,26 +532,392 @@ __device__ __forceinline__ void unit_step(const ColParams& P, ColShared& sh, int
             rec->nc = 0;
         }
     }
-    // the record is complete once every lane has written its part; lane 0's
-    // release publishes all of it
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0) old = atom_add_release_gpu(&P.counters[u.r], 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == uint32_t(P.gc - 1)) {
-        float mrow;
-        int arow;
-        const int fb = finish_row(P, buf, u.r, ri, &mrow, &arow);
-        if (fb && lane == 0) {
-            const int q = atomicAdd(&sh.n_fallback, 1);
-            sh.fallback_rows[q] = u.r;
-            sh.fb_m[q] = mrow;
-            sh.fb_amax[q] = arow;
-        }
-    }
     __syncwarp();
 }
 
+// ---------------------------------------------------------------- grid barrier
+constexpr uint32_t kBarPolls = 1u << 24;  // about a second of polling
+
+// Every CTA of the (cooperative) grid waits here until all have arrived; the
+// writes before it are visible to every CTA after it. Returns false if this
+// CTA gave up waiting (the barrier is then marked broken for later launches).
+__device__ __noinline__ bool grid_sync(ColShared& sh, GridBar* bar)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const uint32_t gen = ld_acquire_gpu(&bar->gen);
+        if (ld_acquire_gpu(&bar->poison) != 0u) {
+            ok = 0;
+        } else {
+            const uint32_t arrived = atom_add_acq_rel_gpu(&bar->count, 1u);
+            if (arrived == gridDim.x - 1) {
+                bar->count = 0u;
+                st_release_gpu(&bar->gen, gen + 1u);
+            } else {
+                uint32_t polls = 0;
+                while (ld_acquire_gpu(&bar->gen) == gen) {
+                    if (++polls > kBarPolls) {
+                        ok = 0;
+                        atomicExch(&bar->poison, 1u);
+                        break;
+                    }
+                    if (polls > 256) __nanosleep(64);
+                }
+            }
+        }
+        sh.bar_ok = ok;
+    }
+    __syncthreads();
+    return sh.bar_ok != 0;
+}
+
+// ---------------------------------------------------------------- phase 2
+__device__ __noinline__ int settle_slow(const GTop2 t, float T) { return settle_top2(t, T); }
+
+// Pick between the two best fp32 Gumbel candidates; double precision only when
+// they are within fp32 reach of each other.
+__device__ __forceinline__ int settle_fast(const GTop2& t, float T)
+{
+    if (t.a.idx == INT_MAX) return -1;
+    if (t.b.idx == INT_MAX) return t.a.idx;
+    const float tol = 1e-4f + 1e-5f * fmaxf(fabsf(t.a.s), fabsf(t.b.s));
+    if (t.a.s - t.b.s > tol) return t.a.idx;
+    return settle_slow(t, T);
+}
+
+// Fast fp32 Gumbel record of a kept candidate.
+__device__ __forceinline__ GRec cand_grec(const RowInfo& ri, float x, int v)
+{
+    const uint4 blk = philox4x32_10(make_uint4(uint32_t(v) >> 2, ri.stream, ri.off_lo, ri.off_hi),
+                                    PhiloxKey{ri.key_lo, ri.key_hi});
+    const uint32_t word = lane_of(blk, uint32_t(v) & 3u);
+    const float w = noise_one_minus_u(word);
+    return GRec{x * ri.invT - fast_ln_exp1(w, __log2f(w), word), v, x, word};
+}
+
+// Finish a greedy, plain or rejected row r from its records (one warp). Loads
+// of the G <= kMaxUnits records are issued together (kLPL per lane).
+__device__ __noinline__ void finish_row(const ColParams& P, const int r, const RowInfo ri)
+{
+    const int lane = threadIdx.x & 31;
+    const KernelParams& kp = P.k;
+    const int G = P.gc;
+    const ColRec* rr = P.rec + int64_t(r) * G;
+    uint4 hd[kLPL];
+    GTop2 t;
+    t.a = grec_empty();
+    t.b = grec_empty();
+    const bool plain = ri.cls == kClsPlain;
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) {
+        const int s = lane + 32 * q;
+        hd[q] = s < G ? __ldcg(reinterpret_cast<const uint4*>(&rr[s]))  // mx, amax, flags, nc
+                      : make_uint4(0xFF800000u, uint32_t(INT_MAX), 0u, 0u);
+        if (plain && s < G) {
+            const uint4 ua = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g0));
+            const uint4 ub = __ldcg(reinterpret_cast<const uint4*>(&rr[s].g1));
+            top2_insert(t, GRec{__uint_as_float(ua.x), int(ua.y), __uint_as_float(ua.z), ua.w});
+            top2_insert(t, GRec{__uint_as_float(ub.x), int(ub.y), __uint_as_float(ub.z), ub.w});
+        }
+    }
+    float m = -INFINITY;
+    int am = INT_MAX;
+    uint32_t fl = 0;
+#pragma unroll
+    for (int q = 0; q < kLPL; ++q) {
+        fl |= hd[q].z;
+        maxidx_merge(m, am, __uint_as_float(hd[q].x), int(hd[q].y));
+    }
+    warp_maxidx(m, am);
+    fl = __reduce_or_sync(0xffffffffu, fl);
+    int status = ri.status;
+    if (status == kRowOk) {
+        if (fl & kFlagNonFinite) status = kRowNonFinite;
+        else if (!(fl & kFlagAnyFinite)) status = kRowAllNegInf;
+    }
+    int token = -1;
+    if (status != kRowOk) {
+        token = -1;
+    } else if (ri.cls == kClsGreedy) {
+        token = am;
+    } else {
+        top2_warp_reduce(t);
+        token = settle_fast(t, ri.T);
+    }
+    if (lane == 0) {
+        kp.out_tokens[r] = token;
+        if (kp.out_status) kp.out_status[r] = status;
+    }
+}
+
+// Number of the first nk sorted tokens (x, two per lane: index lane and
+// lane + 32) kept by top-p, walked in double: for cuts that fp32 cannot call.
+__device__ __noinline__ int topp_keep_f64(const RowInfo ri, float xA, float xB, int nk, float m, bool small_k,
+                                          const float* hmx, const float* hzs, const float* hzc, int G)
+{
+    const int lane = threadIdx.x & 31;
+    const int iA = lane, iB = lane + 32;
+    const double Te = double(ri.Te);
+    const double y0 = double(m) / Te;
+    const double dA = iA < nk ? exp(double(xA) / Te - y0) : 0.0;
+    const double dB = iB < nk ? exp(double(xB) / Te - y0) : 0.0;
+    double qA = dA, qB = dB;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double oA = __shfl_up_sync(0xffffffffu, qA, off);
+        const double oB = __shfl_up_sync(0xffffffffu, qB, off);
+        if (lane >= off) {
+            qA += oA;
+            qB += oB;
+        }
+    }
+    qB += __shfl_sync(0xffffffffu, qA, 31);
+    double ZD;
+    if (small_k) {
+        ZD = __shfl_sync(0xffffffffu, qB, 31);
+    } else {
+        double z = 0.0;
+        for (int s = lane; s < G; s += 32) {
+            if (!(hmx[s] > -INFINITY)) continue;
+            z += (double(hzs[s]) - double(hzc[s])) * exp((double(hmx[s]) - double(m)) / Te);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        ZD = z;
+    }
+    const double pzd = double(ri.p) * ZD;
+    const bool kA = iA < nk && ((qA - dA) < pzd || iA == 0);
+    const bool kB = iB < nk && ((qB - dB) < pzd);
+    return __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
+}
+
+// Smallest fp32 x with x >= m + T ln(min_p) in exact arithmetic.
+__device__ __noinline__ float minp_threshold(float m, float Te, float minp)
+{
+    const double th = double(m) + double(Te) * log(double(minp));
+    float xthr = float(th);
+    if (double(xthr) < th) xthr = nextafterf(xthr, INFINITY);
+    return xthr;
+}
+
+// The kept set of a truncated row from L[0, n): the largest tokens of the
+// units' lists by (value desc, index asc), sorted; every token missing from the
+// lists lies below tau_inc, so L[i] is the row's i-th token when L[i] >= tau_inc.
+// Warp 0 only. Returns the token, or sets `fallback` when the list cannot
+// settle it.
+__device__ __noinline__ int cut_and_pick(const RowInfo ri, const unsigned long long* L, int n,
+                                         unsigned long long tau_inc, float m, const float* hmx,
+                                         const float* hzs, const float* hzc, int G, bool& fallback)
+{
+    const int lane = threadIdx.x & 31;
+    const bool small_k = ri.small_k;
+    const int lim = min(n, kKeepCap);
+    const int nk = small_k ? min(ri.k, n) : lim;
+    const int iA = lane, iB = lane + 32;
+    const unsigned long long cA = iA < lim ? L[iA] : 0ull;
+    const unsigned long long cB = iB < lim ? L[iB] : 0ull;
+    const float xA = key2f(cand_key(cA)), xB = key2f(cand_key(cB));
+    const int idxA = cand_idx(cA), idxB = cand_idx(cB);
+    auto complete = [&](int i) { return i < 0 || L[i] >= tau_inc; };
+    int np = nk;
+    if (ri.do_topp) {
+        // prefix masses in fp32; redone in double when a prefix lies near the cut
+        const float eA = iA < nk ? __expf((xA - m) * ri.invT) : 0.0f;
+        const float eB = iB < nk ? __expf((xB - m) * ri.invT) : 0.0f;
+        float sA = eA, sB = eB;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float oA = __shfl_up_sync(0xffffffffu, sA, off);
+            const float oB = __shfl_up_sync(0xffffffffu, sB, off);
+            if (lane >= off) {
+                sA += oA;
+                sB += oB;
+            }
+        }
+        sB += __shfl_sync(0xffffffffu, sA, 31);
+        float Z;
+        if (small_k) {
+            Z = __shfl_sync(0xffffffffu, sB, 31);
+        } else {
+            float z = 0.0f;
+            for (int s = lane; s < G; s += 32)
+                if (hmx[s] > -INFINITY) z += (hzs[s] - hzc[s]) * __expf((hmx[s] - m) * ri.invT);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+            Z = z;
+        }
+        const float pz = ri.p * Z;
+        const float exA = sA - eA, exB = sB - eB;
+        const float tol = 1e-4f * Z;
+        const bool nearcut = __any_sync(0xffffffffu, (iA < nk && fabsf(exA - pz) < tol) ||
+                                                         (iB < nk && fabsf(exB - pz) < tol));
+        if (!nearcut) {
+            const bool kA = iA < nk && (exA < pz || iA == 0);
+            const bool kB = iB < nk && (exB < pz);
+            np = __popc(__ballot_sync(0xffffffffu, kA)) + __popc(__ballot_sync(0xffffffffu, kB));
+        } else {
+            np = topp_keep_f64(ri, xA, xB, nk, m, small_k, hmx, hzs, hzc, G);
+        }
+        if (!small_k && np >= lim) fallback = true;  // the set may run past the list
+    } else if (!small_k) {
+        np = lim;
+    }
+    int nkept = np;
+    if (ri.do_minp) {
+        const float xthr = minp_threshold(m, ri.Te, ri.minp);
+        const bool mA = iA < np && xA >= xthr;
+        const bool mB = iB < np && xB >= xthr;
+        nkept = __popc(__ballot_sync(0xffffffffu, mA)) + __popc(__ballot_sync(0xffffffffu, mB));
+        nkept = max(nkept, 1);
+        if (!small_k && !ri.do_topp && nkept >= lim) fallback = true;
+    } else if (!small_k && !ri.do_topp) {
+        fallback = true;
+    }
+    if (!fallback) {
+        // every kept token must be known exactly, and so must the first dropped
+        // one when min-p or top-p (not top-k) closed the set
+        if (!complete(nkept - 1)) fallback = true;
+        if (small_k && !complete(nk - 1)) fallback = true;
+        if (nkept < (small_k ? nk : lim) && !complete(nkept)) fallback = true;
+    }
+    int token = -1;
+    if (!fallback) {
+        GTop2 t;
+        t.a = grec_empty();
+        t.b = grec_empty();
+        if (iA < nkept) top2_insert(t, cand_grec(ri, xA, idxA));
+        if (iB < nkept) top2_insert(t, cand_grec(ri, xB, idxB));
+        top2_warp_reduce(t);
+        token = settle_fast(t, ri.T);
+    }
+    return token;
+}
+
+// Finish truncated row r with the whole CTA. One round of copies brings every
+// unit's sorted top list and header into shared memory. t1 = the C-th largest of
+// the lists' first h words (G h >= C) bounds the row's top C from below, so the
+// listed words >= t1 hold them; those are gathered, ranked, and warp 0 cuts and
+// picks. `dyn` is the CTA's free dynamic shared memory.
+__device__ __noinline__ void cta_cand_row(ColShared& sh, const ColParams& P, int r, const RowInfo ri,
+                                          unsigned char* dyn)
+{
+    const KernelParams& kp = P.k;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int G = P.gc;
+    const int C = ri.small_k ? ri.k : kCandCap;
+    unsigned long long* Lst = reinterpret_cast<unsigned long long*>(dyn);  // [G][kCandCap]
+    unsigned long long* S = Lst + size_t(kMaxUnits) * kCandCap;            // gathered
+    unsigned long long* Out = S + kSelCap;                                  // ranked
+    uint32_t* rank = reinterpret_cast<uint32_t*>(Out + kSelCap);
+    float* hmx = reinterpret_cast<float*>(rank + kSelCap);
+    float* hzs = hmx + kMaxUnits;
+    float* hzc = hzs + kMaxUnits;
+    uint32_t* hnc = reinterpret_cast<uint32_t*>(hzc + kMaxUnits);
+    int32_t* ham = reinterpret_cast<int32_t*>(hnc + kMaxUnits);
+    uint32_t* hfl = reinterpret_cast<uint32_t*>(ham + kMaxUnits);
+    const ColRec* rr = P.rec + int64_t(r) * G;
+    const int pieces = (C + 1) / 2;  // 16-byte pieces of a list
+    for (int c = tid; c < G * pieces; c += kT) {
+        const int s = c / pieces, h = c - s * pieces;
+        cp_async16(Lst + s * kCandCap + 2 * h, &rr[s].cand[2 * h]);
+    }
+    cp_async_commit();
+    if (tid < G) {
+        const uint4 hd = __ldcg(reinterpret_cast<const uint4*>(&rr[tid]));  // mx, amax, flags, nc
+        hmx[tid] = __uint_as_float(hd.x);
+        ham[tid] = int(hd.y);
+        hfl[tid] = hd.z;
+        hnc[tid] = hd.w;
+        const uint4 hz = __ldcg(reinterpret_cast<const uint4*>(&rr[tid].zs));  // zs, zc, tau, pad
+        hzs[tid] = __uint_as_float(hz.x);
+        hzc[tid] = __uint_as_float(hz.y);
+    }
+    if (tid == 0) sh.n_sel = 0;
+    cp_async_wait<0>();
+    __syncthreads();
+    if (wid == 0) {
+        float m = -INFINITY;
+        int am = INT_MAX;
+        uint32_t fl = 0, over = 0;
+        unsigned long long ti = 0ull;  // tokens missing from every list lie below it
+        for (int s = lane; s < G; s += 32) {
+            maxidx_merge(m, am, hmx[s], ham[s]);
+            fl |= hfl[s];
+            over |= hnc[s] == kOverflow ? 1u : 0u;
+            if (hnc[s] == uint32_t(C)) ti = max(ti, Lst[s * kCandCap + C - 1]);
+        }
+        warp_maxidx(m, am);
+        fl = __reduce_or_sync(0xffffffffu, fl);
+        over = __reduce_or_sync(0xffffffffu, over);
+        ti = warp_max_u64(ti);
+        if (lane == 0) {
+            sh.fin_m = m;
+            sh.fin_amax = am;
+            sh.fin_flags = fl;
+            sh.fin_over = over;
+            sh.fin_tinc = ti;
+        }
+    }
+    __syncthreads();
+    const float m = sh.fin_m;
+    const int am = sh.fin_amax;
+    int status = ri.status;
+    if (status == kRowOk) {
+        if (sh.fin_flags & kFlagNonFinite) status = kRowNonFinite;
+        else if (!(sh.fin_flags & kFlagAnyFinite)) status = kRowAllNegInf;
+    }
+    bool fallback = status == kRowOk && (sh.fin_over != 0 || (ri.do_topk && !ri.small_k));
+    int n = 0;
+    if (status == kRowOk && !fallback) {
+        // samples: the first h words of every list
+        const int h = min(C, (C + G - 1) / G);
+        for (int e = tid; e < G * h; e += kT) {
+            const int s = e / h, i = e - s * h;
+            if (uint32_t(i) < hnc[s]) S[atomicAdd(&sh.n_sel, 1)] = Lst[s * kCandCap + i];
+        }
+        __syncthreads();
+        const int ns = sh.n_sel;  // <= G h < G + C <= kSelCap
+        unsigned long long t1 = 0ull;
+        if (ns >= C) {
+            cta_rank_sort_desc(S, ns, rank, Out);
+            t1 = Out[C - 1];
+        }
+        __syncthreads();
+        if (tid == 0) sh.n_sel = 0;
+        __syncthreads();
+        for (int e = tid; e < G * kCandCap; e += kT) {
+            const int s = e / kCandCap, i = e - s * kCandCap;
+            if (uint32_t(i) < hnc[s] && Lst[e] >= t1) {
+                const int pos = atomicAdd(&sh.n_sel, 1);
+                if (pos < kSelCap) S[pos] = Lst[e];
+            }
+        }
+        __syncthreads();
+        n = sh.n_sel;
+        if (n > kSelCap || n == 0) fallback = true;
+        else cta_rank_sort_desc(S, n, rank, Out);
+    }
+    if (wid == 0) {
+        int token = -1;
+        if (status == kRowOk && !fallback)
+            token = cut_and_pick(ri, Out, n, sh.fin_tinc, m, hmx, hzs, hzc, G, fallback);
+        if (lane == 0) {
+            if (fallback) {
+                const int q = atomicAdd(&sh.n_fallback, 1);
+                sh.fallback_rows[q] = r;
+                sh.fb_m[q] = m;
+                sh.fb_amax[q] = am;
+            } else {
+                kp.out_tokens[r] = token;
+                if (kp.out_status) kp.out_status[r] = status;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- the kernel
 template <typename InT>
 __global__ void __launch_bounds__(kT, 1) colsplit_kernel(const ColParams P)
 {
@@ -882,10 +928,33 @@ __global__ void __launch_bounds__(kT, 1) colsplit_kernel(const ColParams P)
     uint4* slot = reinterpret_cast<uint4*>(wbase);
     unsigned long long* buf = reinterpret_cast<unsigned long long*>(wbase + kSlotBytes);
     if (tid == 0) sh.n_fallback = 0;
-    __syncthreads();
+
+    // ---- phase 1: units, dealt so that consecutive CTAs take consecutive units
 #pragma unroll 1
     for (int u = blockIdx.x + gridDim.x * wid; u < P.n_units; u += gridDim.x * kW)
-        unit_step<InT>(P, sh, u, slot, buf);
+        unit_step<InT>(P, u, slot, buf);
+
+    const bool ok = grid_sync(sh, P.bar);
+
+    // ---- phase 2: rows, dealt round-robin to the CTAs
+    const KernelParams& kp = P.k;
+#pragma unroll 1
+    for (int r = blockIdx.x; r < P.n_rows; r += gridDim.x) {
+        int lrow = r;
+        if (kp.logit_row) lrow = kp.logit_row[r];
+        const bool lrow_ok = lrow >= 0 && int64_t(lrow) < kp.n_logit_rows;
+        const RowInfo ri = load_row_info(P, r, lrow_ok ? lrow : -1);
+        if (!ok) {
+            if (tid == 0) {
+                kp.out_tokens[r] = -1;
+                if (kp.out_status) kp.out_status[r] = kRowTimeout;
+            }
+        } else if (ri.cls == kClsCand) {
+            cta_cand_row(sh, P, r, ri, smem_raw + kSharedHead);
+        } else if (wid == 0) {
+            finish_row(P, r, ri);
+        }
+    }
     __syncthreads();
 
     // ---- rows the lists could not settle: exact path, whole CTA

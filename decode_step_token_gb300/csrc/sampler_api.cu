@@ -63,9 +63,9 @@ struct sampler_s {
     uint32_t flags;
     size_t smem_set[4];  // dynamic shared memory already granted per kernel variant
     size_t col_smem_set[2];
-    // workspace of the unit-split path: per-(row, unit) records and row counters
+    // workspace of the unit-split path: per-(row, unit) records and the grid barrier
     dst::col::ColRec* col_rec;
-    uint32_t* col_counters;
+    dst::col::GridBar* col_bar;
     unsigned long long* stats;  // device counters (diagnostics)
     int col_rows;
     int64_t col_units;  // records in col_rec
@@ -165,7 +165,8 @@ ColGeometry col_geometry(int64_t N, int64_t V, int esize, int sms)
     g.w = int(w);
     g.gc = int((V + w - 1) / w);
     g.units = N * g.gc;
-    g.grid = int(std::min<int64_t>(sms, std::max<int64_t>(g.units, 1)));
+    // enough CTAs for one unit per warp, at most one per SM (all co-resident)
+    g.grid = int(std::min<int64_t>(sms, std::max<int64_t>((g.units + dst::col::kW - 1) / dst::col::kW, 1)));
     return g;
 }
 
@@ -221,6 +222,25 @@ void fill_col_params(dst::col::ColParams& p, const sampler_args_t* a, const ColG
     p.n_units = int(g.units);
 }
 
+// A cooperative launch: the CTAs meet at a grid barrier, so all must be resident.
+int launch_col_kernel(void* fn, dst::col::ColParams& p, const ColGeometry& g, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(g.grid);
+    cfg.blockDim = dim3(dst::col::kT);
+    cfg.dynamicSmemBytes = dst::col::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&p};
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
 int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream)
 {
     const bool bf = a->dtype == SAMPLER_DTYPE_BF16;
@@ -235,12 +255,9 @@ int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaS
     dst::col::ColParams p;
     fill_col_params(p, a, g);
     p.rec = h->col_rec;
-    p.counters = h->col_counters;
+    p.bar = h->col_bar;
     p.stats = h->stats;
-    void* args[] = {&p};
-    if (cudaLaunchKernel(fn, dim3(g.grid), dim3(dst::col::kT), args, dst::col::kSmemBytes, stream) != cudaSuccess)
-        return SAMPLER_ERR_CUDA;
-    return SAMPLER_OK;
+    return launch_col_kernel(fn, p, g, stream);
 }
 
 int check_args(sampler_t h, const sampler_args_t* a)
@@ -260,16 +277,16 @@ int check_args(sampler_t h, const sampler_args_t* a)
 }  // namespace
 
 // ---------------------------------------------------------------- allocation-free entry
-// The column-split kernel's workspace (row counters, then the per-(row, slice)
+// The unit-split kernel's workspace (the grid barrier, then the per-(row, unit)
 // records) lives in this module's own device memory for sampler_sample_noalloc.
 namespace {
 
 constexpr int kNoAllocRows = SAMPLER_NOALLOC_MAX_ROWS;
-constexpr size_t kNoAllocCounterBytes = 256;  // kNoAllocRows 32-bit counters, padded
+constexpr size_t kNoAllocCounterBytes = 256;  // the grid barrier, padded
 constexpr size_t kNoAllocScratchBytes = size_t(9) << 19;  // 4.5 MiB: 64 rows of up to 262144
 constexpr int64_t kNoAllocUnits =
     int64_t((kNoAllocScratchBytes - kNoAllocCounterBytes) / sizeof(dst::col::ColRec));
-static_assert(kNoAllocRows * sizeof(uint32_t) <= kNoAllocCounterBytes, "counter area");
+static_assert(sizeof(dst::col::GridBar) <= kNoAllocCounterBytes, "barrier area");
 static_assert(kNoAllocCounterBytes % alignof(dst::col::ColRec) == 0, "record alignment");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -287,8 +304,8 @@ std::mutex g_noalloc_mutex;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
 // Once per device (the device current): find the scratch array's address, read
-// the SM count and clear the row counters, which must start at zero (the kernel
-// leaves them at zero after every row it finishes).
+// the SM count and clear the grid barrier, which must start at zero (every
+// barrier leaves its count at zero).
 int noalloc_setup(int dev, cudaStream_t stream, NoAllocDevice* out)
 {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -398,13 +415,13 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
     {
         const size_t rec_bytes = size_t(h->col_units) * sizeof(dst::col::ColRec);
         if (cudaMalloc(&h->col_rec, rec_bytes) != cudaSuccess ||
-            cudaMalloc(&h->col_counters, size_t(h->col_rows) * sizeof(uint32_t)) != cudaSuccess ||
-            cudaMemset(h->col_counters, 0, size_t(h->col_rows) * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMalloc(&h->col_bar, sizeof(dst::col::GridBar)) != cudaSuccess ||
+            cudaMemset(h->col_bar, 0, sizeof(dst::col::GridBar)) != cudaSuccess ||
             cudaMalloc(&h->stats, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
             cudaMemset(h->stats, 0, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
             cudaDeviceSynchronize() != cudaSuccess) {
             cudaFree(h->col_rec);
-            cudaFree(h->col_counters);
+            cudaFree(h->col_bar);
             cudaFree(h->stats);
             delete h;
             return SAMPLER_ERR_CUDA;
@@ -419,7 +436,7 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
         bytes += align16((R + 1) * 4) + align16(size_t(cfg->max_history) * 4 + 4);
         if (cudaMalloc(&h->stage_base, bytes) != cudaSuccess) {
             cudaFree(h->col_rec);
-            cudaFree(h->col_counters);
+            cudaFree(h->col_bar);
             cudaFree(h->stats);
             delete h;
             return SAMPLER_ERR_CUDA;
@@ -438,7 +455,7 @@ void sampler_destroy(sampler_t h)
     cudaSetDevice(h->device);
     if (h->stage_base) cudaFree(h->stage_base);
     if (h->col_rec) cudaFree(h->col_rec);
-    if (h->col_counters) cudaFree(h->col_counters);
+    if (h->col_bar) cudaFree(h->col_bar);
     if (h->stats) cudaFree(h->stats);
     if (cur >= 0) cudaSetDevice(cur);
     delete h;
@@ -478,13 +495,10 @@ int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
     if (rc != SAMPLER_OK) return rc;
     dst::col::ColParams p;
     fill_col_params(p, a, g);
-    p.counters = reinterpret_cast<uint32_t*>(d.scratch);
+    p.bar = reinterpret_cast<dst::col::GridBar*>(d.scratch);
     p.rec = reinterpret_cast<dst::col::ColRec*>(d.scratch + kNoAllocCounterBytes);
     p.stats = nullptr;
-    void* args[] = {&p};
-    if (cudaLaunchKernel(fn, dim3(g.grid), dim3(dst::col::kT), args, dst::col::kSmemBytes, stream) != cudaSuccess)
-        return SAMPLER_ERR_CUDA;
-    return SAMPLER_OK;
+    return launch_col_kernel(fn, p, g, stream);
 }
 
 int sampler_sample_host(sampler_t h, const sampler_args_t* a, sampler_stream_t stream_)
