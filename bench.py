@@ -38,14 +38,15 @@ METRIC = "sampled rows/s and HBM GB/s vs ~8 TB/s at N=64 V=128000 bf16, mixed pa
 UNIT = "rows/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = ("row_sampler.cuh", "row_sampler_kernel.cuh", "philox.cuh", "ptx.cuh",
-                  "sampler_api.cu")
+KERNEL_DIR = os.path.join(ROOT, "decode_step_token_gb300", "csrc")
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "decode_step_token_gb300", "csrc", f), "rb") as fh:
+    for f in sorted(os.listdir(KERNEL_DIR)):
+        if not f.endswith((".cu", ".cuh")):
+            continue
+        with open(os.path.join(KERNEL_DIR, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -77,15 +78,29 @@ def measured_peaks():
 
 
 def traffic_record():
-    """dram bytes per launch from the committed ncu summary, if it matches this kernel."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """dram bytes per launch of the dominant kernel, from the committed ncu summaries
+    (profiles/*.md lines `kernel_hash: ...` and `dram_bytes_per_launch: ...`), if one
+    was taken on the kernel as it is now."""
+    pdir = os.path.join(ROOT, "profiles")
+    want = kernel_hash()
     try:
-        with open(path) as f:
-            d = json.load(f)
-        if d.get("kernel_hash") == kernel_hash():
-            return d
-    except Exception:
-        pass
+        names = sorted(os.listdir(pdir))
+    except OSError:
+        return None
+    for name in names:
+        if not name.endswith(".md"):
+            continue
+        fields = {}
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                if ":" in line and not line.startswith(("|", "#", " ")):
+                    k, _, v = line.partition(":")
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_hash") == want and "dram_bytes_per_launch" in fields:
+            try:
+                return {"dram_bytes_per_launch": int(fields["dram_bytes_per_launch"]), "source": name}
+            except ValueError:
+                continue
     return None
 
 
