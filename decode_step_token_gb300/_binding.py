@@ -33,6 +33,7 @@ SAMPLER_ROW_BAD_HISTORY = 4
 SAMPLER_ROW_TIMEOUT = 5
 
 SAMPLER_CREATE_HOST_STAGING = 1
+SAMPLER_CREATE_ROW_KERNEL = 2
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
             "sampler_status_string", "sampler_abi_version", "sampler_get_stat",

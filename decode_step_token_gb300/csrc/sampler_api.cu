@@ -11,6 +11,7 @@
 #include <new>
 
 #include "colsplit_kernel.cuh"
+#include "group_sampler_kernel.cuh"
 #include "row_sampler_kernel.cuh"
 #include "sampler.h"
 
@@ -63,6 +64,9 @@ struct sampler_s {
     uint32_t flags;
     size_t smem_set[4];  // dynamic shared memory already granted per kernel variant
     size_t col_smem_set[2];
+    size_t grp_smem_set[4];
+    size_t grp_occ_smem[4];  // shared memory of the cached cluster occupancy below
+    int grp_occ[4];          // co-resident clusters of the fork-group kernel
     // workspace of the unit-split path: per-(row, unit) records and the grid barrier
     dst::col::ColRec* col_rec;
     dst::col::GridBar* col_bar;
@@ -85,10 +89,156 @@ struct ColGeometry {
 bool col_eligible(sampler_t h, const sampler_args_t* a, ColGeometry* g);
 int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaStream_t stream);
 
+// ---------------------------------------------------------------- fork-group kernel
+constexpr size_t kTwoPerSm = 113 * 1024;  // dynamic shared memory that lets two CTAs share an SM
+
+struct GroupGeometry {
+    int parts;       // CTAs per cluster
+    int slice;       // elements per CTA
+    int list_cap, part_cap;
+    uint32_t off_list, off_cand, off_cnt, off_stage;
+    size_t smem;
+};
+
+// Parts of at most 64 KB each (up to eight), then the largest candidate lists that
+// keep two CTAs per SM; fp32 rows with penalties reuse the count table's space for
+// the lists (the counts are folded into the staged row before any list exists).
+bool group_geometry(int64_t V, int esize, bool pen, GroupGeometry* g)
+{
+    const int64_t parts = std::min<int64_t>(dst::grp::kMaxParts, std::max<int64_t>(1, (V * esize + 65535) / 65536));
+    int64_t l = (V + parts - 1) / parts;
+    l = (l + 15) & ~int64_t(15);
+    g->parts = int(parts);
+    g->slice = int(l);
+    const size_t head = (sizeof(dst::grp::GShared) + 127) & ~size_t(127);
+    const size_t stage = align16(size_t(l) * esize + 32);
+    const size_t cnt = pen ? align16(size_t(l) * 2 + 16) : 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        const size_t limit = pass == 0 ? kTwoPerSm : size_t(kMaxSmem) - 1024;
+        for (int cap = 4096; cap >= (pass == 0 ? 1024 : 256); cap >>= 1) {
+            // the leader also bins the row's thread maxima (4 x 256 words) in the list area
+            if (size_t(cap) * 8 < 4096) break;
+            const int pcap = std::min(cap, 1024);
+            const size_t lists = size_t(cap) * 8 + size_t(pcap) * 8;
+            const bool alias = pen && esize == 4;
+            const size_t region = alias ? std::max(cnt, lists) : lists + cnt;
+            const size_t total = head + region + stage;
+            if (total > limit) continue;
+            g->list_cap = cap;
+            g->part_cap = pcap;
+            g->off_list = uint32_t(head);
+            g->off_cand = uint32_t(head + size_t(cap) * 8);
+            g->off_cnt = uint32_t(alias ? head : head + lists);
+            g->off_stage = uint32_t(head + region);
+            g->smem = total;
+            return true;
+        }
+    }
+    return false;
+}
+
+template <typename InT, bool kPen>
+void* grp_kernel_ptr()
+{
+    return reinterpret_cast<void*>(&dst::grp::group_kernel<InT, kPen>);
+}
+
+void* grp_pick(int dtype, bool pen)
+{
+    if (dtype == SAMPLER_DTYPE_BF16) return pen ? grp_kernel_ptr<uint16_t, true>() : grp_kernel_ptr<uint16_t, false>();
+    return pen ? grp_kernel_ptr<float, true>() : grp_kernel_ptr<float, false>();
+}
+
+int launch_group(sampler_t h, const sampler_args_t* a, const GroupGeometry& gg, cudaStream_t stream)
+{
+    const bool pen = a->hist_offsets != nullptr;
+    void* fn = grp_pick(a->dtype, pen);
+    const int slot = kernel_slot(a->dtype, pen);
+    if (h->grp_smem_set[slot] < gg.smem) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(gg.smem)) != cudaSuccess)
+            return SAMPLER_ERR_CUDA;
+        h->grp_smem_set[slot] = gg.smem;
+    }
+    dst::grp::GroupParams p;
+    std::memset(&p, 0, sizeof p);
+    dst::KernelParams& k = p.k;
+    k.logits = a->logits;
+    k.vocab = a->vocab;
+    k.row_stride = a->row_stride;
+    k.n_logit_rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
+    k.logit_row = a->logit_row;
+    k.temperature = a->temperature;
+    k.top_k = a->top_k;
+    k.top_p = a->top_p;
+    k.min_p = a->min_p;
+    k.presence = a->presence_penalty;
+    k.frequency = a->frequency_penalty;
+    k.repetition = a->repetition_penalty;
+    k.seed = a->seed;
+    k.has_seed = a->has_seed;
+    k.stream_id = a->stream_id;
+    k.hist_offsets = a->hist_offsets;
+    k.hist_ids = a->hist_ids;
+    k.global_seed = a->global_seed;
+    k.philox_offset = a->philox_offset;
+    k.philox_offset_dev = a->philox_offset_dev;
+    k.out_tokens = a->out_tokens;
+    k.out_probs = a->out_probs;
+    k.out_logprobs = a->out_logprobs;
+    k.out_status = a->out_status;
+    k.slice_len = gg.slice;
+    p.n_rows = int(a->n_rows);
+    p.group = (a->logit_row != nullptr && !pen) ? 1 : 0;
+    p.chunk = p.group ? dst::grp::kMaxForks : 1;
+    p.n_chunks = int((a->n_rows + p.chunk - 1) / p.chunk);
+    p.slice_len = gg.slice;
+    p.list_cap = gg.list_cap;
+    p.part_cap = gg.part_cap;
+    p.off_list = gg.off_list;
+    p.off_cand = gg.off_cand;
+    p.off_cnt = gg.off_cnt;
+    p.off_stage = gg.off_stage;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.blockDim = dim3(dst::grp::kT, 1, 1);
+    cfg.dynamicSmemBytes = gg.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(gg.parts);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid: as many clusters as fit at once, never more than chunks
+    if (h->grp_occ_smem[slot] != gg.smem || h->grp_occ[slot] < 1) {
+        cfg.gridDim = dim3(unsigned(gg.parts), 1, 1);
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, fn, &cfg) != cudaSuccess || nc < 1) {
+            cudaGetLastError();
+            return SAMPLER_ERR_CUDA;
+        }
+        h->grp_occ[slot] = nc;
+        h->grp_occ_smem[slot] = gg.smem;
+    }
+    const int clusters = std::max(1, std::min(h->grp_occ[slot], p.n_chunks));
+    cfg.gridDim = dim3(unsigned(clusters * gg.parts), 1, 1);
+    void* args[] = {&p};
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
 int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
 {
     ColGeometry cg;
     if (col_eligible(h, a, &cg)) return launch_col(h, a, cg, stream);
+    {
+        GroupGeometry gg;
+        const int es = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
+        if (!(h->flags & SAMPLER_CREATE_ROW_KERNEL) && group_geometry(a->vocab, es, a->hist_offsets != nullptr, &gg))
+            return launch_group(h, a, gg, stream);
+    }
     const bool pen = a->hist_offsets != nullptr;
     const int esize = a->dtype == SAMPLER_DTYPE_BF16 ? 2 : 4;
     const Geometry g = geometry(a->vocab, esize, pen);

@@ -111,6 +111,11 @@ typedef struct {
  * fp32 logits, probs, logprobs, and the per-row arrays). */
 #define SAMPLER_CREATE_HOST_STAGING 1u
 
+/* Serve the batches that the small-batch kernel does not take with the
+ * cluster-per-output-row kernel instead of the fork-group kernel (same results;
+ * kept to cross-check the two). */
+#define SAMPLER_CREATE_ROW_KERNEL 2u
+
 /*
  * Arguments of one sampling call. For sampler_sample every pointer is a device
  * pointer; for sampler_sample_host every pointer is a host pointer. The caller

@@ -10,12 +10,15 @@ from parity import compare
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def sampler():
+@pytest.fixture(scope="module", params=["group", "row"])
+def sampler(request):
+    """Both large-batch kernels: the fork-group kernel (default) and the
+    cluster-per-row kernel (SAMPLER_CREATE_ROW_KERNEL); small batches without
+    outputs take the unit-split kernel either way."""
     from decode_step_token_gb300 import build
     build.build_library()
     import decode_step_token_gb300 as d
-    s = d.Sampler(max_rows=2048, max_vocab=262144, host_staging=False)
+    s = d.Sampler(max_rows=2048, max_vocab=262144, host_staging=False, row_kernel=request.param == "row")
     yield s
     s.close()
 
@@ -70,6 +73,22 @@ def test_forks_full_size(sampler):
 def test_forks_with_probs_sampled_rows(sampler):
     b = workloads.forks(base_rows=24)
     _check(sampler, b, want_probs=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fork_groups_irregular(sampler, dtype):
+    """Runs of forks of every length (longer than one group, split, interleaved),
+    each fork with its own parameters and stream."""
+    rng = np.random.default_rng(12)
+    lrow = np.int32([0, 0, 0, 1, 1, 2] + [3] * 12 + [0, 4, 4, 1, 2, 2, 3, 3])
+    n = len(lrow)
+    b = workloads.random_batch(77, n, 30000, dtype, want_probs=True)
+    base = workloads.random_batch(78, 5, 30000, dtype)
+    b = b.with_(logits=base.logits, logit_row=lrow,
+                stream_id=rng.integers(0, 2**31, size=n).astype(np.uint32))
+    g, _, _ = _check(sampler, b)
+    g2, _, _ = _check(sampler, b.with_(want_probs=False))
+    assert np.array_equal(g.tokens, g2.tokens)
 
 
 # ----------------------------------------------------------------------------- randomized small
