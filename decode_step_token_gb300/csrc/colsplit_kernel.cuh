@@ -261,33 +261,24 @@ __device__ __forceinline__ float fast_ln_exp1(float w, float lg2w, uint32_t word
     return w < 0.03125f ? series : direct;
 }
 
-struct PlainAcc {
-    GRec best;  // this lane's best token so far (fp32 score)
-    float c2;   // entry bar in the log2 domain: -(best - margin) * log2 e
-};
-
-__device__ __forceinline__ float bar_of(float s)
+// Hardware log2 of a positive normal fp32 value (flush-to-zero form: the inputs
+// here are draws >= 2^-24 and their logs, never denormal).
+__device__ __forceinline__ float lg2_ftz(float x)
 {
-    return -(s - (1e-4f + 1e-6f * fabsf(s))) * 1.4426950408889634f;
+    float r;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
-__device__ __noinline__ void plain_take(PlainAcc& a, float invT, int v, float x, uint32_t word)
+// log2 of E = -ln(u) for the draw of word `word`, branch-free: for 1 - u < 1/32 the
+// series of fast_ln_exp1 (in log2 units), else log2(-log2 u) + log2(ln 2).
+__device__ __forceinline__ float log2_exp1(uint32_t word)
 {
     const float w = noise_one_minus_u(word);
-    const float s = x * invT - fast_ln_exp1(w, __log2f(w), word);
-    if (s > a.best.s || (s == a.best.s && v < a.best.idx)) {
-        a.best = GRec{s, v, x, word};
-        a.c2 = bar_of(s);
-    }
-}
-
-template <int E>
-__device__ __forceinline__ uint32_t picku(const uint32_t (&a)[E], int e)
-{
-    uint32_t r = a[0];
-#pragma unroll
-    for (int i = 1; i < E; ++i) r = (e == i) ? a[i] : r;
-    return r;
+    const float lw = lg2_ftz(w);
+    const float series = w * fmaf(w, fmaf(w, 0.125f, 0.20833333f), 0.5f) * 1.4426950408889634f + lw;
+    const float direct = lg2_ftz(-lg2_ftz(noise_u(word))) - 0.52876637294489771f;
+    return w < 0.03125f ? series : direct;
 }
 
 template <typename InT>
@@ -297,45 +288,10 @@ __device__ __forceinline__ uint4 neg_inf_vec()
     return make_uint4(w, w, w, w);
 }
 
-// Philox words and entry mask of one vector: bit q is set when token vb + q may
-// beat the bar, i.e. x/T - ln(1 - u) clears it.
-template <typename InT>
-__device__ __forceinline__ uint32_t plain_mask(const uint4& raw, int vb, float a2, float c2,
-                                               const PhiloxSchedule& ks, uint32_t stream, uint32_t olo,
-                                               uint32_t ohi, uint32_t (&ws)[Vec<InT>::E])
-{
-    constexpr int EPV = Vec<InT>::E;
-#pragma unroll
-    for (int b = 0; b < EPV / 4; ++b) {
-        const uint4 blk = philox4x32_10(make_uint4(uint32_t(vb >> 2) + b, stream, olo, ohi), ks);
-        ws[4 * b + 0] = blk.x;
-        ws[4 * b + 1] = blk.y;
-        ws[4 * b + 2] = blk.z;
-        ws[4 * b + 3] = blk.w;
-    }
-    uint32_t mask = 0;
-#pragma unroll
-    for (int q = 0; q < EPV; ++q) {
-        const float lg2w = __log2f(noise_one_minus_u(ws[q]));
-        mask |= (fmaf(Vec<InT>::get(raw, q), a2, c2) > lg2w) ? (1u << q) : 0u;
-    }
-    return mask;
-}
-
-template <typename InT>
-__device__ __forceinline__ void plain_takes(PlainAcc& a, float invT, const uint4& raw, int vb, uint32_t mask,
-                                            const uint32_t (&ws)[Vec<InT>::E])
-{
-    while (mask) {
-        const int q = __ffs(mask) - 1;
-        mask &= mask - 1;
-        plain_take(a, invT, vb + q, Vec<InT>::get(raw, q), picku<Vec<InT>::E>(ws, q));
-    }
-}
-
-// Gumbel-max over the unit: a token may win only if x/T - ln(1 - u) clears the
-// lane's bar (its best score so far, less a margin); the exact score is taken
-// only for those. Two vectors per step, for independent work to overlap.
+// Gumbel-max over the unit, scores x/T - ln E in log2 units. A bound with one log2
+// per token filters against the warp's best; vectors with a surviving token are
+// scored exactly by the whole warp at once (a per-lane slow path would diverge).
+// The Philox blocks of a vector come from the row-folded generator.
 template <typename InT>
 __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const uint4* slot, ColRec* rec)
 {
@@ -343,36 +299,70 @@ __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const ui
     const int lane = threadIdx.x & 31;
     const float invT = ri.invT;
     const float a2 = invT * 1.4426950408889634f;
-    const PhiloxSchedule ks = philox_schedule(PhiloxKey{ri.key_lo, ri.key_hi});
-    const uint32_t stream = ri.stream, olo = ri.off_lo, ohi = ri.off_hi;
-    PlainAcc a;
-    a.best = grec_empty();
-    a.c2 = INFINITY;
+    const RowPhilox ph = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, ri.off_lo, ri.off_hi);
+    float c2 = INFINITY;  // minus the bar, log2 units: +inf until the warp has a best
+    float best2 = -INFINITY, bx = 0.0f;
+    int bi = INT_MAX;
+    uint32_t bw = 0;
     float lm = -INFINITY;
     bool nan = false;
 #pragma unroll 1
     for (int st = 0; st < kStages; ++st) {
         wait_stage(st);
         const int e = min((st + 1) * u.q, u.nvec);
+        // a token can beat the warp's best only if x/T - ln(1 - u) clears it (E >= 1 - u):
+        // one log2 per token decides; a vector where any lane has such a token is
+        // scored exactly by the whole warp (a uniform branch), which also lifts the bar
+        // the loop is warp-uniform (every lane runs every step; lanes past the end see
+        // -inf) because the step holds warp-wide votes and shuffles
 #pragma unroll 1
-        for (int j = st * u.q + lane; j < e; j += 64) {
-            const int j2 = j + 32;
-            const uint4 r1 = slot[j];
-            const uint4 r2 = j2 < e ? slot[j2] : neg_inf_vec<InT>();
-            const int vb1 = u.v0 + j * EPV, vb2 = u.v0 + j2 * EPV;  // multiples of 4
-            bool n1, n2;
-            lm = fmaxf(lm, fmaxf(Vec<InT>::vmax(r1, n1), Vec<InT>::vmax(r2, n2)));
-            nan |= n1 || n2;
-            uint32_t w1[EPV], w2[EPV];
-            const uint32_t m1 = plain_mask<InT>(r1, vb1, a2, a.c2, ks, stream, olo, ohi, w1);
-            const uint32_t m2 = plain_mask<InT>(r2, vb2, a2, a.c2, ks, stream, olo, ohi, w2);
-            plain_takes<InT>(a, invT, r1, vb1, m1, w1);
-            plain_takes<InT>(a, invT, r2, vb2, m2, w2);
+        for (int j0 = st * u.q; j0 < e; j0 += 32) {
+            const int j = j0 + lane;
+            const uint4 raw = j < e ? slot[j] : neg_inf_vec<InT>();
+            const int vb = u.v0 + j * EPV;  // a multiple of 4: the vector's blocks start at vb / 4
+            bool vn;
+            lm = fmaxf(lm, Vec<InT>::vmax(raw, vn));
+            nan |= vn;
+            uint32_t ws[EPV];
+#pragma unroll
+            for (int b = 0; b < EPV / 4; ++b) {
+                const uint4 blk = philox_block(ph, uint32_t(vb >> 2) + uint32_t(b));
+                ws[4 * b + 0] = blk.x;
+                ws[4 * b + 1] = blk.y;
+                ws[4 * b + 2] = blk.z;
+                ws[4 * b + 3] = blk.w;
+            }
+            bool pass = false;
+#pragma unroll
+            for (int q = 0; q < EPV; ++q)
+                pass |= fmaf(Vec<InT>::get(raw, q), a2, c2) > lg2_ftz(noise_one_minus_u(ws[q]));
+            if (__any_sync(0xffffffffu, pass)) {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) {
+                    const float s2 = fmaf(Vec<InT>::get(raw, q), a2, -log2_exp1(ws[q]));
+                    if (s2 > best2) {  // tokens come in increasing order: ties keep the first
+                        best2 = s2;
+                        bi = vb + q;
+                    }
+                }
+                float wb = best2;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xffffffffu, wb, off));
+                // bar: the warp's best less the margin of the final comparison (log2 units)
+                if (wb > -INFINITY) c2 = -(wb - (1e-4f + 1e-6f * fabsf(wb * 0.69314718055994531f)) * 1.4426950408889634f);
+            }
         }
+    }
+    // the lane's winner: its logit and Philox word once more
+    if (bi != INT_MAX) {
+        const int jb = (bi - u.v0) / EPV, qb = (bi - u.v0) % EPV;
+        const uint4 rb = slot[jb];
+        bx = Vec<InT>::get(rb, qb);
+        bw = lane_of(philox_block(ph, uint32_t(bi) >> 2), uint32_t(bi) & 3u);
     }
     const uint32_t flags = unit_flags(lm, nan);
     GTop2 t;
-    t.a = a.best;
+    t.a = bi != INT_MAX ? GRec{best2 * 0.69314718055994531f, bi, bx, bw} : grec_empty();
     t.b = grec_empty();
     top2_warp_reduce(t);
     if (lane == 0) {

@@ -63,6 +63,67 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxSchedule& s)
     return c;
 }
 
+// The 32x32 -> 64 product of the two Philox lanes in one instruction.
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo)
+{
+    unsigned long long r;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(r) : "r"(a), "r"(b));
+    lo = uint32_t(r);
+    hi = uint32_t(r >> 32);
+}
+
+// Philox4x32-10 for the counters (b, c1, c2, c3) of one row, where only b varies:
+// the first round's product of counter lane 2 and the second round's product of
+// counter lane 0 depend on the row alone, so they are taken once per row. Same
+// output as philox4x32_10(make_uint4(b, c1, c2, c3), key).
+struct RowPhilox {
+    uint32_t k0[10], k1[10];  // round keys (entries 0 and 1 unused after folding)
+    uint32_t r1z;             // round 1: lane 3 of the counter xor round key 1
+    uint32_t r2x;             // round 2: what lane 0 takes besides the varying product
+    uint32_t r2z;             // round 2: lane 2 is r2z xor the round-1 low product
+    uint32_t r2w;             // round 2 output lane 3 (a row constant)
+};
+
+__device__ __forceinline__ RowPhilox row_philox(PhiloxKey k, uint32_t c1, uint32_t c2, uint32_t c3)
+{
+    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+    RowPhilox p;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        p.k0[round] = k.lo + uint32_t(round) * 0x9E3779B9u;
+        p.k1[round] = k.hi + uint32_t(round) * 0xBB67AE85u;
+    }
+    uint32_t hb, lb, ha, la;
+    mul_wide(kMulB, c2, hb, lb);            // round 1, lane 2: a row constant
+    const uint32_t x1 = hb ^ c1 ^ p.k0[0];  // round 1 output lane 0
+    p.r1z = c3 ^ p.k1[0];
+    mul_wide(kMulA, x1, ha, la);            // round 2, lane 0: a row constant
+    p.r2x = lb ^ p.k0[1];
+    p.r2z = ha ^ p.k1[1];
+    p.r2w = la;
+    return p;
+}
+
+__device__ __forceinline__ uint4 philox_block(const RowPhilox& p, uint32_t b)
+{
+    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+    uint32_t ha, la, hb, lb;
+    mul_wide(kMulA, b, ha, la);                 // round 1, lane 0
+    mul_wide(kMulB, ha ^ p.r1z, hb, lb);        // round 2, lane 2
+    uint32_t x = hb ^ p.r2x, y = lb, z = p.r2z ^ la, w = p.r2w;
+#pragma unroll
+    for (int round = 2; round < 10; ++round) {
+        mul_wide(kMulA, x, ha, la);
+        mul_wide(kMulB, z, hb, lb);
+        const uint32_t nx = hb ^ y ^ p.k0[round], nz = ha ^ w ^ p.k1[round];
+        x = nx;
+        y = lb;
+        z = nz;
+        w = la;
+    }
+    return make_uint4(x, y, z, w);
+}
+
 __device__ __forceinline__ uint32_t lane_of(uint4 b, uint32_t i)
 {
     return i == 0 ? b.x : (i == 1 ? b.y : (i == 2 ? b.z : b.w));
