@@ -173,41 +173,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Bitonic sort, descending, of the 128 keys a warp holds four per lane (key q of
-// lane l is element 32 q + l). The stage loop stays rolled: one short body.
-__device__ __forceinline__ void warp_sort128_u32_desc(uint32_t (&a)[4])
-{
-    const int lane = threadIdx.x & 31;
-#pragma unroll 1
-    for (int size = 2; size <= 128; size <<= 1) {
-#pragma unroll 1
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride >= 32) {
-                const int qs = stride >> 5;  // 1 or 2
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int p = q ^ qs;
-                    if (p > q) {
-                        const bool desc = ((q * 32) & size) == 0;
-                        const uint32_t x = a[q], y = a[p];
-                        const bool sw = desc ? (x < y) : (x > y);
-                        a[q] = sw ? y : x;
-                        a[p] = sw ? x : y;
-                    }
-                }
-            } else {
-                const bool low = (lane & stride) == 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t o = __shfl_xor_sync(0xffffffffu, a[q], stride);
-                    const bool desc = ((q * 32 + lane) & size) == 0;
-                    a[q] = (low == desc) ? max(a[q], o) : min(a[q], o);
-                }
-            }
-        }
-    }
-}
-
 // Sort n <= kBufCap words in warp-private shared memory, descending (bitonic,
 // padded to a power of two with zeros; the array must hold that many words).
 __device__ __forceinline__ void warp_sort_smem_desc(unsigned long long* a, int n)

@@ -377,17 +377,42 @@ __device__ __noinline__ void unit_plain(const Unit u, const RowInfo ri, const ui
 
 // ---------------------------------------------------------------- truncated units
 // The unit's top-C list (C = k for k <= 64, else 64), sorted by (value desc,
-// index asc): tau = the C-th largest of 128 group maxima (each lane deals its
-// vectors to four groups in turn) is reached by at least C of the unit's tokens,
-// so its top C are among the tokens >= tau, which are gathered and sorted.
-template <typename InT>
-__device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uint4* slot,
-                                       unsigned long long* buf, ColRec* rec)
+// index asc): each lane deals its vectors to GPL groups in turn (GPL = 1, 2 or 4
+// as C needs), tau = the C-th largest of the 32 GPL group maxima -- found by a
+// bitwise search counted with warp ballots -- is reached by at least C of the
+// unit's tokens, so the unit's top C are among the tokens >= tau, which are
+// gathered and sorted.
+template <int GPL>
+__device__ __forceinline__ uint32_t kth_group_max(const float (&g)[GPL], int C)
+{
+    // the largest key K with at least C group maxima >= K, one bit at a time from
+    // the top: each step counts the qualifying maxima of the warp with ballots
+    uint32_t key[GPL];
+#pragma unroll
+    for (int a = 0; a < GPL; ++a) key[a] = f2key(g[a]);
+    uint32_t K = 0;
+#pragma unroll 1
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t cand = K | (1u << b);
+        int n = 0;
+#pragma unroll
+        for (int a = 0; a < GPL; ++a) n += __popc(__ballot_sync(0xffffffffu, key[a] >= cand));
+        if (n >= C) K = cand;
+    }
+    return K;
+}
+
+template <typename InT, int GPL>
+__device__ __forceinline__ void unit_cand_impl(const Unit u, const RowInfo ri, const uint4* slot,
+                                               unsigned long long* buf, ColRec* rec)
 {
     constexpr int EPV = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
     const int C = ri.small_k ? ri.k : kCandCap;
-    float mx = -INFINITY, g0 = -INFINITY, g1 = -INFINITY, g2 = -INFINITY, g3 = -INFINITY;
+    float mx = -INFINITY;
+    float g[GPL];
+#pragma unroll
+    for (int a = 0; a < GPL; ++a) g[a] = -INFINITY;
     int am = INT_MAX;
     bool nan = false;
 #pragma unroll 1
@@ -404,18 +429,16 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
                 mx = m;
                 am = u.v0 + j * EPV + vec_find<InT>(raw, m);
             }
-            const float g = fmaxf(g0, m);  // this vector joins group 0, then the groups rotate
-            g0 = g1;
-            g1 = g2;
-            g2 = g3;
-            g3 = g;
+            // this vector joins group 0, then the groups rotate
+            const float gn = fmaxf(g[0], m);
+#pragma unroll
+            for (int a = 0; a + 1 < GPL; ++a) g[a] = g[a + 1];
+            g[GPL - 1] = gn;
         }
     }
     const uint32_t flags = unit_flags(mx, nan);
     warp_maxidx(mx, am);
-    uint32_t gk[4] = {f2key(g0), f2key(g1), f2key(g2), f2key(g3)};
-    warp_sort128_u32_desc(gk);
-    const uint32_t tauk = __shfl_sync(0xffffffffu, C <= 32 ? gk[0] : gk[1], (C - 1) & 31);
+    const uint32_t tauk = kth_group_max<GPL>(g, C);
     const float tau = key2f(tauk);
     // tokens >= tau (finite), each lane into its own kSeg words of buf (word i of
     // lane l at buf[32 i + l]); and, for top-p without top-k, the unit's mass
@@ -427,17 +450,26 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
     for (int j = lane; j < u.nvec; j += 32) {
         const uint4 raw = slot[j];
         const int vb = u.v0 + j * EPV;
+        if (need_z) {
+#pragma unroll
+            for (int q = 0; q < EPV; ++q) {
+                const float x = Vec<InT>::get(raw, q);
+                if (x > -INFINITY) {
+                    const float y = __expf((x - mx) * invT) - zc;
+                    const float s2 = zs + y;
+                    zc = (s2 - zs) - y;
+                    zs = s2;
+                }
+            }
+        } else {
+            bool vn;
+            if (!(Vec<InT>::vmax(raw, vn) >= tau)) continue;  // no token of the vector qualifies
+        }
         uint32_t mask = 0;
 #pragma unroll
         for (int q = 0; q < EPV; ++q) {
             const float x = Vec<InT>::get(raw, q);
             mask |= (x >= tau && x > -INFINITY) ? (1u << q) : 0u;
-            if (need_z && x > -INFINITY) {
-                const float y = __expf((x - mx) * invT) - zc;
-                const float s2 = zs + y;
-                zc = (s2 - zs) - y;
-                zs = s2;
-            }
         }
         while (mask) {
             const int q = __ffs(mask) - 1;
@@ -488,6 +520,16 @@ __device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uin
         rec->tau = tauk;
     }
     __syncwarp();
+}
+
+template <typename InT>
+__device__ __noinline__ void unit_cand(const Unit u, const RowInfo ri, const uint4* slot,
+                                       unsigned long long* buf, ColRec* rec)
+{
+    const int C = ri.small_k ? ri.k : kCandCap;
+    if (C <= 16) unit_cand_impl<InT, 1>(u, ri, slot, buf, rec);
+    else if (C <= 32) unit_cand_impl<InT, 2>(u, ri, slot, buf, rec);
+    else unit_cand_impl<InT, 4>(u, ri, slot, buf, rec);
 }
 
 // ---------------------------------------------------------------- one unit (phase 1)
