@@ -267,51 +267,41 @@ __device__ __forceinline__ unsigned long long block_incl_scan_u64(unsigned long 
 
 // Leader CTA: the smallest thread maximum t such that the thread maxima >= t reach
 // `target` -- a count, or their mass in units of 2^-20 of exp((x - m) / Te), each
-// term rounded down -- or NaN when all of them fall short. Two rounds of 256
-// value bins: over [min maximum, m], then inside the bin where the target is met.
+// term rounded down -- or NaN when all of them fall short. Two rounds of 256 bins:
+// on a log scale of the distance to m, then evenly inside the bin where the target
+// is met. Bins only order the values (larger bin, smaller value).
 // `bins` is 4 x 256 words of shared memory.
 __device__ __noinline__ float tmax_select(GShared& sh, uint32_t* bins, const float* v, int C, float m, float tmin,
                                           bool mass, float invT, unsigned long long target)
 {
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     uint32_t* bcnt = bins;
     uint32_t* bmin = bins + 256;
     uint32_t* bmax = bins + 512;
     uint32_t* bms = bins + 768;
     float lo = tmin, hi = m;
     unsigned long long pre = 0;
+    // level-0 bin = 16 log2(1 + 64 (m - x) / (m - min maximum)): about 97 bins in all
+    const float invT_bins = (m > tmin && m - tmin < INFINITY) ? 64.0f / (m - tmin) : 1.0f;
     for (int level = 0; level < 2; ++level) {
         bcnt[tid] = 0;
         bmin[tid] = 0xFFFFFFFFu;
         bmax[tid] = 0;
         bms[tid] = 0;
         __syncthreads();
+        // level 0: bins on a log scale of the distance to m (heavy tails and narrow
+        // rows alike spread over them); level 1: even bins inside the chosen bin
         const float inv = hi > lo ? 256.0f / (hi - lo) : 0.0f;
         for (int c = 0; c < C; ++c) {
             const float x = v[c];
-            const bool in = x > -INFINITY && x >= lo && x <= hi;
-            const int bin = in ? min(255, max(0, int((hi - x) * inv))) : 256;
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (bin < 256) {
-                const uint32_t key = f2key(x);
-                const uint32_t wq = mass ? uint32_t(expf((x - m) * invT) * 1048576.0f) : 0u;
-                uint32_t kmin = key, kmax = key, wsum = 0;
-                unsigned rest = peers;
-                while (rest) {
-                    const int j = __ffs(rest) - 1;
-                    rest &= rest - 1;
-                    const uint32_t kj = __shfl_sync(peers, key, j);
-                    kmin = min(kmin, kj);
-                    kmax = max(kmax, kj);
-                    wsum += __shfl_sync(peers, wq, j);
-                }
-                if (lane == __ffs(peers) - 1) {
-                    atomicAdd(&bcnt[bin], uint32_t(__popc(peers)));
-                    atomicMin(&bmin[bin], kmin);
-                    atomicMax(&bmax[bin], kmax);
-                    if (mass) atomicAdd(&bms[bin], wsum);
-                }
-            }
+            if (!(x > -INFINITY && x >= lo && x <= hi)) continue;
+            const int bin = level == 0 ? min(255, int(__log2f(1.0f + (m - x) * invT_bins) * 16.0f))
+                                       : min(255, max(0, int((hi - x) * inv)));
+            const uint32_t key = f2key(x);
+            atomicAdd(&bcnt[bin], 1u);
+            atomicMin(&bmin[bin], key);
+            atomicMax(&bmax[bin], key);
+            if (mass) atomicAdd(&bms[bin], uint32_t(expf((x - m) * invT) * 1048576.0f));
         }
         __syncthreads();
         const unsigned long long w = mass ? (unsigned long long)bms[tid] : (unsigned long long)bcnt[tid];
@@ -594,6 +584,49 @@ __device__ __noinline__ void plain_fork(GShared& sh, const Part& pt, int f)
 
 // Pick pass of fork f over this CTA's part: the best two Gumbel scores among the
 // kept tokens and their mass relative to the row max.
+// One warp's pick pass of a listed fork f over this CTA's candidate list: the best
+// two exact fp32 Gumbel scores among the kept tokens and their mass (lane 0 stores).
+__device__ __noinline__ void pick_warp(GShared& sh, int f, const unsigned long long* cand, int ncand)
+{
+    const int lane = threadIdx.x & 31;
+    const RowParams& rp = sh.rp[f];
+    const ForkOut& fo = sh.bc.f[f];
+    const float m = sh.bc.m;
+    const bool hb = fo.has_bound != 0, mp = rp.do_minp != 0;
+    const float a2 = rp.invT * 1.4426950408889634f;
+    GTop2 t;
+    t.a = grec_empty();
+    t.b = grec_empty();
+    float s = 0.0f, comp = 0.0f;
+    for (int i = lane; i < ncand; i += 32) {
+        const unsigned long long w = cand[i];
+        const float x = key2f(cand_key(w));
+        const int v = cand_idx(w);
+        if (!(x > -INFINITY)) continue;
+        if (hb && !in_prefix(cand_key(w), v, fo.bkey, fo.bidx)) continue;
+        if (mp && !(x >= fo.xthr)) continue;
+        if (!rp.greedy) {
+            const uint32_t word = noise_word(rp, v);
+            top2_insert(t, GRec{x * rp.invT - logf(noise_exp1_f32(word)), v, x, word});
+        }
+        if (rp.want_out) {
+            const float e = exp2f((x - m) * a2);
+            const float y = e - comp;
+            const float u = s + y;
+            comp = (u - s) - y;
+            s = u;
+        }
+    }
+    top2_warp_reduce(t);
+    double z = double(s) - double(comp);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (lane == 0) {
+        sh.part.g[f] = t;
+        sh.part.zk[f] = z;
+    }
+}
+
 // A fork whose kept tokens are all listed reads only this CTA's candidate list.
 template <typename InT>
 __device__ __noinline__ void pick_part(GShared& sh, const Part& pt, int f, const unsigned long long* cand,
@@ -1293,21 +1326,32 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
                     if (sh.bc.f[f].kind == kKindExact) exact_fork<InT>(sh, pt, rank, C, f);
             }
 
-            // ---- pick pass: Gumbel-max and kept mass over the kept tokens of each fork
+            // ---- pick pass: Gumbel-max and kept mass over the kept tokens of each fork;
+            // a listed fork takes one warp over this CTA's candidates (all such forks at
+            // once), any other the whole CTA over the staged part
             bool any_pick = false;
             for (int f = 0; f < g; ++f) {
                 const RowParams& rp = sh.rp[f];
                 const bool pk = sh.bc.f[f].kind == kKindPick && (!rp.greedy || rp.want_out);
                 any_pick |= pk;
-                if (pk) pick_part<InT>(sh, pt, f, cand, min(sh.ncand, P.part_cap));
+                if (pk && !sh.bc.f[f].listed) pick_part<InT>(sh, pt, f, cand, 0);
+            }
+            if (wid < g) {
+                const RowParams& rp = sh.rp[wid];
+                const ForkOut& fo = sh.bc.f[wid];
+                if (fo.kind == kKindPick && fo.listed && (!rp.greedy || rp.want_out))
+                    pick_warp(sh, wid, cand, min(sh.ncand, P.part_cap));
             }
             if (any_pick) {
+                __syncthreads();
                 cluster_sync();
-                if (rank == 0 && wid == 0) {
-                    const bool have = lane < int(C);
-                    for (int f = 0; f < g; ++f) {
-                        const RowParams& rp = sh.rp[f];
-                        if (!(sh.bc.f[f].kind == kKindPick && (!rp.greedy || rp.want_out))) continue;
+                // leader: warp f merges fork f over the CTAs and settles it
+                if (rank == 0 && wid < g) {
+                    const int f = wid;
+                    const RowParams& rp = sh.rp[f];
+                    ForkOut& fo = sh.bc.f[f];
+                    if (fo.kind == kKindPick && (!rp.greedy || rp.want_out)) {
+                        const bool have = lane < int(C);
                         GTop2 t;
                         t.a = grec_empty();
                         t.b = grec_empty();
@@ -1320,20 +1364,9 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
                         top2_warp_reduce(t);
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-                        __syncwarp();
                         if (lane == 0) {
-                            sh.part.g[f] = t;
-                            sh.part.zk[f] = z;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane < g) {
-                        const int f = lane;
-                        const RowParams& rp = sh.rp[f];
-                        ForkOut& fo = sh.bc.f[f];
-                        if (fo.kind == kKindPick && (!rp.greedy || rp.want_out)) {
-                            if (!rp.greedy) fo.token = settle_pair(sh.part.g[f], rp.T);
-                            if (rp.want_out) fo.lnz = logf(float(sh.part.zk[f]));
+                            if (!rp.greedy) fo.token = settle_pair(t, rp.T);
+                            if (rp.want_out) fo.lnz = logf(float(z));
                         }
                     }
                 }
