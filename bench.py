@@ -77,10 +77,11 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record():
+def traffic_record(workload: str):
     """dram bytes per launch of the dominant kernel, from the committed ncu summaries
-    (profiles/*.md lines `kernel_hash: ...` and `dram_bytes_per_launch: ...`), if one
-    was taken on the kernel as it is now."""
+    (profiles/*.md lines `kernel_hash: ...`, `workload: ...` and
+    `dram_bytes_per_launch: ...`), if one was taken on this workload with the
+    kernels as they are now."""
     pdir = os.path.join(ROOT, "profiles")
     want = kernel_hash()
     try:
@@ -96,6 +97,8 @@ def traffic_record():
                 if ":" in line and not line.startswith(("|", "#", " ")):
                     k, _, v = line.partition(":")
                     fields[k.strip()] = v.strip()
+        if fields.get("workload", workload) != workload:
+            continue
         if fields.get("kernel_hash") == want and "dram_bytes_per_launch" in fields:
             try:
                 return {"dram_bytes_per_launch": int(fields["dram_bytes_per_launch"]), "source": name}
@@ -299,7 +302,7 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     launch_s = ms_step / 1e3
     achieved = step_bytes / launch_s / 1e9
-    tr = traffic_record()
+    tr = traffic_record(batch.name)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": tr["dram_bytes_per_launch"] if tr else None,
             "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth), kernel timed inside a graph "
