@@ -2,8 +2,8 @@
 //
 // Each row is cut into G equal vocabulary units, and the N x G units are spread
 // over every warp of a cooperative grid (one CTA of 16 warps per SM), one unit
-// per warp when the batch allows. The kernel runs in two phases split by one
-// grid-wide barrier:
+// per warp when the batch allows. The kernel runs in two phases; a row's
+// phase 2 starts once all of that row's units are done (no grid-wide barrier):
 //
 //   phase 1  a warp copies its unit into its own shared-memory slot (16-byte
 //            cp.async copies in four groups; work starts on the first while the
@@ -24,10 +24,12 @@
 //
 // A truncated row whose kept set reaches below what the lists cover is sampled
 // exactly by its phase-2 CTA, streaming the row from global memory (radix
-// select by count or fixed-point softmax mass, then a Gumbel pass). The grid
-// barrier is the only wait on other CTAs (the cooperative launch makes them
-// co-resident); it gives up after a bounded number of polls and marks the rows
-// SAMPLER_ROW_TIMEOUT.
+// select by count or fixed-point softmax mass, then a Gumbel pass). A row's
+// finishing CTA waits only for that row: every unit adds one to the row's
+// counter once its record is written (release), and the finisher polls it
+// (acquire) until all G units are in, then sets it back to zero. The cooperative
+// launch keeps every CTA resident, so each wait ends; it gives up after a
+// bounded number of polls and marks the row SAMPLER_ROW_TIMEOUT.
 #pragma once
 
 #include "row_sampler.cuh"
@@ -66,11 +68,10 @@ struct alignas(16) ColRec {  // one (row, unit) summary
     unsigned long long cand[kCandCap];  // truncated rows: the unit's top list, descending
 };
 
-struct GridBar {      // grid barrier state, zero-initialised once
-    uint32_t count;   // CTAs arrived (back to 0 after every barrier)
-    uint32_t gen;     // bumped by the last arrival
-    uint32_t poison;  // set when a CTA gave up waiting: later barriers fail at once
-    uint32_t pad;
+struct RowSync {                // zero-initialised once; every launch leaves it zero
+    uint32_t done[kMaxRows];    // units of each row whose record is written
+    uint32_t poison;            // set when a wait gave up: later waits fail at once
+    uint32_t pad[3];
 };
 
 struct ColParams {
@@ -80,7 +81,7 @@ struct ColParams {
     int32_t w;        // elements per unit (a multiple of 16 bytes)
     int32_t n_units;  // n_rows * gc
     ColRec* rec;      // [n_rows][gc]
-    GridBar* bar;
+    RowSync* sync;
     unsigned long long* stats;  // [0] rows finished by the exact path (diagnostic)
 };
 

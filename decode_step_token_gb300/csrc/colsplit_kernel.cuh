@@ -564,38 +564,36 @@ __device__ __forceinline__ void unit_step(const ColParams& P, int uid, uint4* sl
             rec->nc = 0;
         }
     }
+    // the record is complete: count the unit in (release after the warp's writes)
     __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        atomicAdd(&P.sync->done[u.r], 1u);
+    }
 }
 
-// ---------------------------------------------------------------- grid barrier
+// ---------------------------------------------------------------- row readiness
 constexpr uint32_t kBarPolls = 1u << 24;  // about a second of polling
 
-// Every CTA of the (cooperative) grid waits here until all have arrived; the
-// writes before it are visible to every CTA after it. Returns false if this
-// CTA gave up waiting (the barrier is then marked broken for later launches).
-__device__ __noinline__ bool grid_sync(ColShared& sh, GridBar* bar)
+// The whole CTA waits until all G units of row r have written their records; the
+// records are then visible to every thread of the CTA. Returns false if the wait
+// gave up (the state is then marked broken for later launches).
+__device__ __noinline__ bool wait_row(ColShared& sh, RowSync* sync, int r, int G)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        const uint32_t gen = ld_acquire_gpu(&bar->gen);
-        if (ld_acquire_gpu(&bar->poison) != 0u) {
+        if (ld_acquire_gpu(&sync->poison) != 0u) {
             ok = 0;
         } else {
-            const uint32_t arrived = atom_add_acq_rel_gpu(&bar->count, 1u);
-            if (arrived == gridDim.x - 1) {
-                bar->count = 0u;
-                st_release_gpu(&bar->gen, gen + 1u);
-            } else {
-                uint32_t polls = 0;
-                while (ld_acquire_gpu(&bar->gen) == gen) {
-                    if (++polls > kBarPolls) {
-                        ok = 0;
-                        atomicExch(&bar->poison, 1u);
-                        break;
-                    }
-                    if (polls > 256) __nanosleep(64);
+            uint32_t polls = 0;
+            while (ld_acquire_gpu(&sync->done[r]) < uint32_t(G)) {
+                if (++polls > kBarPolls) {
+                    ok = 0;
+                    atomicExch(&sync->poison, 1u);
+                    break;
                 }
+                if (polls > 64) __nanosleep(32);
             }
         }
         sh.bar_ok = ok;
@@ -966,12 +964,11 @@ __global__ void __launch_bounds__(kT, 1) colsplit_kernel(const ColParams P)
     for (int u = blockIdx.x + gridDim.x * wid; u < P.n_units; u += gridDim.x * kW)
         unit_step<InT>(P, u, slot, buf);
 
-    const bool ok = grid_sync(sh, P.bar);
-
-    // ---- phase 2: rows, dealt round-robin to the CTAs
+    // ---- phase 2: rows, dealt round-robin to the CTAs; each waits for its own units
     const KernelParams& kp = P.k;
 #pragma unroll 1
     for (int r = blockIdx.x; r < P.n_rows; r += gridDim.x) {
+        const bool ok = wait_row(sh, P.sync, r, P.gc);
         int lrow = r;
         if (kp.logit_row) lrow = kp.logit_row[r];
         const bool lrow_ok = lrow >= 0 && int64_t(lrow) < kp.n_logit_rows;
@@ -986,6 +983,9 @@ __global__ void __launch_bounds__(kT, 1) colsplit_kernel(const ColParams P)
         } else if (wid == 0) {
             finish_row(P, r, ri);
         }
+        // the row's records are read: zero its counter for the next launch
+        __syncthreads();
+        if (tid == 0 && ok) P.sync->done[r] = 0u;
     }
     __syncthreads();
 

@@ -67,9 +67,9 @@ struct sampler_s {
     size_t grp_smem_set[4];
     size_t grp_occ_smem[4];  // shared memory of the cached cluster occupancy below
     int grp_occ[4];          // co-resident clusters of the fork-group kernel
-    // workspace of the unit-split path: per-(row, unit) records and the grid barrier
+    // workspace of the unit-split path: per-(row, unit) records and the per-row counters
     dst::col::ColRec* col_rec;
-    dst::col::GridBar* col_bar;
+    dst::col::RowSync* col_bar;
     unsigned long long* stats;  // device counters (diagnostics)
     int col_rows;
     int64_t col_units;  // records in col_rec
@@ -372,7 +372,8 @@ void fill_col_params(dst::col::ColParams& p, const sampler_args_t* a, const ColG
     p.n_units = int(g.units);
 }
 
-// A cooperative launch: the CTAs meet at a grid barrier, so all must be resident.
+// A cooperative launch: a row's finishing CTA waits for units on other CTAs, so all
+// must be resident.
 int launch_col_kernel(void* fn, dst::col::ColParams& p, const ColGeometry& g, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg;
@@ -405,7 +406,7 @@ int launch_col(sampler_t h, const sampler_args_t* a, const ColGeometry& g, cudaS
     dst::col::ColParams p;
     fill_col_params(p, a, g);
     p.rec = h->col_rec;
-    p.bar = h->col_bar;
+    p.sync = h->col_bar;
     p.stats = h->stats;
     return launch_col_kernel(fn, p, g, stream);
 }
@@ -427,16 +428,16 @@ int check_args(sampler_t h, const sampler_args_t* a)
 }  // namespace
 
 // ---------------------------------------------------------------- allocation-free entry
-// The unit-split kernel's workspace (the grid barrier, then the per-(row, unit)
+// The unit-split kernel's workspace (the per-row counters, then the per-(row, unit)
 // records) lives in this module's own device memory for sampler_sample_noalloc.
 namespace {
 
 constexpr int kNoAllocRows = SAMPLER_NOALLOC_MAX_ROWS;
-constexpr size_t kNoAllocCounterBytes = 256;  // the grid barrier, padded
+constexpr size_t kNoAllocCounterBytes = 2048;  // the per-row counters, padded
 constexpr size_t kNoAllocScratchBytes = size_t(9) << 19;  // 4.5 MiB: 64 rows of up to 262144
 constexpr int64_t kNoAllocUnits =
     int64_t((kNoAllocScratchBytes - kNoAllocCounterBytes) / sizeof(dst::col::ColRec));
-static_assert(sizeof(dst::col::GridBar) <= kNoAllocCounterBytes, "barrier area");
+static_assert(sizeof(dst::col::RowSync) <= kNoAllocCounterBytes, "row counter area");
 static_assert(kNoAllocCounterBytes % alignof(dst::col::ColRec) == 0, "record alignment");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -454,8 +455,8 @@ std::mutex g_noalloc_mutex;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
 // Once per device (the device current): find the scratch array's address, read
-// the SM count and clear the grid barrier, which must start at zero (every
-// barrier leaves its count at zero).
+// the SM count and clear the per-row counters, which must start at zero (every
+// launch leaves them at zero).
 int noalloc_setup(int dev, cudaStream_t stream, NoAllocDevice* out)
 {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -565,8 +566,8 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
     {
         const size_t rec_bytes = size_t(h->col_units) * sizeof(dst::col::ColRec);
         if (cudaMalloc(&h->col_rec, rec_bytes) != cudaSuccess ||
-            cudaMalloc(&h->col_bar, sizeof(dst::col::GridBar)) != cudaSuccess ||
-            cudaMemset(h->col_bar, 0, sizeof(dst::col::GridBar)) != cudaSuccess ||
+            cudaMalloc(&h->col_bar, sizeof(dst::col::RowSync)) != cudaSuccess ||
+            cudaMemset(h->col_bar, 0, sizeof(dst::col::RowSync)) != cudaSuccess ||
             cudaMalloc(&h->stats, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
             cudaMemset(h->stats, 0, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
             cudaDeviceSynchronize() != cudaSuccess) {
@@ -645,7 +646,7 @@ int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
     if (rc != SAMPLER_OK) return rc;
     dst::col::ColParams p;
     fill_col_params(p, a, g);
-    p.bar = reinterpret_cast<dst::col::GridBar*>(d.scratch);
+    p.sync = reinterpret_cast<dst::col::RowSync*>(d.scratch);
     p.rec = reinterpret_cast<dst::col::ColRec*>(d.scratch + kNoAllocCounterBytes);
     p.stats = nullptr;
     return launch_col_kernel(fn, p, g, stream);
