@@ -616,16 +616,6 @@ __device__ __forceinline__ int settle_fast(const GTop2& t, float T)
     return settle_slow(t, T);
 }
 
-// Fast fp32 Gumbel record of a kept candidate.
-__device__ __forceinline__ GRec cand_grec(const RowInfo& ri, float x, int v)
-{
-    const uint4 blk = philox4x32_10(make_uint4(uint32_t(v) >> 2, ri.stream, ri.off_lo, ri.off_hi),
-                                    PhiloxKey{ri.key_lo, ri.key_hi});
-    const uint32_t word = lane_of(blk, uint32_t(v) & 3u);
-    const float w = noise_one_minus_u(word);
-    return GRec{x * ri.invT - fast_ln_exp1(w, __log2f(w), word), v, x, word};
-}
-
 // Finish a greedy, plain or rejected row r from its records (one warp). Loads
 // of the G <= kMaxUnits records are issued together (kLPL per lane).
 __device__ __noinline__ void finish_row(const ColParams& P, const int r, const RowInfo ri)
@@ -813,13 +803,62 @@ __device__ __noinline__ int cut_and_pick(const RowInfo ri, const unsigned long l
     }
     int token = -1;
     if (!fallback) {
-        GTop2 t;
-        t.a = grec_empty();
-        t.b = grec_empty();
-        if (iA < nkept) top2_insert(t, cand_grec(ri, xA, idxA));
-        if (iB < nkept) top2_insert(t, cand_grec(ri, xB, idxB));
-        top2_warp_reduce(t);
-        token = settle_fast(t, ri.T);
+        // exact fp32 scores (log2 units) of the lane's two candidates, their Philox
+        // blocks taken together from the row-folded generator
+        const RowPhilox ph = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, ri.off_lo, ri.off_hi);
+        const uint4 bA = philox_block(ph, uint32_t(idxA) >> 2);
+        const uint4 bB = philox_block(ph, uint32_t(idxB) >> 2);
+        const uint32_t wA = lane_of(bA, uint32_t(idxA) & 3u), wB = lane_of(bB, uint32_t(idxB) & 3u);
+        const float a2 = ri.invT * 1.4426950408889634f;
+        const float sA = iA < nkept ? fmaf(xA, a2, -log2_exp1(wA)) : -INFINITY;
+        const float sB = iB < nkept ? fmaf(xB, a2, -log2_exp1(wB)) : -INFINITY;
+        const int jA = iA < nkept ? idxA : INT_MAX, jB = iB < nkept ? idxB : INT_MAX;
+        // the warp's best two (score desc, token asc): a warp maximum, then another
+        // without the winner
+        const bool aFirst = sA > sB || (sA == sB && jA < jB);
+        float s1 = aFirst ? sA : sB, s2 = aFirst ? sB : sA;
+        int i1 = aFirst ? jA : jB, i2 = aFirst ? jB : jA;
+        float bs = s1;
+        int bi = i1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (os > bs || (os == bs && oi < bi)) {
+                bs = os;
+                bi = oi;
+            }
+        }
+        float cs = i1 == bi ? s2 : s1;  // this lane's best apart from the winner
+        int ci = i1 == bi ? i2 : i1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, cs, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, ci, off);
+            if (os > cs || (os == cs && oi < ci)) {
+                cs = os;
+                ci = oi;
+            }
+        }
+        token = bi == INT_MAX ? -1 : bi;
+        const float n1 = bs * 0.69314718055994531f, n2 = cs * 0.69314718055994531f;
+        const float tol = 1e-4f + 1e-5f * fmaxf(fabsf(n1), fabsf(n2));
+        if (bi != INT_MAX && ci != INT_MAX && !(n1 - n2 > tol)) {
+            // within fp32 reach: settle the pair in double from their logits and words
+            GTop2 t;
+            t.a = grec_empty();
+            t.b = grec_empty();
+            const unsigned ha = __ballot_sync(0xffffffffu, jA == bi || jB == bi);
+            const unsigned hb = __ballot_sync(0xffffffffu, jA == ci || jB == ci);
+            const int la = __ffs(ha) - 1, lb = __ffs(hb) - 1;
+            const float xa = __shfl_sync(0xffffffffu, jA == bi ? xA : xB, la);
+            const uint32_t wa = __shfl_sync(0xffffffffu, jA == bi ? wA : wB, la);
+            const float xb = __shfl_sync(0xffffffffu, jA == ci ? xA : xB, lb);
+            const uint32_t wb = __shfl_sync(0xffffffffu, jA == ci ? wA : wB, lb);
+            t.a = GRec{n1, bi, xa, wa};
+            t.b = GRec{n2, ci, xb, wb};
+            token = settle_fast(t, ri.T);
+        }
     }
     return token;
 }
