@@ -533,6 +533,174 @@ __device__ __noinline__ void resolve_cut(GShared& sh, const unsigned long long* 
     __syncthreads();
 }
 
+// Warp 0 of the leader: sort n <= 256 list words descending in registers and
+// shuffles (word q * 32 + lane in v[q]; no block-wide waits), written back in place.
+template <int PER>
+__device__ __forceinline__ void warp_sort_words(unsigned long long* list, int n)
+{
+    const int lane = threadIdx.x & 31;
+    constexpr int N = PER * 32;
+    unsigned long long v[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) v[q] = q * 32 + lane < n ? list[q * 32 + lane] : 0ull;
+#pragma unroll 1
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll 1
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 32) {
+                const int qs = stride / 32;
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+#pragma unroll
+                    for (int p2 = q + 1; p2 < PER; ++p2) {
+                        if ((q ^ p2) != qs) continue;
+                        const bool desc = ((q * 32 + lane) & size) == 0;
+                        const unsigned long long a = v[q], b = v[p2];
+                        const bool sw = desc ? (a < b) : (a > b);
+                        v[q] = sw ? b : a;
+                        v[p2] = sw ? a : b;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    const int i = q * 32 + lane;
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[q], stride);
+                    const bool keep_max = ((i & stride) == 0) == ((i & size) == 0);
+                    v[q] = keep_max ? (v[q] > o ? v[q] : o) : (v[q] < o ? v[q] : o);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) list[q * 32 + lane] = v[q];
+    __syncwarp();
+}
+
+__device__ __noinline__ void warp_sort_list(unsigned long long* list, int n)
+{
+    if (n <= 32) warp_sort_words<1>(list, n);
+    else if (n <= 64) warp_sort_words<2>(list, n);
+    else if (n <= 128) warp_sort_words<4>(list, n);
+    else warp_sort_words<8>(list, n);
+}
+
+// Warp 0 of the leader: the same cut as resolve_cut, for short lists, with warp
+// reductions and scans only.
+__device__ __noinline__ void resolve_cut_warp(GShared& sh, const unsigned long long* list, int total, int f)
+{
+    const int lane = threadIdx.x & 31;
+    const RowParams& rp = sh.rp[f];
+    ForkOut& fo = sh.bc.f[f];
+    const float m = sh.bc.m;
+    const uint32_t tkey = f2key(fo.tau);
+    int c = 0;
+    for (int i = lane; i < total; i += 32) c += cand_key(list[i]) >= tkey ? 1 : 0;
+    const int nf = __reduce_add_sync(0xffffffffu, c);
+    const bool dom_complete = rp.do_topk && nf >= rp.k;
+    const int dn = rp.do_topk ? min(rp.k, nf) : nf;
+    bool unresolved = dn < 1;
+    int np = dn;
+    if (rp.do_topp && !unresolved) {
+        const int per = (dn + 31) / 32;
+        const int i0 = min(dn, lane * per), i1 = min(dn, i0 + per);
+        float ls = 0.0f, lc = 0.0f;
+        for (int i = i0; i < i1; ++i) {
+            const float e = expf((key2f(cand_key(list[i])) - m) * rp.invT);
+            const float y = e - lc;
+            const float t = ls + y;
+            lc = (t - ls) - y;
+            ls = t;
+        }
+        const double loc = double(ls) - double(lc);
+        double incl = loc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const double tot = __shfl_sync(0xffffffffu, incl, 31);
+        double zdom = sh.zrow[f];
+        if (rp.do_topk) {
+            if (!dom_complete) unresolved = true;
+            zdom = tot;
+        }
+        const double pz = double(rp.p) * zdom;
+        int first = INT_MAX;
+        double sacc = incl - loc;
+        for (int i = i0; i < i1; ++i) {
+            if (i > 0 && sacc >= pz) {
+                first = i;
+                break;
+            }
+            sacc += double(expf((key2f(cand_key(list[i])) - m) * rp.invT));
+        }
+        first = __reduce_min_sync(0xffffffffu, first);
+        const bool minp_caps = rp.do_minp && fo.tau <= fo.xthr;
+        if (first != INT_MAX) np = first;
+        else if (!dom_complete && tot < pz && !minp_caps) unresolved = true;
+    } else if (rp.do_topk && !dom_complete && !(rp.do_minp && fo.tau <= fo.xthr)) {
+        unresolved = true;
+    }
+    if (unresolved) {
+        if (lane == 0) fo.kind = kKindExact;
+        __syncwarp();
+        return;
+    }
+    int nk = np;
+    if (rp.do_minp) {
+        int b = INT_MAX;
+        for (int i = lane; i < np; i += 32)
+            if (key2f(cand_key(list[i])) < fo.xthr) b = min(b, i);
+        b = __reduce_min_sync(0xffffffffu, b);
+        nk = b == INT_MAX ? np : max(b, 1);
+    }
+    if (lane == 0) {
+        const unsigned long long last = list[nk - 1];
+        fo.bkey = cand_key(last);
+        fo.bidx = cand_idx(last);
+        fo.has_bound = 1;
+        fo.kind = kKindPick;
+        fo.listed = 1;
+    }
+    __syncwarp();
+}
+
+// Warp 0 of the leader: sort a short list and cut every listed fork from it;
+// a fork whose parameters and bound match an earlier listed fork copies its cut.
+__device__ __noinline__ void warp_cut_lists(GShared& sh, unsigned long long* list, int total, int g)
+{
+    const int lane = threadIdx.x & 31;
+    warp_sort_list(list, total);
+    for (int f = 0; f < g; ++f) {
+        if (sh.bc.f[f].kind != kKindList) continue;
+        const RowParams& rp = sh.rp[f];
+        int twin = -1;
+        for (int e = 0; e < f; ++e) {
+            const RowParams& re = sh.rp[e];
+            const ForkOut& fe = sh.bc.f[e];
+            if (fe.kind == kKindPick && fe.listed && re.k == rp.k && re.p == rp.p && re.minp == rp.minp &&
+                re.invT == rp.invT && re.do_topk == rp.do_topk && re.do_topp == rp.do_topp &&
+                re.do_minp == rp.do_minp && fe.tau == sh.bc.f[f].tau && sh.zrow[e] == sh.zrow[f])
+                twin = e;
+        }
+        if (twin < 0) {
+            resolve_cut_warp(sh, list, total, f);
+            continue;
+        }
+        if (lane == 0) {
+            ForkOut& fo = sh.bc.f[f];
+            const ForkOut& fe = sh.bc.f[twin];
+            fo.kind = kKindPick;
+            fo.listed = 1;
+            fo.has_bound = fe.has_bound;
+            fo.bkey = fe.bkey;
+            fo.bidx = fe.bidx;
+        }
+        __syncwarp();
+    }
+}
+
 }  // namespace grp
 }  // namespace dst
 
@@ -1263,7 +1431,13 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
                     overflow |= total > uint32_t(P.list_cap);
                     bool need_sort = false;
                     for (int f = 0; f < g; ++f) need_sort |= sh.bc.f[f].kind == kKindList;
-                    if (!overflow && need_sort) {
+                    // short lists: warp 0 sorts and cuts alone (no block-wide waits)
+                    const bool small = !overflow && need_sort && total <= 256u;
+                    if (small) {
+                        gather_lists(list, cand, counts, C, int(total));
+                        if (wid == 0) warp_cut_lists(sh, list, int(total), g);
+                        __syncthreads();
+                    } else if (!overflow && need_sort) {
                         gather_lists(list, cand, counts, C, int(total));
                         sort_desc<unsigned long long>(list, int(total));
                     }
@@ -1272,7 +1446,7 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
                         if (tid < g && sh.bc.f[tid].kind == kKindPick && sh.bc.f[tid].listed) sh.bc.f[tid].listed = 0;
                         __syncthreads();
                     }
-                    for (int f = 0; f < g; ++f) {
+                    for (int f = 0; f < g && !small; ++f) {
                         if (sh.bc.f[f].kind != kKindList) continue;
                         if (overflow) {
                             __syncthreads();
