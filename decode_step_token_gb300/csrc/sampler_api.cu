@@ -315,8 +315,10 @@ ColGeometry col_geometry(int64_t N, int64_t V, int esize, int sms)
     g.w = int(w);
     g.gc = int((V + w - 1) / w);
     g.units = N * g.gc;
-    // enough CTAs for one unit per warp, at most one per SM (all co-resident)
-    g.grid = int(std::min<int64_t>(sms, std::max<int64_t>((g.units + dst::col::kW - 1) / dst::col::kW, 1)));
+    // enough CTAs for one unit per warp and one per row (rows finish in parallel),
+    // at most one per SM (all co-resident)
+    const int64_t want = std::max<int64_t>((g.units + dst::col::kW - 1) / dst::col::kW, std::max<int64_t>(N, 1));
+    g.grid = int(std::min<int64_t>(sms, want));
     return g;
 }
 
