@@ -726,7 +726,7 @@ __device__ __noinline__ float minp_threshold(float m, float Te, float minp)
 // lists lies below tau_inc, so L[i] is the row's i-th token when L[i] >= tau_inc.
 // Warp 0 only. Returns the token, or sets `fallback` when the list cannot
 // settle it.
-__device__ __noinline__ int cut_and_pick(const RowInfo ri, const unsigned long long* L, int n,
+__device__ __forceinline__ int cut_and_pick(const RowInfo ri, const unsigned long long* L, int n,
                                          unsigned long long tau_inc, float m, const float* hmx,
                                          const float* hzs, const float* hzc, int G, bool& fallback)
 {
