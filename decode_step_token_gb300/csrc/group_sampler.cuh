@@ -336,19 +336,6 @@ __device__ __forceinline__ double block_sum_f64(double v, GShared& sh)
     return t;
 }
 
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, GShared& sh)
-{
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    v = warp_sum_u64(v);
-    __syncthreads();
-    if (lane == 0) sh.red_q[wid] = v;
-    __syncthreads();
-    unsigned long long t = 0;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) t += sh.red_q[w];
-    return t;
-}
-
 // Inclusive prefix sum (index order) of one double per thread over the block.
 __device__ __forceinline__ double block_incl_scan_f64(double v, GShared& sh, double& total)
 {

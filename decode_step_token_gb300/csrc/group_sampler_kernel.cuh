@@ -6,8 +6,6 @@
 namespace dst {
 namespace grp {
 
-__device__ __forceinline__ int a16(int x) { return (x + 15) & ~15; }
-
 __device__ __forceinline__ float nan_f() { return __int_as_float(0x7fc00000); }
 
 // Fork classes decided from the parameters alone (every CTA decides alike).

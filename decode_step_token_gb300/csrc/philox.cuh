@@ -35,34 +35,6 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey k)
     return c;
 }
 
-// The ten round keys of a key, for loops that draw many blocks under one key.
-struct PhiloxSchedule {
-    uint32_t k0[10], k1[10];
-};
-
-__device__ __forceinline__ PhiloxSchedule philox_schedule(PhiloxKey k)
-{
-    PhiloxSchedule s;
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        s.k0[round] = k.lo + uint32_t(round) * 0x9E3779B9u;
-        s.k1[round] = k.hi + uint32_t(round) * 0xBB67AE85u;
-    }
-    return s;
-}
-
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxSchedule& s)
-{
-    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        const uint32_t hiA = __umulhi(kMulA, c.x), loA = kMulA * c.x;
-        const uint32_t hiB = __umulhi(kMulB, c.z), loB = kMulB * c.z;
-        c = make_uint4(hiB ^ c.y ^ s.k0[round], loB, hiA ^ c.w ^ s.k1[round], loA);
-    }
-    return c;
-}
-
 // The 32x32 -> 64 product of the two Philox lanes in one instruction.
 __device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo)
 {

@@ -162,19 +162,4 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
                  : "memory");
 }
 
-// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
-// arrival is counted in the barrier's initial count).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
-// Plain arrival (release semantics) on `bar`.
-__device__ __forceinline__ void mbar_arrive_release(uint64_t* bar)
-{
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
 }  // namespace dst
