@@ -170,6 +170,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest replica's time (the job ends with the last one); every rank gets
+    it. Needs an initialised process group; ends with a barrier."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_rows_per_second(world: int, n_rows: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every replica samples `n_rows` rows per step."""
+    return world * n_rows * steps / (ms / 1e3)
+
+
 def oracle_rows_per_second(batch, seconds: float, nthreads: int):
     """Time the CPU oracle on whole batches (rotating rows) for about `seconds`."""
     import oracle
@@ -283,13 +300,9 @@ def run_ours(args):
     ms = e0.elapsed_time(e1)
     clk = clocks.stop(t0, t1) if clocks else None
     if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-        dist.barrier()
+        ms = max_over_ranks(ms, dev)
     ms_step = ms / steps
-    value = world * batch.n_rows * steps / (ms / 1e3)
+    value = job_rows_per_second(world, batch.n_rows, steps, ms)
 
     exact_rows = sampler.stat(0, reset=True)
     if rank != 0:
