@@ -28,7 +28,9 @@
  * Readings where the pages are silent (each is listed in the design notes):
  *  - penalty formulas: repetition divides positive / multiplies non-positive
  *    logits of tokens seen before, then frequency subtracts f * count, then
- *    presence subtracts p once for tokens seen before;
+ *    presence subtracts p once for tokens seen before. Parity unpinned: no page
+ *    prints these formulas or a worked example, so only hand-computed cases of
+ *    this reading check them;
  *  - greedy when T < 1e-5 ([NOTE] sampling type); outputs of greedy rows use T = 1;
  *  - top-k keeps exactly k tokens in (value desc, index asc) order; -1 or k >= V
  *    keeps all;
