@@ -247,6 +247,34 @@ def test_gumbel_max_draws_the_categorical_distribution(v):
     assert tvd < 0.01
 
 
+def test_gumbel_max_over_the_kept_set_draws_the_renormalised_distribution():
+    # top-k then top-p then min-p by their textbook definitions, then the draw must
+    # follow softmax(x / T) over the kept tokens only
+    rng = np.random.default_rng(11)
+    v, T, k, p, mp = 12, 0.7, 7, 0.95, 0.15
+    x = (rng.standard_normal(v) * 1.5).astype(np.float32)
+    order = sorted(range(v), key=lambda i: (-float(x[i]), i))[:k]
+    y = x.astype(np.float64)[order] / T
+    q = scipy.special.softmax(y)
+    excl = np.concatenate([[0.0], np.cumsum(q)[:-1]])
+    kept_p = [order[i] for i in range(k) if i == 0 or excl[i] < p]
+    keep = [i for i in kept_p if x[i] / T - y.max() >= np.log(mp)]
+    # each cut removes something here: 12 -> 7 (top-k) -> 5 (top-p) -> 4 (min-p)
+    assert (len(order), len(kept_p), len(keep)) == (7, 5, 4)
+    want = scipy.special.softmax(x.astype(np.float64)[keep] / T)
+    n = 200_000
+    b = SamplerBatch("g", x[None, :], "f32", v, n, np.full(n, T, np.float32),
+                     top_k=np.full(n, k, np.int32), top_p=np.full(n, p, np.float32),
+                     min_p=np.full(n, mp, np.float32), logit_row=np.zeros(n, np.int32),
+                     global_seed=7, philox_offset=1)
+    res = oracle.sample(b, nthreads=os.cpu_count() or 1)
+    counts = np.bincount(res.tokens, minlength=v)
+    assert counts[[i for i in range(v) if i not in keep]].sum() == 0
+    got = counts[keep]
+    chi2 = ((got - n * want) ** 2 / (n * want)).sum()
+    assert scipy.stats.chi2.sf(chi2, len(keep) - 1) > 1e-4
+
+
 def test_seeded_rows_ignore_batch_position_and_forks_differ():
     rng = np.random.default_rng(3)
     x = (rng.standard_normal((1, 500)) * 2).astype(np.float32)
