@@ -198,6 +198,15 @@ def test_topk_topp_minp_kept_sets_by_brute_force(seed):
         dom = {i for i, q in zip(sorted(dom), pr) if q >= np.float32(mp) * pmax * (1 - 1e-12)}
     assert _kept_from_probs(res, 0) == dom
     assert res.tokens[0] in dom
+    # probs / logprobs: the softmax at T renormalised over the kept set, 0 and -inf
+    # elsewhere
+    kept = sorted(dom)
+    yk = x.astype(np.float64)[kept] / t
+    np.testing.assert_allclose(res.probs[0][kept], scipy.special.softmax(yk), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(res.logprobs[0][kept], scipy.special.log_softmax(yk), rtol=1e-6,
+                               atol=1e-6)
+    out = [i for i in range(v) if i not in dom]
+    assert (res.probs[0][out] == 0).all() and np.isneginf(res.logprobs[0][out]).all()
 
 
 def test_topk_ties_keep_lowest_indices():
