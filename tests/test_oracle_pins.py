@@ -318,6 +318,29 @@ def test_penalty_hand_cases():
         assert xp[1] == np.float32(7.0)
 
 
+def test_penalty_counts_follow_the_history_multiset():
+    # counts come from the whole ragged history of the row (repeats and any order),
+    # other rows' histories do not leak in, and unseen tokens are untouched
+    rng = np.random.default_rng(5)
+    v = 40
+    x = (rng.standard_normal((2, v)) * 2).astype(np.float32)
+    h0 = rng.integers(0, 10, size=25).astype(np.int32)   # row 0: ids 0..9 with repeats
+    h1 = np.array([30, 30, 31], np.int32)                  # row 1
+    offs = np.array([0, len(h0), len(h0) + len(h1)], np.int32)
+    b = _batch(x, [1.0, 1.0], presence=np.float32([0.5, 0.5]), frequency=np.float32([0.25, 0.25]),
+               repetition=np.float32([1.0, 1.0]), hist_offsets=offs,
+               hist_ids=np.concatenate([h0, h1]))
+    st, xp = oracle.penalized_logits(b, 0)
+    assert st == 0
+    c = np.bincount(h0, minlength=v)
+    # repetition 1: x - 0.25 c - 0.5 [c > 0], up to the rounding of two fp32 steps
+    want = x[0].astype(np.float64) - 0.25 * c - 0.5 * (c > 0)
+    seen = c > 0
+    np.testing.assert_allclose(xp[seen], want[seen], rtol=0, atol=4e-6)
+    np.testing.assert_array_equal(xp[~seen], x[0][~seen])
+    assert (xp[30:32] == x[0][30:32]).all()  # row 1's ids do not touch row 0
+
+
 def test_identity_penalties_change_nothing():
     rng = np.random.default_rng(5)
     x = (rng.standard_normal((1, 64)) * 3).astype(np.float32)
