@@ -152,9 +152,26 @@ class OracleResult:
     def kept(self):
         return self.diag[:, 3]
 
+    def gumbel_tie(self, tol: float = 1e-6) -> np.ndarray:
+        """Rows whose two best Gumbel scores lie within `tol` of each other: the
+        sampled token is then one of two correct answers (greedy rows never are)."""
+        return self.gumbel_gap < tol
+
+    def topp_boundary(self, tol: float = 1e-6) -> np.ndarray:
+        """Rows whose top-p cut has a prefix mass within `tol` of p."""
+        return self.topp_margin < tol
+
+    def minp_boundary(self, tol: float = 1e-6) -> np.ndarray:
+        """Rows with a kept-set token whose min-p ratio lies within `tol` of ln(min_p)."""
+        return self.minp_margin < tol
+
+    def boundary(self, tol: float = 1e-6) -> np.ndarray:
+        """Rows whose kept set sits within `tol` of a top-p or min-p cut."""
+        return self.topp_boundary(tol) | self.minp_boundary(tol)
+
     def ambiguous(self, tol: float = 1e-6) -> np.ndarray:
-        """Rows whose pick or kept set sits within `tol` of a decision boundary."""
-        return (self.gumbel_gap < tol) | (self.topp_margin < tol) | (self.minp_margin < tol)
+        """Rows that have any of the near-decisions above (for counting)."""
+        return self.gumbel_tie(tol) | self.boundary(tol)
 
 
 def _arr(a, dtype):
