@@ -11,7 +11,7 @@ import ctypes
 from typing import Optional
 
 from . import _binding as abi
-from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_ROW_KERNEL, SAMPLER_DTYPE_BF16,
+from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHORT_WAITS, SAMPLER_DTYPE_BF16,
                        SAMPLER_DTYPE_F32, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK, load_library,
                        sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
                        sampler_destroy, sampler_sample, sampler_sample_host,
@@ -47,8 +47,9 @@ class Sampler:
     """
 
     def __init__(self, max_rows: int, max_vocab: int, device: int = 0, max_history: int = 0,
-                 host_staging: bool = False, row_kernel: bool = False):
-        flags = (SAMPLER_CREATE_HOST_STAGING if host_staging else 0) | (SAMPLER_CREATE_ROW_KERNEL if row_kernel else 0)
+                 host_staging: bool = False, short_waits: bool = False):
+        flags = ((SAMPLER_CREATE_HOST_STAGING if host_staging else 0)
+                 | (SAMPLER_CREATE_SHORT_WAITS if short_waits else 0))
         cfg = sampler_config_t(device, max_rows, max_vocab, max_history, flags)
         rc, h = sampler_create(cfg)
         if rc != SAMPLER_OK:

@@ -34,6 +34,7 @@ SAMPLER_ROW_TIMEOUT = 5
 
 SAMPLER_CREATE_HOST_STAGING = 1
 SAMPLER_CREATE_ROW_KERNEL = 2
+SAMPLER_CREATE_SHORT_WAITS = 4
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
             "sampler_status_string", "sampler_abi_version", "sampler_get_stat",

@@ -1,26 +1,31 @@
-"""Build libsampler.so in-tree with nvcc for sm_103a (GB300)."""
+"""Build libsampler.so in-tree with nvcc for sm_103a (GB300).
+
+The library has three translation units (the C ABI's host code, the slice
+kernel, the fork-group kernel); they compile in parallel and link into one
+shared object.
+"""
 from __future__ import annotations
 
 import glob
 import os
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsampler.so")
+OBJ_DIR = os.path.join(PKG, "_build")
 
-NVCC_FLAGS = [
-    "-gencode", "arch=compute_103a,code=sm_103a",
-    "-lineinfo", "-O3", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
-]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = [*ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC"]
+UNITS = ("sampler_api.cu", "slice_kernel.cu", "group_kernel.cu")
 
 
 def sources() -> list:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-                  + glob.glob(os.path.join(INCLUDE, "*.h")))
+                  + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def is_stale() -> bool:
@@ -37,17 +42,30 @@ def nvcc() -> str:
     return "nvcc"
 
 
+def _compile(unit: str, verbose: bool) -> str:
+    obj = os.path.join(OBJ_DIR, unit.replace(".cu", f".{os.getpid()}.o"))
+    cmd = [nvcc(), *NVCC_FLAGS, f"-I{INCLUDE}", "-c", "-o", obj, os.path.join(CSRC, unit)]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    subprocess.run(cmd, check=True)
+    return obj
+
+
 def build_library(force: bool = False, verbose: bool = False) -> str:
     """Compile the CUDA sources into libsampler.so next to this file (if stale)."""
     if not force and not is_stale():
         return LIB
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    with ThreadPoolExecutor(len(UNITS)) as ex:
+        objs = list(ex.map(lambda u: _compile(u, verbose), UNITS))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, f"-I{INCLUDE}", "-o", tmp,
-           os.path.join(CSRC, "sampler_api.cu")]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    try:
+        subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
 
 

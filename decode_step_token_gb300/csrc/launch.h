@@ -1,0 +1,77 @@
+// launch.h -- internal interface between the host code of the C ABI
+// (sampler_api.cu) and the translation units that hold the kernels. Not part
+// of the public header.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "sampler.h"
+
+namespace dst {
+
+struct SliceHdr;   // defined with the slice kernel
+struct SliceBody;
+
+// ---------------------------------------------------------------- slice kernel
+// Small batches without history and without probs / logprobs outputs.
+struct SliceGeometry {
+    int G;           // slices per row (CTAs)
+    int W;           // elements per slice
+    int slots;       // staging slots per CTA
+    int slot_bytes;
+    size_t smem;     // dynamic shared memory per CTA
+};
+
+struct SliceWorkspace {
+    void* hdr;       // [rows][G] 16-byte slice headers
+    void* body;      // [rows][G] slice bodies
+    uint32_t* cnt;   // [rows * kSliceCntStride] arrival counters (one per 128-byte line), zero between launches
+    unsigned long long* stats;  // may be NULL
+};
+
+// Limits and record sizes of the slice kernel (checked against its own
+// definitions in slice_kernel.cu).
+constexpr int kSliceMaxRows = 256;
+constexpr int kSliceMaxSlices = 256;
+constexpr size_t kSliceHdrBytes = 16;
+constexpr size_t kSliceBodyBytes = 128;
+constexpr int kSliceCntStride = 32;  // 32-bit words between two rows' counters
+
+// True when this library's kernels load on the current device.
+bool kernels_loadable();
+
+// Geometry for n_rows x vocab of esize-byte logits on `sms` SMs; false when the
+// slice kernel does not take the shape.
+bool slice_geometry(int64_t n_rows, int64_t vocab, int esize, int sms, SliceGeometry* g);
+
+// Grant the kernel its dynamic shared memory (once per device and size).
+int slice_prepare(int dtype, size_t smem);
+
+// Enqueue one slice-kernel launch. max_polls bounds each wait on a staging copy.
+int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWorkspace& ws, uint32_t max_polls,
+                 cudaStream_t stream);
+
+// ---------------------------------------------------------------- fork-group kernel
+// Everything the slice kernel does not take.
+struct GroupGeometry {
+    int parts;       // CTAs per cluster
+    int slice;       // elements per CTA
+    int list_cap, part_cap;
+    uint32_t off_list, off_cand, off_cnt, off_stage;
+    size_t smem;
+};
+
+bool group_geometry(int64_t V, int esize, bool pen, GroupGeometry* g);
+
+// Clusters of the fork-group kernel that fit on the device at once (for the
+// given variant and shared memory); 0 on error.
+int group_occupancy(int dtype, bool pen, const GroupGeometry& g);
+
+int group_prepare(int dtype, bool pen, size_t smem);
+
+int group_launch(const sampler_args_t* a, const GroupGeometry& g, int clusters, cudaStream_t stream);
+
+}  // namespace dst

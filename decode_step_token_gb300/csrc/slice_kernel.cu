@@ -1,0 +1,132 @@
+// slice_kernel.cu -- instantiation, geometry and launch of the slice kernel
+// (design in slice_sampler.cuh).
+#include <algorithm>
+#include <cstring>
+
+#include "launch.h"
+#include "slice_kernel.cuh"
+
+namespace dst {
+
+static_assert(sizeof(slc::SliceHdr) == 16, "slice header layout");
+static_assert(sizeof(slc::SliceBody) % 16 == 0, "slice body alignment");
+static_assert(slc::kMaxRows <= slc::kT, "one thread per row classifies the batch");
+static_assert(slc::kHead < slc::kMaxSmem, "shared-memory head");
+
+static_assert(kSliceMaxRows == slc::kMaxRows && kSliceMaxSlices == slc::kMaxSlices, "slice limits");
+static_assert(kSliceHdrBytes == sizeof(slc::SliceHdr) && kSliceBodyBytes == sizeof(slc::SliceBody),
+              "slice record sizes");
+static_assert(kSliceCntStride == slc::kCntStride, "counter stride");
+
+namespace {
+
+constexpr int64_t kTinyBytes = 64 * 1024;  // a batch this small is one CTA's work
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+size_t slot_bytes_of(int64_t w, int esize) { return size_t(round_up(w * esize, 16)); }
+
+template <typename InT>
+void* kernel_of() { return reinterpret_cast<void*>(&slc::slice_kernel<InT>); }
+
+}  // namespace
+
+bool kernels_loadable()
+{
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel_of<float>()) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+bool slice_geometry(int64_t N, int64_t V, int esize, int sms, SliceGeometry* g)
+{
+    if (N < 1 || N > slc::kMaxRows || V < 1 || sms < 1) return false;
+    const int64_t epv = 16 / esize;
+    const size_t budget = slc::kMaxSmem - slc::kHead;
+    const int64_t whole = round_up(V, epv);
+    // one slice per SM, at least kMinSlice elements; a tiny batch is one slice
+    int64_t W = round_up(std::max<int64_t>(slc::kMinSlice, (V + sms - 1) / sms), epv);
+    if (N * V * esize <= kTinyBytes) W = whole;
+    W = std::min(W, whole);
+    int64_t S;
+    if (size_t(N) * slot_bytes_of(W, esize) <= budget) {
+        S = N;  // every row of this CTA in flight at once
+    } else {
+        // several waves of slots: at least 32 slots, a multiple of 32
+        const int64_t wmax = int64_t(budget / 32 / 16 * 16) / esize / epv * epv;
+        W = std::min(W, wmax);
+        S = int64_t(budget / slot_bytes_of(W, esize));
+        S = std::min<int64_t>(S, N);
+        if (S < N) S = S / 32 * 32;
+        if (S < 32) return false;
+    }
+    const int64_t G = (V + W - 1) / W;
+    if (G > slc::kMaxSlices || S > slc::kMaxSlots) return false;
+    g->G = int(G);
+    g->W = int(W);
+    g->slots = int(S);
+    g->slot_bytes = int(slot_bytes_of(W, esize));
+    g->smem = slc::kHead + size_t(S) * size_t(g->slot_bytes);
+    return g->smem <= slc::kMaxSmem;
+}
+
+int slice_prepare(int dtype, size_t smem)
+{
+    void* fn = dtype == SAMPLER_DTYPE_BF16 ? kernel_of<uint16_t>() : kernel_of<float>();
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
+int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWorkspace& ws, uint32_t max_polls,
+                 cudaStream_t stream)
+{
+    slc::SliceParams p;
+    std::memset(&p, 0, sizeof p);
+    KernelParams& k = p.k;
+    k.logits = a->logits;
+    k.vocab = a->vocab;
+    k.row_stride = a->row_stride;
+    k.n_logit_rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
+    k.logit_row = a->logit_row;
+    k.temperature = a->temperature;
+    k.top_k = a->top_k;
+    k.top_p = a->top_p;
+    k.min_p = a->min_p;
+    k.presence = a->presence_penalty;
+    k.frequency = a->frequency_penalty;
+    k.repetition = a->repetition_penalty;
+    k.seed = a->seed;
+    k.has_seed = a->has_seed;
+    k.stream_id = a->stream_id;
+    k.global_seed = a->global_seed;
+    k.philox_offset = a->philox_offset;
+    k.philox_offset_dev = a->philox_offset_dev;
+    k.out_tokens = a->out_tokens;
+    k.out_status = a->out_status;
+    p.n_rows = int(a->n_rows);
+    p.G = g.G;
+    p.W = g.W;
+    p.slots = g.slots;
+    p.slot_bytes = g.slot_bytes;
+    p.hdr = static_cast<slc::SliceHdr*>(ws.hdr);
+    p.body = static_cast<slc::SliceBody*>(ws.body);
+    p.cnt = ws.cnt;
+    p.stats = ws.stats;
+    p.max_polls = max_polls;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(unsigned(g.G));
+    cfg.blockDim = dim3(slc::kT);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = stream;
+    void* fn = a->dtype == SAMPLER_DTYPE_BF16 ? kernel_of<uint16_t>() : kernel_of<float>();
+    void* args[] = {&p};
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return SAMPLER_OK;
+}
+
+}  // namespace dst

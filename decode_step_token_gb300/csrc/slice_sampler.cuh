@@ -1,0 +1,316 @@
+// slice_sampler.cuh -- the slice kernel: small batches without history or
+// probs / logprobs outputs (sm_103a).
+//
+// Layout of the work. The vocabulary is cut into G equal slices of W elements
+// and CTA b takes slice b of EVERY row, so each SM sees the same mix of row
+// kinds: the Philox work of plain-temperature rows (the ALU-heavy part) is
+// spread evenly over the GPU, whatever the order of the rows in the batch.
+//
+//   staging   thread 0 arms one mbarrier per slot; the first warp issues one
+//             1-D bulk (TMA-engine) copy per row slice at kernel start, so the
+//             CTA's whole share of the batch is requested before anything else
+//             happens. When the rows do not fit the slots, a slot is refilled
+//             with the next row as soon as its warp is done with it.
+//   parameters read while the copies fly; every CTA classifies every row the
+//             same way (truncated / plain / greedy / bad parameter) and deals
+//             the rows of each wave to its warps in that order, so every warp
+//             gets the same mix of kinds.
+//   slice     one warp per (row, slice), from shared memory:
+//               greedy     the slice maximum and its lowest index;
+//               plain      the slice's best two Gumbel scores x/T - ln E. The
+//                          two largest logits are scored first; their smaller
+//                          score bounds the slice's second best from below, and
+//                          a per-token bound x/T - ln(1 - u) (one MUFU log2)
+//                          against it leaves almost no token to score exactly;
+//               truncated  the slice maximum, the m-th largest lane maximum
+//                          tau (so at least m tokens reach it) and every token
+//                          at or above tau (a short list; the list is complete
+//                          above tau);
+//             then a record in global memory and an atomic arrival on the
+//             row's counter (release / acquire fences around it).
+//   finish    the warp whose arrival completes a row finishes it at once from
+//             the row's G records and resets the counter; nothing ever waits on
+//             another CTA. A truncated row gathers the listed tokens above a
+//             bound B of its kept set (top-k: a lower bound of the k-th value
+//             from the slice maxima; min-p: the threshold), re-reads from
+//             global memory the slices whose lists are not complete above B,
+//             sorts the candidates and cuts top-k, top-p and min-p before the
+//             Gumbel pick. Rows the candidates cannot settle (large k, a top-p
+//             cut that reaches past the lists, too many candidates) are sampled
+//             by the whole CTA after its slices are done, streaming the row.
+//
+// Stage order and definitions follow the xbrilliance.ai note "采样参数对解码开销的影响：
+// temperature、top_p 与采样核路径", section "解码一步里采样做什么" (penalties,
+// temperature, top-k / top-p, min-p, softmax, pick), and the Gumbel-max rule of
+// the dev.to claim check "SGLang's +75% sampler speedup skips Qwen3 chat
+// requests", section "Nine lines, and exactly one call site".
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+#include "row_sampler.cuh"
+
+namespace dst {
+namespace slc {
+
+constexpr int kT = 512;                 // threads per CTA
+constexpr int kW = kT / 32;             // warps per CTA
+constexpr int kMaxRows = 256;           // rows the slice kernel takes
+constexpr int kMaxSlices = 256;         // slices per row
+constexpr int kSPL = kMaxSlices / 32;   // slices per lane when finishing
+constexpr int kMLanes = 4;              // lane maxima that bound a slice's list
+constexpr int kLCap = 12;               // list entries one record holds
+constexpr int kCandCap = 512;           // a finishing warp's candidate buffer
+constexpr int kKCap = 128;              // largest top-k the lists settle
+constexpr int kReCap = 32;              // slices a finishing warp may re-read
+constexpr int kMinSlice = 512;          // smallest slice, in elements
+constexpr int kMaxSlots = 256;          // staging slots per CTA
+constexpr uint32_t kOverflow = 0xFFFFFFFFu;
+// Each row's arrival counter sits in its own 128-byte line: G CTAs add to every
+// counter, and counters sharing a line would serialise all rows' atomics in one
+// L2 slice.
+constexpr int kCntStride = 32;
+constexpr uint32_t kDrainPolls = 1u << 26;  // polls granted to a copy after a wait gave up
+
+enum : uint8_t { kClsTrunc = 0, kClsPlain = 1, kClsGreedy = 2, kClsErr = 3 };
+
+// One (row, slice) summary in global memory.
+struct alignas(16) SliceHdr {
+    float mx;       // slice maximum (NaN ignored), -inf when nothing is finite
+    int32_t amax;   // its lowest index
+    uint32_t flags; // kFlag* bits
+    uint32_t n;     // truncated rows: listed tokens, kOverflow when they did not fit
+};
+
+struct alignas(16) SliceBody {
+    // plain rows: the slice's best two Gumbel scores as composite keys
+    // (order key of the fp32 score << 32 | ~token: larger is better, ties to the
+    // lower token), 0 when absent
+    unsigned long long ga, gb;
+    uint32_t tau;   // truncated rows: order key every listed token reaches
+    float zs;       // top-p rows without top-k: sum of exp((x - mx) / T) over the slice
+    float zc;       // its low-order part (the sum is zs + zc)
+    uint32_t pad;
+    unsigned long long list[kLCap];  // truncated rows: cand_word of each listed token
+};
+
+struct SliceParams {
+    KernelParams k;
+    int32_t n_rows;
+    int32_t G;           // slices per row = CTAs
+    int32_t W;           // elements per slice (a multiple of 16 bytes)
+    int32_t slots;       // staging slots (rows of this CTA in flight)
+    int32_t slot_bytes;  // bytes per slot (W elements, rounded up to 16)
+    SliceHdr* hdr;       // [n_rows][G]
+    SliceBody* body;     // [n_rows][G]
+    uint32_t* cnt;       // [n_rows * kCntStride] arrivals (one per line); zero between launches
+    unsigned long long* stats;  // [0]: rows finished by the exact path (may be NULL)
+    uint32_t max_polls;  // bound of each wait on a staging copy
+};
+
+struct alignas(16) RowInfo {
+    float T;       // temperature used for scores (1 for greedy rows)
+    float invT;
+    float s2;      // log2(e) / T: scores are kept in log2 units
+    float p, minp;
+    int32_t k;
+    uint32_t stream, key_lo, key_hi;
+    int32_t lrow;
+    uint8_t cls, do_topk, do_topp, do_minp;
+    uint8_t need_z, aligned, m, pad;
+};
+
+struct alignas(16) SliceShared {
+    uint64_t full[kMaxSlots];
+    RowInfo info[kMaxRows];
+    uint16_t order[kMaxRows];     // rows of each wave, truncated first, then plain, greedy
+    uint32_t wcls[kMaxRows / 32][4];
+    uint32_t off_lo, off_hi;
+    int32_t n_exact;
+    int32_t pad0;
+    int32_t exact_rows[kMaxRows];
+    float exact_m[kMaxRows];
+    int32_t exact_amax[kMaxRows];
+    uint16_t wrow[kW][kMaxRows / kW];  // rows each warp sampled in the current wave
+    uint32_t wn[kW];              // per-warp candidate count
+    uint32_t wre_n[kW];           // per-warp re-read count
+    uint16_t wre[kW][kReCap];     // per-warp slices to re-read
+    // CTA-wide scratch of the exact path
+    uint32_t hcnt[256];
+    unsigned long long hmass[256];
+    unsigned long long scan_w[kW];
+    int32_t red_i[kW];
+    GTop2 red_g[kW];
+    unsigned long long sel_prefix, sel_wabove, sel_target;
+    int32_t sel_idx;
+    int32_t pad1;
+    unsigned long long cand[kW][kCandCap];
+};
+
+constexpr size_t kHead = (sizeof(SliceShared) + 127) & ~size_t(127);
+constexpr size_t kMaxSmem = 227 * 1024;
+
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ void warp_max_idx(float& m, int& i)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+        if (om > m || (om == m && oi < i)) {
+            m = om;
+            i = oi;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
+
+// The 8 (bf16) or 4 (fp32) logits of a 16-byte vector.
+template <typename InT>
+struct Vec;
+
+template <>
+struct Vec<uint16_t> {
+    static constexpr int E = 8;
+    __device__ static __forceinline__ float get(const uint4& r, int e) { return ElemTraits<uint16_t>::get(r, e); }
+    // maximum (NaN ignored) and whether a NaN is present
+    __device__ static __forceinline__ float vmax(const uint4& r, bool& nan)
+    {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
+        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
+        const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+        const __nv_bfloat162 mn = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+        const float n0 = __low2float(mn), n1 = __high2float(mn);
+        nan = (n0 != n0) || (n1 != n1);
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+};
+
+template <>
+struct Vec<float> {
+    static constexpr int E = 4;
+    __device__ static __forceinline__ float get(const uint4& r, int e) { return ElemTraits<float>::get(r, e); }
+    __device__ static __forceinline__ float vmax(const uint4& r, bool& nan)
+    {
+        const float a = __uint_as_float(r.x), b = __uint_as_float(r.y);
+        const float c = __uint_as_float(r.z), d = __uint_as_float(r.w);
+        nan = (a != a) || (b != b) || (c != c) || (d != d);
+        return fmaxf(fmaxf(a, b), fmaxf(c, d));
+    }
+};
+
+// One row slice as a warp sees it: staged vectors [0, nb) in shared memory,
+// the rest (a ragged tail, or everything for a row that is not 16-byte aligned)
+// read from global memory, padded with -inf.
+template <typename InT>
+struct SliceView {
+    const uint4* sm;
+    const InT* g;    // first element of the slice in global memory
+    int nb;          // staged vectors
+    int nvec;        // vectors covering the slice
+    int n;           // elements in the slice
+    int c0;          // first token of the slice
+
+    __device__ __forceinline__ uint4 vec(int j) const
+    {
+        if (j < nb) return sm[j];
+        constexpr int E = Vec<InT>::E;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < E; ++q) {
+            const int i = j * E + q;
+            if (sizeof(InT) == 2) {
+                const uint32_t b = i < n ? uint32_t(reinterpret_cast<const uint16_t*>(g)[i]) : 0xFF80u;
+                if (q & 1) w[q >> 1] |= b << 16;
+                else w[q >> 1] = b;
+            } else {
+                w[q] = i < n ? reinterpret_cast<const uint32_t*>(g)[i] : 0xFF800000u;
+            }
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+__device__ __forceinline__ uint32_t flags_of(bool nan, float vmax)
+{
+    uint32_t f = 0;
+    if (nan || vmax == INFINITY) f |= kFlagNonFinite;
+    if (vmax > -INFINITY && vmax < INFINITY) f |= kFlagAnyFinite;
+    return f;
+}
+
+__device__ __forceinline__ uint32_t warp_or(uint32_t v) { return __reduce_or_sync(0xffffffffu, v); }
+
+// Exact Gumbel score in log2 units: log2(e) * (x / T - ln E).
+__device__ __forceinline__ float score2(float x, float s2, uint32_t w)
+{
+    return x * s2 - log2f(noise_exp1_f32(w));
+}
+
+__device__ __forceinline__ GRec grec_of(float x, float s2, uint32_t w, int v)
+{
+    return GRec{score2(x, s2, w), v, x, w};
+}
+
+// ---------------------------------------------------------------- composite keys
+// A Gumbel candidate as one 64-bit word: order key of its fp32 score (log2
+// units) above the complemented token, so that max() ranks by score and breaks
+// ties to the lower token; 0 is "none".
+__device__ __forceinline__ unsigned long long gkey(float s, int v) { return cand_word(f2key(s), v); }
+__device__ __forceinline__ float gkey_score(unsigned long long c) { return key2f(cand_key(c)); }
+
+struct K2 {
+    unsigned long long a, b;  // a >= b
+};
+
+__device__ __forceinline__ void k2_insert(K2& t, unsigned long long c)
+{
+    if (c > t.a) {
+        t.b = t.a;
+        t.a = c;
+    } else if (c > t.b) {
+        t.b = c;
+    }
+}
+
+// Best two of the warp (every lane gets them).
+__device__ __forceinline__ void k2_warp_reduce(K2& t)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long oa = __shfl_xor_sync(0xffffffffu, t.a, off);
+        const unsigned long long ob = __shfl_xor_sync(0xffffffffu, t.b, off);
+        const bool mine = t.a >= oa;
+        const unsigned long long lo = mine ? oa : t.a;   // the smaller of the two firsts
+        const unsigned long long sec = mine ? t.b : ob;  // the winner's second
+        t.a = mine ? t.a : oa;
+        t.b = lo > sec ? lo : sec;
+    }
+}
+
+// The two largest of a lane's 32-bit keys across the warp (0 when absent).
+__device__ __forceinline__ void warp_top2_u32(uint32_t k, uint32_t& k1, uint32_t& k2)
+{
+    const int lane = threadIdx.x & 31;
+    k1 = __reduce_max_sync(0xffffffffu, k);
+    const uint32_t holder = __ballot_sync(0xffffffffu, k == k1);
+    k2 = __reduce_max_sync(0xffffffffu, lane == __ffs(holder) - 1 ? 0u : k);
+}
+
+// Bound on the fp32 error of the difference of two scores score2() returns:
+// when two scores differ by more, their order is the order of the exact
+// (double-precision) scores.
+__device__ __forceinline__ float settle_eps(float sa, float sb)
+{
+    return 3e-5f + 1e-6f * (fabsf(sa) + fabsf(sb));
+}
+
+}  // namespace slc
+}  // namespace dst

@@ -95,7 +95,9 @@ enum {
                                        ids in one row's history */
     SAMPLER_ROW_NONFINITE = 1,      /* a NaN or +inf logit (after penalties) */
     SAMPLER_ROW_ALL_NEG_INF = 2,    /* every logit is -inf */
-    SAMPLER_ROW_TIMEOUT = 5         /* an internal wait gave up (never expected) */
+    SAMPLER_ROW_TIMEOUT = 5         /* an internal wait gave up (never expected outside
+                                       SAMPLER_CREATE_SHORT_WAITS); the call's other rows
+                                       and every later call are unaffected */
 };
 
 /* Create-time limits. */
@@ -111,10 +113,16 @@ typedef struct {
  * fp32 logits, probs, logprobs, and the per-row arrays). */
 #define SAMPLER_CREATE_HOST_STAGING 1u
 
-/* Serve the batches that the small-batch kernel does not take with the
- * cluster-per-output-row kernel instead of the fork-group kernel (same results;
- * kept to cross-check the two). */
+/* Retired: selected a cluster-per-output-row kernel that has been removed.
+ * Accepted and ignored, so that callers built against ABI 1.0 still work. */
 #define SAMPLER_CREATE_ROW_KERNEL 2u
+
+/* Test aid: every wait of the small-batch kernel on its own staging copy gives
+ * up at once, so each row it samples reports SAMPLER_ROW_TIMEOUT (token -1).
+ * The kernel still lets each copy land before it reuses or releases the
+ * buffer, so nothing faults and nothing hangs; later calls are unaffected
+ * (no state survives a call). Lets a test observe the timeout status. */
+#define SAMPLER_CREATE_SHORT_WAITS 4u
 
 /*
  * Arguments of one sampling call. For sampler_sample every pointer is a device
@@ -171,8 +179,20 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg);
  * pointers on the handle's device. Validates only host-visible scalars and
  * pointers, allocates nothing, never synchronizes and never reads device
  * memory on the host; per-row data errors go to out_status. Returns SAMPLER_OK
- * once the work is enqueued, or a negative code (nothing enqueued). The device
- * must be current on the calling thread (the call sets it). */
+ * once the work is enqueued, or a negative code (nothing enqueued). The call
+ * makes the handle's device current while it runs and restores the caller's
+ * current device before returning.
+ *
+ * Every parameter is per row, so one top-p or greedy request never moves the
+ * other rows of the batch to another path: the batch-wide flag problem of the
+ * dev.to claim check "SGLang's +75% sampler speedup skips Qwen3 chat
+ * requests", section "One request with top_p takes the whole batch off the
+ * fast path". The call can be captured in a CUDA graph (no allocation, no
+ * synchronization, no host read of device memory, and a Philox offset that may
+ * be read from device memory through philox_offset_dev), as the SGLang manual
+ * "manual-sglang-101" asks of every step of a captured decode graph in its
+ * CUDA-graphs section "The cost: one decode step is a long list of small
+ * launches". */
 int sampler_sample(sampler_t h, const sampler_args_t* args, sampler_stream_t stream);
 
 /* The same step from host memory: copies the inputs (n_logit_rows rows of
@@ -186,10 +206,12 @@ int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_
 /*
  * Allocation-free sampling step. None of the pages has a counterpart: the
  * sampler they describe always owns its buffers. This entry point takes no
- * handle and allocates nothing. Its workspace (row counters and per-(row,
- * unit) records, 4.5 MiB) is an array in the library's own device memory, one
- * copy per device. It runs the same kernel sampler_sample uses for small
- * batches and returns the same tokens.
+ * handle and allocates nothing. Its workspace (per-row arrival counters and
+ * per-(row, slice) records, 2.3 MiB) is an array in the library's own device
+ * memory, one copy per device. It runs the same kernel sampler_sample uses for
+ * small batches and returns the same tokens. Every launch leaves the counters
+ * at zero, and a row whose wait gave up (SAMPLER_ROW_TIMEOUT) leaves no state
+ * behind, so one bad call never affects a later one.
  *
  * The first call on a device does a one-time set-up on the current device:
  * it looks up that array's address, reads the SM count and clears the row
@@ -214,9 +236,10 @@ void sampler_destroy(sampler_t h);
 const char* sampler_status_string(int code);
 
 /* Diagnostic counters kept on the device (reading one synchronizes the device):
- *   SAMPLER_STAT_EXACT_ROWS  rows whose kept set reached below what the per-slice
- *                            candidates of the small-batch path cover, and which
- *                            were therefore finished by its slower exact path.
+ *   SAMPLER_STAT_EXACT_ROWS  rows of the small-batch kernel whose kept set its
+ *                            per-slice candidate lists could not settle (top-k
+ *                            above 128, a top-p cut past the lists, too many
+ *                            candidates), finished by its slower exact path.
  * Writes the count to *value and clears it when reset != 0. */
 enum { SAMPLER_STAT_EXACT_ROWS = 0 };
 int sampler_get_stat(sampler_t h, int which, uint64_t* value, int reset);

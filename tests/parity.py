@@ -8,7 +8,7 @@ Acceptance rules (each kind of near-decision excuses only what it can change):
   scores lie within TIE_TOL (a Gumbel tie), or the row's kept set sits within
   TIE_TOL of its top-p or min-p cut (a boundary row), in which case the kept set
   itself may legitimately differ and the pick with it;
-* kept sets (probs > 0, logprobs > -inf): identical, always, for rows without a
+* kept sets (logprobs > -inf; probs are 0 outside): identical, always, for rows without a
   boundary -- in particular every top-k set. On a boundary row the two sets
   must be nested and differ only in tokens that sit at the tail of the kept
   order (no kept token of either side may rank below a token they disagree on);
@@ -102,12 +102,11 @@ def compare(batch, gpu, ora, rows=None, check_probs=True) -> ParityReport:
                 if not (np.isnan(gp).all() and np.isnan(gl).all()):
                     rep.fail(f"row {r}: error row outputs are not NaN")
                 continue
-            kept_g, kept_o = gp > 0, op > 0
-            if not np.array_equal(kept_g, gl > -np.inf):
-                rep.fail(f"row {r}: gpu probs and logprobs disagree on the kept set")
-                continue
-            if not np.array_equal(ol > -np.inf, kept_o):
-                rep.fail(f"row {r}: oracle probs and logprobs disagree on the kept set")
+            # the kept set is where logprobs are finite (a kept token's probability
+            # may underflow to 0 in fp32); no token outside it has a probability
+            kept_g, kept_o = gl > -np.inf, ol > -np.inf
+            if (gp[~kept_g] != 0).any():
+                rep.fail(f"row {r}: gpu probability outside its kept set")
                 continue
             if not np.array_equal(kept_g, kept_o):
                 if bnd[j] and _tail_only(batch, int(r), kept_g, kept_o):

@@ -10,15 +10,14 @@ from parity import compare
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["group", "row"])
-def sampler(request):
-    """Both large-batch kernels: the fork-group kernel (default) and the
-    cluster-per-row kernel (SAMPLER_CREATE_ROW_KERNEL); small batches without
-    outputs take the unit-split kernel either way."""
+@pytest.fixture(scope="module")
+def sampler():
+    """One handle: small batches without outputs take the slice kernel, the rest
+    the fork-group kernel."""
     from decode_step_token_gb300 import build
     build.build_library()
     import decode_step_token_gb300 as d
-    s = d.Sampler(max_rows=2048, max_vocab=262144, host_staging=False, row_kernel=request.param == "row")
+    s = d.Sampler(max_rows=2048, max_vocab=262144, host_staging=False)
     yield s
     s.close()
 
@@ -31,43 +30,46 @@ def _check(sampler, batch, rows=None, want_probs=None, nthreads=8, **kw):
     return g, o, rep
 
 
+def _named(sampler, batch, want_probs):
+    """Every row of a named workload; no Gumbel tie and no excused difference."""
+    _, _, rep = _check(sampler, batch, want_probs=want_probs, nthreads=16)
+    print(f"{batch.name} want_probs={want_probs}: {rep}")
+    assert rep.rows == batch.n_rows
+    assert rep.gumbel_ties == 0 and rep.excused == 0, rep
+    return rep
+
+
 # ----------------------------------------------------------------------------- named workloads
 
 @pytest.mark.parametrize("want", [False, True])
 def test_tiny(sampler, want):
-    _check(sampler, workloads.tiny(), want_probs=want)
+    _named(sampler, workloads.tiny(), want)
 
 
 @pytest.mark.parametrize("want", [False, True])
 def test_mixed_full_size(sampler, want):
-    b = workloads.mixed()
-    _, _, rep = _check(sampler, b, want_probs=want)
-    assert rep.rows == 64 and rep.ambiguous == 0
+    _named(sampler, workloads.mixed(), want)
 
 
 @pytest.mark.parametrize("n", [1, 32])
-def test_latency_full_size(sampler, n):
-    b = workloads.latency(n)
-    _check(sampler, b, want_probs=True)
-    _check(sampler, b, want_probs=False)
+@pytest.mark.parametrize("want", [False, True])
+def test_latency_full_size(sampler, n, want):
+    _named(sampler, workloads.latency(n), want)
 
 
 def test_penalties_full_size(sampler):
-    b = workloads.penalties()
-    rows = np.random.default_rng(0).choice(b.n_rows, 24, replace=False)
-    _, _, rep = _check(sampler, b, rows=rows, want_probs=True)
-    assert rep.ambiguous == 0
+    _named(sampler, workloads.penalties(), True)
 
 
-def test_forks_full_size(sampler):
+@pytest.mark.parametrize("want", [False, True])
+def test_forks_full_size(sampler, want):
     b = workloads.forks()
-    rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(b.n_rows, 48, replace=False))
-    _check(sampler, b, rows=rows, want_probs=False)
-    # forks of one base row with different streams draw independently
-    g = dev.run(sampler, b, want_probs=False)
-    base = g.tokens.reshape(-1, 4)
-    assert (base[:, 0] != base[:, 1]).any()
+    _named(sampler, b, want)
+    if not want:
+        # forks of one base row with different streams draw independently
+        g = dev.run(sampler, b, want_probs=False)
+        base = g.tokens.reshape(-1, 4)
+        assert (base[:, 0] != base[:, 1]).any()
 
 
 def test_forks_with_probs_sampled_rows(sampler):
@@ -102,30 +104,33 @@ def test_random_rows(sampler, v, dtype):
         _check(sampler, b)
 
 
+@pytest.mark.parametrize("want", [False, True])
 @pytest.mark.parametrize("mix", ["topk", "topp", "minp", "plain"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_each_stage_alone(sampler, mix, dtype):
-    b = workloads.random_batch(7, 16, 50000, dtype, mix=mix, want_probs=True)
+def test_each_stage_alone(sampler, mix, dtype, want):
+    b = workloads.random_batch(7, 16, 50000, dtype, mix=mix, want_probs=want)
     _check(sampler, b)
 
 
+@pytest.mark.parametrize("want", [False, True])
 @pytest.mark.parametrize("k", [65, 100, 1000, 5000, 60000])
-def test_large_topk_radix_path(sampler, k):
-    b = workloads.random_batch(k, 8, 70000, "bf16", mix="plain", want_probs=True)
+def test_large_topk_radix_path(sampler, k, want):
+    b = workloads.random_batch(k, 8, 70000, "bf16", mix="plain", want_probs=want)
     b = b.with_(top_k=np.full(8, k, np.int32), top_p=np.float32(np.linspace(0.3, 1.0, 8)))
     _check(sampler, b)
 
 
-def test_ties_everywhere(sampler):
+@pytest.mark.parametrize("want", [False, True])
+def test_ties_everywhere(sampler, want):
     for dtype in ("f32", "bf16"):
-        b = workloads.random_batch(11, 16, 30000, dtype, ties=True, want_probs=True)
+        b = workloads.random_batch(11, 16, 30000, dtype, ties=True, want_probs=want)
         _check(sampler, b)
     # a flat top: more tied candidates than the candidate buffer holds
     x = np.zeros((4, 20000), np.float32)
     x[:, ::3] = 5.0
     b = SamplerBatch("flat", x, "f32", 20000, 4, np.float32([1.0, 0.5, 0.0, 2.0]),
                      top_k=np.int32([50, 3000, 7, 64]), top_p=np.float32([1.0, 0.2, 0.9, 0.999]),
-                     want_probs=True)
+                     want_probs=want)
     _check(sampler, b)
 
 
@@ -166,9 +171,10 @@ def test_long_history_is_rejected_per_row(sampler):
     assert list(g.status) == [4, 0]
 
 
-def test_unaligned_rows_and_strides(sampler):
+@pytest.mark.parametrize("want", [False, True])
+def test_unaligned_rows_and_strides(sampler, want):
     for dtype, off in (("bf16", 1), ("bf16", 3), ("f32", 1), ("f32", 2)):
-        b = workloads.random_batch(3, 6, 9001, dtype, stride_pad=5, want_probs=True)
+        b = workloads.random_batch(3, 6, 9001, dtype, stride_pad=5, want_probs=want)
         _check(sampler, b, logits_offset_elems=off)
 
 
@@ -201,7 +207,8 @@ def test_host_rejections(sampler):
     assert e.value.code == d._binding.SAMPLER_ERR_BAD_SHAPE
 
 
-def test_greedy_threshold_and_extreme_params(sampler):
+@pytest.mark.parametrize("want", [False, True])
+def test_greedy_threshold_and_extreme_params(sampler, want):
     V = 5000
     rng = np.random.default_rng(9)
     x = (rng.standard_normal((8, V)) * 3).astype(np.float32)
@@ -210,7 +217,7 @@ def test_greedy_threshold_and_extreme_params(sampler):
     p = np.float32([1, 1, 1, 1, 1e-7, 1, 1, 1])
     mp = np.float32([0, 0, 0, 0, 0, 0, 0, 1.0])
     b = SamplerBatch("x", x, "f32", V, 8, t, top_k=k, top_p=p, min_p=mp, global_seed=77,
-                     want_probs=True)
+                     want_probs=want)
     _check(sampler, b)
 
 
@@ -252,6 +259,34 @@ def test_plain_rows_ignore_their_neighbours_parameters(sampler):
     p2[~plain] = 0.1
     g2 = dev.run(sampler, b.with_(top_k=k2, top_p=p2))
     assert np.array_equal(g1.tokens[plain], g2.tokens[plain])
+
+
+def test_exact_path_runs_and_matches(sampler):
+    """Rows the slice kernel's candidate lists cannot settle (top-k above their
+    cap, top-p reaching past the lists, flat rows) take its exact path."""
+    sampler.stat(0, reset=True)
+    b = workloads.random_batch(91, 12, 30000, "bf16", mix="topp")
+    b = b.with_(top_k=np.int32([200, 500, -1, -1, 129, 3000, -1, -1, 1000, -1, 150, -1]),
+                top_p=np.float32([1.0, 0.9, 0.95, 0.5, 1.0, 0.99, 0.8, 0.999, 0.7, 0.3, 0.6, 0.9]))
+    _check(sampler, b, want_probs=False)
+    assert sampler.stat(0, reset=True) > 0
+
+
+def test_wait_timeout_status():
+    """A handle whose staging waits give up at once reports status 5 on every row
+    of a small batch (token -1), and the next call on an ordinary handle is
+    unaffected."""
+    import decode_step_token_gb300 as d
+    b = workloads.random_batch(92, 16, 20000, "bf16")
+    with d.Sampler(max_rows=64, max_vocab=20000, short_waits=True) as s:
+        g = dev.run(s, b, want_probs=False)
+    assert (g.status == 5).all(), g.status
+    assert (g.tokens == -1).all()
+    with d.Sampler(max_rows=64, max_vocab=20000) as s:
+        g = dev.run(s, b, want_probs=False)
+    o = oracle.sample(b, want_probs=False)
+    rep = compare(b, g, o)
+    assert rep.ok(), rep
 
 
 def test_device_philox_offset(sampler):
