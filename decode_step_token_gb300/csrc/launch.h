@@ -18,10 +18,10 @@ struct SliceBody;
 // ---------------------------------------------------------------- slice kernel
 // Small batches without history and without probs / logprobs outputs.
 struct SliceGeometry {
-    int G;           // slices per row (CTAs)
+    int G;           // slices per row
     int W;           // elements per slice
-    int slots;       // staging slots per CTA
-    int slot_bytes;
+    int units;       // rows x slices, one warp's work each
+    int ctas;        // grid
     size_t smem;     // dynamic shared memory per CTA
 };
 
@@ -37,7 +37,7 @@ struct SliceWorkspace {
 constexpr int kSliceMaxRows = 256;
 constexpr int kSliceMaxSlices = 256;
 constexpr size_t kSliceHdrBytes = 16;
-constexpr size_t kSliceBodyBytes = 128;
+constexpr size_t kSliceBodyBytes = 192;
 constexpr int kSliceCntStride = 32;  // 32-bit words between two rows' counters
 
 // True when this library's kernels load on the current device.

@@ -20,10 +20,7 @@ static_assert(kSliceCntStride == slc::kCntStride, "counter stride");
 
 namespace {
 
-constexpr int64_t kTinyBytes = 64 * 1024;  // a batch this small is one CTA's work
-
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
-size_t slot_bytes_of(int64_t w, int esize) { return size_t(round_up(w * esize, 16)); }
 
 template <typename InT>
 void* kernel_of() { return reinterpret_cast<void*>(&slc::slice_kernel<InT>); }
@@ -44,32 +41,24 @@ bool slice_geometry(int64_t N, int64_t V, int esize, int sms, SliceGeometry* g)
 {
     if (N < 1 || N > slc::kMaxRows || V < 1 || sms < 1) return false;
     const int64_t epv = 16 / esize;
-    const size_t budget = slc::kMaxSmem - slc::kHead;
-    const int64_t whole = round_up(V, epv);
-    // one slice per SM, at least kMinSlice elements; a tiny batch is one slice
-    int64_t W = round_up(std::max<int64_t>(slc::kMinSlice, (V + sms - 1) / sms), epv);
-    if (N * V * esize <= kTinyBytes) W = whole;
-    W = std::min(W, whole);
-    int64_t S;
-    if (size_t(N) * slot_bytes_of(W, esize) <= budget) {
-        S = N;  // every row of this CTA in flight at once
-    } else {
-        // several waves of slots: at least 32 slots, a multiple of 32
-        const int64_t wmax = int64_t(budget / 32 / 16 * 16) / esize / epv * epv;
-        W = std::min(W, wmax);
-        S = int64_t(budget / slot_bytes_of(W, esize));
-        S = std::min<int64_t>(S, N);
-        if (S < N) S = S / 32 * 32;
-        if (S < 32) return false;
-    }
-    const int64_t G = (V + W - 1) / W;
-    if (G > slc::kMaxSlices || S > slc::kMaxSlots) return false;
+    const int64_t wmax = int64_t(slc::kSlotBytes) / esize / epv * epv;  // one warp's slot
+    // about one unit per warp of the GPU, each between kMinUnit elements (or the
+    // whole row) and one slot
+    const int64_t gs_min = (V + wmax - 1) / wmax;
+    const int64_t gs_max = std::max<int64_t>(gs_min, (V + slc::kMinUnit - 1) / slc::kMinUnit);
+    const int64_t gs_want = (int64_t(sms) * slc::kW + N - 1) / N;
+    int64_t G = std::min(std::max(gs_want, gs_min), gs_max);
+    if (G > slc::kMaxSlices) return false;
+    const int64_t W = std::min(wmax, round_up((V + G - 1) / G, epv));
+    G = (V + W - 1) / W;
+    if (G > slc::kMaxSlices) return false;
+    const int64_t units = N * G;
     g->G = int(G);
     g->W = int(W);
-    g->slots = int(S);
-    g->slot_bytes = int(slot_bytes_of(W, esize));
-    g->smem = slc::kHead + size_t(S) * size_t(g->slot_bytes);
-    return g->smem <= slc::kMaxSmem;
+    g->units = int(units);
+    g->ctas = int(std::min<int64_t>(sms, (units + slc::kW - 1) / slc::kW));
+    g->smem = slc::kSmemBytes;
+    return true;
 }
 
 int slice_prepare(int dtype, size_t smem)
@@ -109,8 +98,7 @@ int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWor
     p.n_rows = int(a->n_rows);
     p.G = g.G;
     p.W = g.W;
-    p.slots = g.slots;
-    p.slot_bytes = g.slot_bytes;
+    p.n_units = g.units;
     p.hdr = static_cast<slc::SliceHdr*>(ws.hdr);
     p.body = static_cast<slc::SliceBody*>(ws.body);
     p.cnt = ws.cnt;
@@ -119,7 +107,7 @@ int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWor
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(unsigned(g.G));
+    cfg.gridDim = dim3(unsigned(g.ctas));
     cfg.blockDim = dim3(slc::kT);
     cfg.dynamicSmemBytes = g.smem;
     cfg.stream = stream;

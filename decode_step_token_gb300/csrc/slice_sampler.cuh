@@ -1,43 +1,44 @@
 // slice_sampler.cuh -- the slice kernel: small batches without history or
 // probs / logprobs outputs (sm_103a).
 //
-// Layout of the work. The vocabulary is cut into G equal slices of W elements
-// and CTA b takes slice b of EVERY row, so each SM sees the same mix of row
-// kinds: the Philox work of plain-temperature rows (the ALU-heavy part) is
-// spread evenly over the GPU, whatever the order of the rows in the batch.
+// Layout of the work. Each row is cut into G equal slices of W elements (at
+// most one warp's staging slot); a (row, slice) pair is a unit, and the units
+// are dealt round-robin over the CTAs first and then over the warps of each
+// CTA, so that the 16 warps of an SM hold slices of 16 different rows. On the
+// 64-row, 128000-token batch this is exactly one unit per warp of the GPU.
+// Every warp works on its own:
 //
-//   staging   thread 0 arms one mbarrier per slot; the first warp issues one
-//             1-D bulk (TMA-engine) copy per row slice at kernel start, so the
-//             CTA's whole share of the batch is requested before anything else
-//             happens. When the rows do not fit the slots, a slot is refilled
-//             with the next row as soon as its warp is done with it.
-//   parameters read while the copies fly; every CTA classifies every row the
-//             same way (truncated / plain / greedy / bad parameter) and deals
-//             the rows of each wave to its warps in that order, so every warp
-//             gets the same mix of kinds.
-//   slice     one warp per (row, slice), from shared memory:
-//               greedy     the slice maximum and its lowest index;
-//               plain      the slice's best two Gumbel scores x/T - ln E. The
-//                          two largest logits are scored first; their smaller
-//                          score bounds the slice's second best from below, and
-//                          a per-token bound x/T - ln(1 - u) (one MUFU log2)
-//                          against it leaves almost no token to score exactly;
-//               truncated  the slice maximum, the m-th largest lane maximum
-//                          tau (so at least m tokens reach it) and every token
-//                          at or above tau (a short list; the list is complete
-//                          above tau);
-//             then a record in global memory and an atomic arrival on the
-//             row's counter (release / acquire fences around it).
-//   finish    the warp whose arrival completes a row finishes it at once from
-//             the row's G records and resets the counter; nothing ever waits on
-//             another CTA. A truncated row gathers the listed tokens above a
-//             bound B of its kept set (top-k: a lower bound of the k-th value
-//             from the slice maxima; min-p: the threshold), re-reads from
-//             global memory the slices whose lists are not complete above B,
-//             sorts the candidates and cuts top-k, top-p and min-p before the
-//             Gumbel pick. Rows the candidates cannot settle (large k, a top-p
-//             cut that reaches past the lists, too many candidates) are sampled
-//             by the whole CTA after its slices are done, streaming the row.
+//   staging   lane 0 arms the warp's mbarrier and starts one 1-D bulk
+//             (TMA-engine) copy of the unit into the warp's shared-memory slot
+//             before anything else, so the whole batch is requested at once;
+//             the row's parameters are read while the copy flies.
+//   summary   the warp summarises its unit into a record in global memory:
+//               greedy     the unit maximum and its lowest index;
+//               plain      the unit's best two Gumbel scores x/T - ln E. Each
+//                          lane scores its largest logit exactly; the second
+//                          best of these 32 scores bounds the unit's second
+//                          best from below, and a per-token bound
+//                          x/T - ln(1 - u) (one MUFU log2) against it leaves
+//                          almost no token to score exactly;
+//               truncated  the unit maximum, its largest lane maxima (a sketch
+//                          of up to 8 order keys: at least that many tokens
+//                          reach each of them), tau = the smallest of them, and
+//                          every token at or above tau (a short list, complete
+//                          above tau).
+//   arrival   an acquire-release atomic add on the row's counter (one counter
+//             per 128-byte line); the warp whose arrival completes the row
+//             finishes it at once and resets the counter. Nothing ever waits
+//             on another warp.
+//   finish    greedy and plain rows reduce their G records. A truncated row
+//             takes a bound B at or below every kept token (top-k: the k-th
+//             largest sketch key over the row, a 16-bit prefix found by a
+//             two-level histogram; min-p: the threshold), gathers the listed
+//             tokens >= B, reads again from global memory the slices whose
+//             lists are not complete above B, sorts the candidates and cuts
+//             top-k, top-p and min-p before the Gumbel pick. Rows the lists
+//             cannot settle (top-k above 128, a top-p cut beyond the lists,
+//             too many candidates) are sampled by the whole CTA after its warps
+//             are done, streaming the row.
 //
 // Stage order and definitions follow the xbrilliance.ai note "采样参数对解码开销的影响：
 // temperature、top_p 与采样核路径", section "解码一步里采样做什么" (penalties,
@@ -62,49 +63,49 @@ constexpr int kW = kT / 32;             // warps per CTA
 constexpr int kMaxRows = 256;           // rows the slice kernel takes
 constexpr int kMaxSlices = 256;         // slices per row
 constexpr int kSPL = kMaxSlices / 32;   // slices per lane when finishing
-constexpr int kMLanes = 4;              // lane maxima that bound a slice's list
-constexpr int kLCap = 12;               // list entries one record holds
-constexpr int kCandCap = 512;           // a finishing warp's candidate buffer
+constexpr int kSketch = 8;              // lane maxima a truncated unit exposes
+constexpr int kLCap = 16;               // list entries one record holds
+constexpr int kCandCap = 256;           // a finishing warp's candidate buffer
 constexpr int kKCap = 128;              // largest top-k the lists settle
-constexpr int kReCap = 32;              // slices a finishing warp may re-read
-constexpr int kMinSlice = 512;          // smallest slice, in elements
-constexpr int kMaxSlots = 256;          // staging slots per CTA
+constexpr int kReCap = 16;              // slices a finishing warp may read again
+constexpr int kSlotBytes = 10240;       // a warp's staging slot
+constexpr int kMinUnit = 2048;          // smallest unit, in elements (unless the row is narrower)
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
-// Each row's arrival counter sits in its own 128-byte line: G CTAs add to every
-// counter, and counters sharing a line would serialise all rows' atomics in one
-// L2 slice.
-constexpr int kCntStride = 32;
 constexpr uint32_t kDrainPolls = 1u << 26;  // polls granted to a copy after a wait gave up
+// Each row's arrival counter sits in its own 128-byte line: G warps add to every
+// counter, and counters sharing a line would serialise their atomics in one L2
+// slice.
+constexpr int kCntStride = 32;
 
 enum : uint8_t { kClsTrunc = 0, kClsPlain = 1, kClsGreedy = 2, kClsErr = 3 };
 
 // One (row, slice) summary in global memory.
 struct alignas(16) SliceHdr {
-    float mx;       // slice maximum (NaN ignored), -inf when nothing is finite
+    float mx;       // unit maximum (NaN ignored), -inf when nothing is finite
     int32_t amax;   // its lowest index
     uint32_t flags; // kFlag* bits
     uint32_t n;     // truncated rows: listed tokens, kOverflow when they did not fit
 };
 
 struct alignas(16) SliceBody {
-    // plain rows: the slice's best two Gumbel scores as composite keys
-    // (order key of the fp32 score << 32 | ~token: larger is better, ties to the
-    // lower token), 0 when absent
+    // plain rows: the unit's best two Gumbel scores as composite keys (order key
+    // of the fp32 score << 32 | ~token: larger is better, ties to the lower
+    // token), 0 when absent
     unsigned long long ga, gb;
     uint32_t tau;   // truncated rows: order key every listed token reaches
-    float zs;       // top-p rows without top-k: sum of exp((x - mx) / T) over the slice
+    float zs;       // top-p rows without top-k: sum of exp((x - mx) / T) over the unit
     float zc;       // its low-order part (the sum is zs + zc)
-    uint32_t pad;
+    uint32_t m;     // entries of the sketch
+    uint32_t sketch[kSketch];        // truncated rows: largest lane maxima (order keys, descending)
     unsigned long long list[kLCap];  // truncated rows: cand_word of each listed token
 };
 
 struct SliceParams {
     KernelParams k;
     int32_t n_rows;
-    int32_t G;           // slices per row = CTAs
+    int32_t G;           // slices per row
     int32_t W;           // elements per slice (a multiple of 16 bytes)
-    int32_t slots;       // staging slots (rows of this CTA in flight)
-    int32_t slot_bytes;  // bytes per slot (W elements, rounded up to 16)
+    int32_t n_units;     // n_rows * G
     SliceHdr* hdr;       // [n_rows][G]
     SliceBody* body;     // [n_rows][G]
     uint32_t* cnt;       // [n_rows * kCntStride] arrivals (one per line); zero between launches
@@ -121,38 +122,39 @@ struct alignas(16) RowInfo {
     uint32_t stream, key_lo, key_hi;
     int32_t lrow;
     uint8_t cls, do_topk, do_topp, do_minp;
-    uint8_t need_z, aligned, m, pad;
+    uint8_t need_z, m, pad0, pad1;
+};
+
+struct alignas(16) WarpScratch {
+    unsigned long long cand[kCandCap];  // candidates of a row being finished
+    uint32_t hist[256];                 // bins of the k-th key search
+    uint32_t n;                         // candidates listed
+    uint32_t nre;                       // slices to read again
+    uint16_t re[kReCap];
 };
 
 struct alignas(16) SliceShared {
-    uint64_t full[kMaxSlots];
-    RowInfo info[kMaxRows];
-    uint16_t order[kMaxRows];     // rows of each wave, truncated first, then plain, greedy
-    uint32_t wcls[kMaxRows / 32][4];
-    uint32_t off_lo, off_hi;
+    uint64_t full[kW];            // one staging mbarrier per warp
+    WarpScratch ws[kW];
     int32_t n_exact;
-    int32_t pad0;
-    int32_t exact_rows[kMaxRows];
+    int32_t exact_rows[kMaxRows]; // rows left for the CTA's exact path
     float exact_m[kMaxRows];
-    int32_t exact_amax[kMaxRows];
-    uint16_t wrow[kW][kMaxRows / kW];  // rows each warp sampled in the current wave
-    uint32_t wn[kW];              // per-warp candidate count
-    uint32_t wre_n[kW];           // per-warp re-read count
-    uint16_t wre[kW][kReCap];     // per-warp slices to re-read
     // CTA-wide scratch of the exact path
     uint32_t hcnt[256];
     unsigned long long hmass[256];
     unsigned long long scan_w[kW];
     int32_t red_i[kW];
-    GTop2 red_g[kW];
+    unsigned long long red_k[2 * kW];
     unsigned long long sel_prefix, sel_wabove, sel_target;
     int32_t sel_idx;
-    int32_t pad1;
-    unsigned long long cand[kW][kCandCap];
+    int32_t pad;
 };
 
 constexpr size_t kHead = (sizeof(SliceShared) + 127) & ~size_t(127);
+constexpr size_t kSmemBytes = kHead + size_t(kW) * kSlotBytes;
 constexpr size_t kMaxSmem = 227 * 1024;
+static_assert(kSmemBytes <= kMaxSmem, "shared memory per CTA");
+static_assert(kSlotBytes >= 1024 * 8, "a free slot holds 1024 candidates");
 
 // ---------------------------------------------------------------- small helpers
 __device__ __forceinline__ void warp_max_idx(float& m, int& i)
@@ -167,8 +169,6 @@ __device__ __forceinline__ void warp_max_idx(float& m, int& i)
         }
     }
 }
-
-__device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
 
 // The 8 (bf16) or 4 (fp32) logits of a 16-byte vector.
 template <typename InT>
@@ -206,9 +206,9 @@ struct Vec<float> {
     }
 };
 
-// One row slice as a warp sees it: staged vectors [0, nb) in shared memory,
-// the rest (a ragged tail, or everything for a row that is not 16-byte aligned)
-// read from global memory, padded with -inf.
+// One unit as a warp sees it: staged vectors [0, nb) in shared memory, the rest
+// (a ragged tail, or everything for a slice that is not 16-byte aligned) read
+// from global memory, padded with -inf.
 template <typename InT>
 struct SliceView {
     const uint4* sm;
@@ -248,15 +248,11 @@ __device__ __forceinline__ uint32_t flags_of(bool nan, float vmax)
 
 __device__ __forceinline__ uint32_t warp_or(uint32_t v) { return __reduce_or_sync(0xffffffffu, v); }
 
-// Exact Gumbel score in log2 units: log2(e) * (x / T - ln E).
-__device__ __forceinline__ float score2(float x, float s2, uint32_t w)
+// Exact Gumbel score in log2 units: log2(e) * (x / T - ln E). Out of line so
+// that every caller shares one copy of the code.
+static __device__ __noinline__ float score2(float x, float s2, uint32_t w)
 {
     return x * s2 - log2f(noise_exp1_f32(w));
-}
-
-__device__ __forceinline__ GRec grec_of(float x, float s2, uint32_t w, int v)
-{
-    return GRec{score2(x, s2, w), v, x, w};
 }
 
 // ---------------------------------------------------------------- composite keys
@@ -293,15 +289,6 @@ __device__ __forceinline__ void k2_warp_reduce(K2& t)
         t.a = mine ? t.a : oa;
         t.b = lo > sec ? lo : sec;
     }
-}
-
-// The two largest of a lane's 32-bit keys across the warp (0 when absent).
-__device__ __forceinline__ void warp_top2_u32(uint32_t k, uint32_t& k1, uint32_t& k2)
-{
-    const int lane = threadIdx.x & 31;
-    k1 = __reduce_max_sync(0xffffffffu, k);
-    const uint32_t holder = __ballot_sync(0xffffffffu, k == k1);
-    k2 = __reduce_max_sync(0xffffffffu, lane == __ffs(holder) - 1 ? 0u : k);
 }
 
 // Bound on the fp32 error of the difference of two scores score2() returns:
