@@ -6,12 +6,17 @@ temperature, top-k/top-p, min-p, pick, optional probs/logprobs). Default
 workload: N=64 rows, V=128000 bf16 logits ~ 2*N(0,1) with one +12 spike per
 row; 32 rows T=0.8, 16 rows top_p=0.9 + top_k=50, 16 greedy; token ids only.
 
-Prints one JSON line (rank 0). Our arm: steps replayed from a CUDA graph over
-rotating input copies larger than L2, timed with CUDA events on the launch
-stream; `e2e` through the host-buffer C entry point; `roofline` for the row
-kernel; `cpu_baseline` = the CPU oracle on a bounded sample. `--impl
-reference` times the CPU oracle itself (the only reference this sampler has).
-Several GPUs run independent replicas (rows are independent: no collective).
+Prints one JSON line (rank 0). Our arm: exactly --steps steps, replayed from
+CUDA graphs over rotating input copies larger than L2, one CUDA-event pair per
+replay on the launching stream; the per-step distribution (median, IQR) comes
+from those replays, and from a sustained run of at least half a second when
+the requested steps take less. `e2e` goes through the host-buffer C entry
+point; `roofline` is for the sampling kernel; `cpu_baseline` = the CPU oracle
+on a bounded sample at one thread and at every core; `ablation` times the
+per-family workloads (plain -> +top-k/top-p -> +min-p -> +penalties).
+`--impl reference` times the CPU oracle itself (the only reference this
+sampler has), one row per step. Several GPUs run independent replicas (rows
+are independent: no collective).
 """
 from __future__ import annotations
 
@@ -22,7 +27,6 @@ import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import threading
 import time
 
@@ -39,12 +43,13 @@ UNIT = "rows/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_DIR = os.path.join(ROOT, "decode_step_token_gb300", "csrc")
+SUSTAINED_S = 0.5
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in sorted(os.listdir(KERNEL_DIR)):
-        if not f.endswith((".cu", ".cuh")):
+        if not f.endswith((".cu", ".cuh", ".h")):
             continue
         with open(os.path.join(KERNEL_DIR, f), "rb") as fh:
             h.update(fh.read())
@@ -78,7 +83,7 @@ def measured_peaks():
 
 
 def traffic_record(workload: str):
-    """dram bytes per launch of the dominant kernel, from the committed ncu summaries
+    """dram bytes per launch of the sampling kernel, from the committed ncu summaries
     (profiles/*.md lines `kernel_hash: ...`, `workload: ...` and
     `dram_bytes_per_launch: ...`), if one was taken on this workload with the
     kernels as they are now."""
@@ -107,8 +112,46 @@ def traffic_record(workload: str):
     return None
 
 
+def cpu_info():
+    """CPU model and logical core count (lscpu, else /proc/cpuinfo)."""
+    model, cores = None, os.cpu_count() or 1
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and not model:
+                model = v.strip()
+            if k.strip() == "CPU(s)":
+                try:
+                    cores = int(v.strip())
+                except ValueError:
+                    pass
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.partition(":")[2].strip()
+                        break
+        except OSError:
+            pass
+    return {"model": model or "unknown", "logical_cpus": cores}
+
+
+def stats_us(per_step_us):
+    """median / IQR / p10 / p90 of per-step microseconds."""
+    a = np.asarray(per_step_us, dtype=np.float64)
+    if a.size == 0:
+        return None
+    q = np.percentile(a, [10, 25, 50, 75, 90])
+    return {"median_us": float(q[2]), "iqr_us": [float(q[1]), float(q[3])], "p10_us": float(q[0]),
+            "p90_us": float(q[4]), "mean_us": float(a.mean()), "samples": int(a.size)}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / throttle samples while a timed region runs."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -133,16 +176,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self, t0, t1):
-        if not self.proc:
-            return None
-        time.sleep(0.05)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=2)
-        except Exception:
-            self.proc.kill()
-        rows = [l for (t, l) in self.lines if t0 - 0.05 <= t <= t1 + 0.05] or [l for (_, l) in self.lines]
+    def window(self, t0, t1):
+        """Summary of the samples taken between t0 and t1 (perf_counter), or None."""
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1]
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for l in rows:
@@ -161,6 +197,16 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+    def stop(self):
+        if not self.proc:
+            return
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
 
 
 def dist_setup():
@@ -188,7 +234,7 @@ def job_rows_per_second(world: int, n_rows: int, steps: int, ms: float) -> float
 
 
 def oracle_rows_per_second(batch, seconds: float, nthreads: int):
-    """Time the CPU oracle on whole batches (rotating rows) for about `seconds`."""
+    """Time the CPU oracle on whole chunks of rows (rotating) for about `seconds`."""
     import oracle
 
     n = batch.n_rows
@@ -207,7 +253,8 @@ def oracle_rows_per_second(batch, seconds: float, nthreads: int):
 
 
 def run_reference(args):
-    """The CPU oracle as it stands, one row of the batch per step (rotating), one thread."""
+    """The CPU oracle as it stands, one thread; a step is one row of the batch
+    (rotating), so that the whole run stays short."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
@@ -223,18 +270,124 @@ def run_reference(args):
         oracle.sample(batch, rows=[s % n], want_probs=batch.want_probs, nthreads=1)
     el = time.perf_counter() - t0
     value = args.steps / el
+    cpu = cpu_info()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * n / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": describe(batch), "n_rows": n,
-                                        "vocab": batch.vocab},
+        "data": "synthetic",
+        "config": {"workload": describe(batch), "n_rows": n, "vocab": batch.vocab,
+                   "step": f"one row of the {n}-row batch (rotating); rows/s = steps / time"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"one row of the {n}-row batch per step, rotating; "
-                                   f"{args.steps} rows in {el:.1f} s"},
+                         "cpu_model": cpu["model"],
+                         "sample": f"{args.steps} rows of the {n}-row batch, one per step, "
+                                   f"rotating; {el:.2f} s at one thread"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+class Replayer:
+    """CUDA graphs of sampling calls over rotating input copies: `full` holds one
+    call per copy; `part(r)` the first r copies (for a step count that is not a
+    multiple of the copies). Each replay is bracketed by its own event pair."""
+
+    def __init__(self, torch, sampler, arg_blocks, stream):
+        self.torch = torch
+        self.sampler = sampler
+        self.args = arg_blocks
+        self.stream = stream
+        self.R = len(arg_blocks)
+        self.graphs = {}
+
+    def graph(self, r):
+        if r not in self.graphs:
+            torch = self.torch
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(r):
+                        self.sampler.sample_args(self.args[i], torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            self.graphs[r] = g
+        return self.graphs[r]
+
+    def run(self, steps):
+        """Replay exactly `steps` calls; returns (total ms, [(calls, ms) per replay])."""
+        torch = self.torch
+        plan = [self.R] * (steps // self.R) + ([steps % self.R] if steps % self.R else [])
+        for r in set(plan):
+            self.graph(r)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(plan) + 1)]
+        with torch.cuda.stream(self.stream):
+            ev[0].record(self.stream)
+            for i, r in enumerate(plan):
+                self.graphs[r].replay()
+                ev[i + 1].record(self.stream)
+        torch.cuda.synchronize()
+        per = [(r, ev[i].elapsed_time(ev[i + 1])) for i, r in enumerate(plan)]
+        return ev[0].elapsed_time(ev[-1]), per
+
+
+def per_step_us(per):
+    return [1e3 * ms / r for (r, ms) in per]
+
+
+def prepare(torch, pkg, wdev, batch, dev, local, no_rotate=False):
+    in_bytes = batch.n_logit_rows * batch.row_stride * batch.elem_bytes
+    copies = 1 if no_rotate else min(64, max(2, int(np.ceil(3 * L2_BYTES / max(1, in_bytes)))))
+    hist = int(batch.hist_ids.size) if batch.hist_ids is not None else 0
+    sampler = pkg.Sampler(max_rows=batch.n_rows, max_vocab=batch.vocab, device=local, max_history=hist)
+    d = wdev.to_device(batch, dev, batch.want_probs, copies=copies)
+    arg_blocks = [wdev.sample_args(sampler, batch, d, copy_index=i) for i in range(copies)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(copies):  # the first calls, outside capture, set kernel attributes
+            sampler.sample_args(arg_blocks[i], stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+    return sampler, d, Replayer(torch, sampler, arg_blocks, stream), copies, in_bytes
+
+
+def sustained(rep, seconds):
+    """Whole replays for at least `seconds`; per-step microseconds of each replay."""
+    out, t_end = [], time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        _, per = rep.run(rep.R * max(1, int(np.ceil(2000 / rep.R))))
+        out.extend(per_step_us(per))
+    return out
+
+
+def host_call_us(sampler, arg_blocks, stream, n=200):
+    """CPU time of one sampling call through the binding (enqueue only, no sync)."""
+    import torch
+
+    ts = []
+    for i in range(n):
+        t0 = time.perf_counter()
+        sampler.sample_args(arg_blocks[i % len(arg_blocks)], stream.cuda_stream)
+        ts.append(1e6 * (time.perf_counter() - t0))
+        if i % 32 == 31:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    return stats_us(ts)
+
+
+def run_ablation(torch, pkg, wdev, dev, local, seconds):
+    """Median step time of each per-family workload (plain -> +top-k/top-p ->
+    +min-p -> +penalties) at N=64, V=128000 bf16."""
+    res = {}
+    for stage in workloads.ABLATION_STAGES:
+        b = workloads.ablation(stage)
+        s, d, rep, copies, _ = prepare(torch, pkg, wdev, b, dev, local)
+        rep.run(copies * 2)
+        st = stats_us(sustained(rep, seconds))
+        st["algorithmic_bytes"] = algorithmic_bytes(b, b.want_probs)
+        st["exact_path_rows"] = s.stat(0, reset=True)
+        res[stage] = st
+        s.close()
+        del d, rep
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args):
@@ -253,96 +406,96 @@ def run_ours(args):
 
     libbuild.build_library()
     batch = workloads.make(args.workload)
-    want = batch.want_probs
-    step_bytes = algorithmic_bytes(batch, want)
-    in_bytes = batch.n_logit_rows * batch.row_stride * batch.elem_bytes
-    copies = max(2, int(np.ceil(3 * L2_BYTES / max(1, in_bytes)))) if not args.no_rotate else 1
-    copies = min(copies, 64)
-    sampler = pkg.Sampler(max_rows=batch.n_rows, max_vocab=batch.vocab, device=local)
-    d = wdev.to_device(batch, dev, want, copies=copies)
-    arg_blocks = [wdev.sample_args(sampler, batch, d, copy_index=i) for i in range(copies)]
-
-    stream = torch.cuda.Stream(device=dev)
+    step_bytes = algorithmic_bytes(batch, batch.want_probs)
+    sampler, d, rep, copies, in_bytes = prepare(torch, pkg, wdev, batch, dev, local, args.no_rotate)
     sampler.stat(0, reset=True)
-    with torch.cuda.stream(stream):
-        for i in range(copies):  # first launches outside capture set kernel attributes
-            sampler.sample_args(arg_blocks[i], stream.cuda_stream)
-        torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(copies):
-                sampler.sample_args(arg_blocks[i], torch.cuda.current_stream().cuda_stream)
-        torch.cuda.synchronize(dev)
 
-    reps_w = max(1, int(np.ceil(args.warmup / copies)))
-    reps = max(1, int(np.ceil(args.steps / copies)))
-    steps = reps * copies
-    with torch.cuda.stream(stream):
-        for _ in range(reps_w):
-            graph.replay()
-    torch.cuda.synchronize(dev)
+    # warm-up: exactly --warmup calls (at least 3), untimed
+    rep.run(max(3, args.warmup))
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     clocks = ClockSampler(local) if not args.no_clocks else None
     time.sleep(0.1 if clocks else 0)
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, per = rep.run(args.steps)
     t1 = time.perf_counter()
-    ms = e0.elapsed_time(e1)
-    clk = clocks.stop(t0, t1) if clocks else None
+    clk = clocks.window(t0, t1) if clocks else None
     if world > 1:
         ms = max_over_ranks(ms, dev)
-    ms_step = ms / steps
-    value = job_rows_per_second(world, batch.n_rows, steps, ms)
-
+    ms_step = ms / args.steps
+    value = job_rows_per_second(world, batch.n_rows, args.steps, ms)
     exact_rows = sampler.stat(0, reset=True)
+
+    # the per-step distribution: the timed replays themselves when they last long
+    # enough, else a sustained run of whole replays (clocks sampled there too)
+    dist_src = "the timed region's replays"
+    samples = per_step_us(per)
+    sus_clk = None
+    if ms / 1e3 < SUSTAINED_S or len(samples) < 20:
+        s0 = time.perf_counter()
+        samples = sustained(rep, SUSTAINED_S)
+        s1 = time.perf_counter()
+        sus_clk = clocks.window(s0, s1) if clocks else None
+        dist_src = f"a sustained run of whole {copies}-call replays ({s1 - s0:.2f} s)"
+    if clocks:
+        clocks.stop()
+    if clk is None or clk.get("samples", 0) < 3:
+        clk = dict(sus_clk or clk or {}, window="sustained run (the timed region was too short to sample)") \
+            if (sus_clk or clk) else None
+    timing = stats_us(samples)
+    timing["source"] = dist_src
+    timing["timed_region_s"] = ms / 1e3
+
     if rank != 0:
         return
     tokens = d["out_tokens"].cpu().numpy()
+    host = host_call_us(sampler, rep.args, rep.stream)
 
-    # e2e through the host-buffer entry point
     e2e = run_e2e(pkg, batch, local, args.e2e_steps) if not args.no_e2e else None
 
     peak, peak_kind = measured_peaks()
-    launch_s = ms_step / 1e3
-    achieved = step_bytes / launch_s / 1e9
+    achieved = step_bytes / (ms_step / 1e3) / 1e9
     tr = traffic_record(batch.name)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": tr["dram_bytes_per_launch"] if tr else None,
-            "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth), kernel timed inside a graph "
-                           f"of back-to-back launches",
-            "algorithmic_bytes_per_launch": step_bytes}
+            "traffic_source": (f"ncu capture summarised in profiles/{tr['source']} (same kernel "
+                               f"sources), not measured in this run") if tr else None,
+            "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth), of {peak_kind}",
+            "algorithmic_bytes_per_launch": step_bytes,
+            "launch_time": "mean of the timed region (CUDA events, graph replays)"}
     cpu = None
     if not args.no_cpu:
-        cores = os.cpu_count() or 1
+        info = cpu_info()
+        cores = info["logical_cpus"]
         rps, nrows, el = oracle_rows_per_second(batch, args.cpu_seconds, cores)
-        cpu = {"value": rps, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{nrows} rows of the same batch ({el:.1f} s, {cores} threads)"}
+        rps1, nrows1, el1 = oracle_rows_per_second(batch, args.cpu_seconds / 2, 1)
+        cpu = {"value": rps, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": info["model"],
+               "sample": f"{nrows} rows of the same batch ({el:.1f} s, {cores} threads)",
+               "one_thread": {"value": rps1, "unit": UNIT, "sample": f"{nrows1} rows ({el1:.1f} s)"}}
+    abl = None
+    if not args.no_ablation and args.workload == "mixed":
+        abl = run_ablation(torch, pkg, wdev, dev, local, args.ablation_seconds)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-        "warmup": reps_w * copies, "ms_per_step": ms_step, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": describe(batch), "n_rows": batch.n_rows, "vocab": batch.vocab,
-                   "logits_dtype": batch.dtype, "l2": f"rotating {copies} input copies "
-                   f"({copies * in_bytes / 1e6:.0f} MB > L2)", "replicas": world},
+                   "logits_dtype": batch.dtype, "compute": "fp32 (exact ties settled in fp64)",
+                   "l2": f"rotating {copies} input copies ({copies * in_bytes / 1e6:.0f} MB > L2)",
+                   "replicas": world},
         "us_per_step": ms_step * 1e3,
+        "timing": timing,
+        "host_call_us": host,
         "hbm_gbs": achieved,
-        "tokens_per_s": value,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": steps,
-        "exact_path_rows_per_step": exact_rows / (steps + (reps_w + 1) * copies),
+        "gpu_launches": args.steps,
+        "exact_path_rows_per_step": exact_rows / args.steps,
         "clocks": clk,
+        "ablation": abl,
         "kernel_hash": kernel_hash(),
         "first_tokens": tokens[:8].tolist(),
     }
@@ -384,15 +537,18 @@ def run_e2e(pkg, batch, device, steps):
     stream = torch.cuda.Stream(device=device)
     for _ in range(3):
         s.sample_host_args(args, stream.cuda_stream)
+    ts = []
     t0 = time.perf_counter()
     for _ in range(steps):
+        a = time.perf_counter()
         s.sample_host_args(args, stream.cuda_stream)
+        ts.append(1e6 * (time.perf_counter() - a))
     el = time.perf_counter() - t0
     h2d = (batch.n_logit_rows * V * batch.elem_bytes + batch.param_bytes() + batch.history_bytes())
     d2h = N * 8 + (8 * N * V if batch.want_probs else 0)
     s.close()
     return {"value": N * steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+            "d2h_bytes_per_step": d2h, "steps": steps, "per_call": stats_us(ts)}
 
 
 def main():
@@ -404,11 +560,15 @@ def main():
     ap.add_argument("--workload", default="mixed", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ablation-seconds", type=float, default=0.3)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
     args = ap.parse_args()
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -35,7 +35,7 @@ struct SliceWorkspace {
 // Limits and record sizes of the slice kernel (checked against its own
 // definitions in slice_kernel.cu).
 constexpr int kSliceMaxRows = 256;
-constexpr int kSliceMaxSlices = 256;
+constexpr int kSliceMaxSlices = 128;
 constexpr size_t kSliceHdrBytes = 16;
 constexpr size_t kSliceBodyBytes = 192;
 constexpr int kSliceCntStride = 32;  // 32-bit words between two rows' counters

@@ -8,6 +8,14 @@
 
 #include "slice_sampler.cuh"
 
+// Timeline hooks: a profiling build defines them to record a timestamp per warp
+// and event; they compile to nothing otherwise.
+#ifndef SLC_MARK
+#define SLC_MARK(i)
+#define SLC_TAG(v)
+#define SLC_UCLS(v)
+#endif
+
 namespace dst {
 namespace slc {
 
@@ -114,27 +122,56 @@ __device__ __forceinline__ int vec_find(const uint4& v, float m)
     return pos;
 }
 
-// Lane maximum (NaN ignored), its lowest token, and the flags of the part of
-// the unit a lane reads.
+// Lane maximum and the flags of the part of the unit a lane reads: one packed,
+// NaN-propagating maximum per vector. A lane that met a NaN reports -inf (its
+// flags mark the row).
 template <typename InT>
-__device__ __forceinline__ void lane_max(const SliceView<InT>& sv, float& m, int& mi, uint32_t& f)
+__device__ __forceinline__ float lane_max_val(const SliceView<InT>& sv, uint32_t& f)
+{
+    const int lane = threadIdx.x & 31;
+    typename Vec<InT>::Acc a = Vec<InT>::acc_init();
+#pragma unroll 2
+    for (int j = lane; j < sv.nvec; j += 32) Vec<InT>::acc_add(a, sv.vec(j));
+    const float m = Vec<InT>::acc_max(a);
+    const bool nan = m != m;
+    f = flags_of(nan, m);
+    return nan ? -INFINITY : m;
+}
+
+// Lowest token of the lane's part of the unit equal to m (a value the lane holds).
+template <typename InT>
+__device__ __forceinline__ int lane_find(const SliceView<InT>& sv, float m)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
-    m = -INFINITY;
-    mi = INT_MAX;
-    f = 0;
 #pragma unroll 1
     for (int j = lane; j < sv.nvec; j += 32) {
         const uint4 v = sv.vec(j);
-        bool nan;
-        const float vm = Vec<InT>::vmax(v, nan);
-        f |= flags_of(nan, vm);
-        if (vm > m) {
-            m = vm;
-            mi = sv.c0 + j * E + vec_find<InT>(v, vm);
-        }
+        if (Vec<InT>::has(v, m)) return sv.c0 + j * E + vec_find<InT>(v, m);
     }
+    return INT_MAX;
+}
+
+// Lane maximum, its lowest token (INT_MAX when nothing is finite) and flags.
+template <typename InT>
+__device__ __forceinline__ void lane_max(const SliceView<InT>& sv, float& m, int& mi, uint32_t& f)
+{
+    m = lane_max_val<InT>(sv, f);
+    mi = m > -INFINITY ? lane_find<InT>(sv, m) : INT_MAX;
+}
+
+// Unit maximum and its lowest token (only lanes holding the maximum search);
+// lm gets the lane maximum.
+template <typename InT>
+__device__ __forceinline__ void unit_max(const SliceView<InT>& sv, float& mx, int& amax, uint32_t& flags, float& lm)
+{
+    uint32_t f;
+    lm = lane_max_val<InT>(sv, f);
+    flags = warp_or(f);
+    mx = key2f(__reduce_max_sync(0xffffffffu, f2key(lm)));
+    int li = INT_MAX;
+    if (mx > -INFINITY && lm == mx) li = lane_find<InT>(sv, lm);
+    amax = __reduce_min_sync(0xffffffffu, li);
 }
 
 // ---------------------------------------------------------------- plain unit
@@ -176,9 +213,34 @@ __device__ __forceinline__ void vec_words(const RowPhilox& rp, int t0, uint4& b0
     }
 }
 
+// Cheap test against the threshold thr (log2 units) of the bound
+// x s2 - log2(1 - u): lets through every token the bound keeps. With
+// L = a 2^-23 <= 1 - u (a = the word's top 23 bits complemented) and the bit
+// pattern of L read as a number (at most log2 L, plus 127, in 2^-23 units), the
+// test is bits(L) <= (x s2 - thr + 127) 2^23, evaluated in 2^-16 units on
+// floats. Negative result = let through.
+struct CheapBound {
+    float A, K;
+    __device__ __forceinline__ CheapBound(float s2, float thr)
+    {
+        A = s2 * 65536.0f;
+        // K = 2^23 + (127 - thr + eps) 2^16 + 4, rounded up; eps covers the fp32
+        // bound's own rounding
+        const double eps = 2e-3 + 1e-6 * fabs(double(thr));
+        K = __double2float_ru(8388608.0 + (127.0 - double(thr) + eps) * 65536.0 + 4.0);
+    }
+    __device__ __forceinline__ float d(float x, uint32_t w) const
+    {
+        const float g = __uint_as_float(0x3F800000u + (w >> 9));  // 1 + (w >> 9) 2^-23
+        const float L = 1.99999988079071044921875f - g;            // (2 - 2^-23) - g = a 2^-23, exact
+        const float F = __uint_as_float(0x4B000000u + (__float_as_uint(L) >> 7));
+        return F - fmaf(x, A, K);
+    }
+};
+
 template <typename InT>
 __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowInfo& ri, uint32_t off_lo,
-                                           uint32_t off_hi, K2& out, uint32_t& flags)
+                                           uint32_t off_hi, uint16_t* q, uint4* qw, K2& out, uint32_t& flags)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -188,6 +250,7 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
     int li;
     uint32_t f;
     lane_max<InT>(sv, lm, li, f);
+    SLC_MARK(4);
     flags = warp_or(f);
     const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
     const float s2 = ri.s2;
@@ -206,32 +269,65 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
         thr = key2f(k2);
         thr -= 1e-4f + 4e-6f * fabsf(thr);
     }
-    // every other token whose bound x/T - ln(1 - u) reaches thr (E >= 1 - u, so
-    // the bound is at least the score; log2 units throughout)
+    // pass 1: the cheap test over every token; vectors with a token through are
+    // queued (warp-private, in order; the first 32 with their Philox words), so
+    // that the exact scoring below runs with all lanes busy
+    const CheapBound cb(s2, thr);
+    int nq = 0;
+    SLC_MARK(20);
 #pragma unroll 1
-    for (int j = lane; j < sv.nvec; j += 32) {
-        const uint4 v = sv.vec(j);
-        const int t0 = sv.c0 + j * E;
+    for (int j0 = 0; j0 < sv.nvec; j0 += 32) {
+        const int j = j0 + lane;
+        uint32_t neg = 0;
         uint4 b0, b1;
-        vec_words<InT>(rp, t0, b0, b1);
-        uint32_t hit = 0;
+        if (j < sv.nvec) {
+            const uint4 v = sv.vec(j);
+            vec_words<InT>(rp, sv.c0 + j * E, b0, b1);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float x = Vec<InT>::get(v, e);
-            const uint32_t we = lane_of(e < 4 ? b0 : b1, uint32_t(e) & 3u);
-            const float bound = fmaf(x, s2, -__log2f(noise_one_minus_u(we)));
-            hit |= (bound >= thr ? 1u : 0u) << e;
+            for (int e = 0; e < E; ++e)
+                neg |= __float_as_uint(cb.d(Vec<InT>::get(v, e), lane_of(e < 4 ? b0 : b1, uint32_t(e) & 3u)));
         }
+        const uint32_t bal = __ballot_sync(0xffffffffu, (neg >> 31) != 0u);
+        if (neg >> 31) {
+            const int at = nq + __popc(bal & ((1u << lane) - 1u));
+            q[at] = uint16_t(j);
+            if (at < 32) {
+                qw[2 * at] = b0;
+                qw[2 * at + 1] = b1;
+            }
+        }
+        nq += __popc(bal);
+    }
+    __syncwarp();
+    SLC_MARK(21);
+    // pass 2: exact scores of the queued vectors' tokens that pass the test; a
+    // vector may go to another lane than the one that read it, whose largest
+    // logit (already scored) is skipped
 #pragma unroll 1
-        for (; hit; hit &= hit - 1) {
-            const int e = __ffs(hit) - 1;
-            const int idx = t0 + e;
-            const float x = Vec<InT>::get(v, e);
-            if (idx == li || !(x > -INFINITY)) continue;
-            const uint32_t we = lane_of(e < 4 ? b0 : b1, uint32_t(e) & 3u);
-            k2_insert(t, gkey(score2(x, s2, we), idx));
+    for (int i0 = 0; i0 < nq; i0 += 32) {
+        const int i = i0 + lane;
+        const int j = i < nq ? int(q[i]) : 0;
+        const int oli = __shfl_sync(0xffffffffu, li, j & 31);
+        if (i < nq) {
+            const uint4 v = sv.vec(j);
+            const int t0 = sv.c0 + j * E;
+            uint4 b0, b1;
+            if (i < 32) {
+                b0 = qw[2 * i];
+                b1 = qw[2 * i + 1];
+            } else {
+                vec_words<InT>(rp, t0, b0, b1);
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float x = Vec<InT>::get(v, e);
+                const uint32_t we = lane_of(e < 4 ? b0 : b1, uint32_t(e) & 3u);
+                if (t0 + e == oli || !(x > -INFINITY) || !(cb.d(x, we) < 0.0f)) continue;
+                k2_insert(t, gkey(score2(x, s2, we), t0 + e));
+            }
         }
     }
+    __syncwarp();
     k2_warp_reduce(t);
     out = t;
 }
@@ -243,14 +339,11 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
-    float lm;
-    int li;
-    uint32_t f;
-    lane_max<InT>(sv, lm, li, f);
-    const uint32_t flags = warp_or(f);
-    float mx = lm;
-    int amax = li;
-    warp_max_idx(mx, amax);
+    float lm, mx;
+    int amax;
+    uint32_t flags;
+    unit_max<InT>(sv, mx, amax, flags, lm);
+    SLC_MARK(4);
     // the sketch: the m largest lane maxima (order keys, descending); tau is the
     // smallest of them, so at least m tokens reach tau
     const uint32_t lkey = lm > -INFINITY ? f2key(lm) : 0u;
@@ -266,20 +359,18 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
         if (lane == __ffs(holder) - 1) left = 0;
     }
     tau = max(tau, 1u);  // -inf (key 0 here) is never listed
-    // list every finite token whose key reaches tau: only lanes whose maximum
-    // reaches it hold any
+    SLC_MARK(17);
+    // list every finite token whose key reaches tau (x >= t as floats, -0 and
+    // +0 alike, as the keys): only lanes whose maximum reaches it hold any
+    const float t = key2f(tau);
+    const typename Vec<InT>::Thr t2 = Vec<InT>::thr(t);
     uint32_t mine = 0;
     if (lkey >= tau) {
-#pragma unroll 1
-        for (int j = lane; j < sv.nvec; j += 32) {
-            const uint4 v = sv.vec(j);
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float x = Vec<InT>::get(v, e);
-                mine += (x > -INFINITY && f2key(x) >= tau) ? 1u : 0u;
-            }
-        }
+#pragma unroll 2
+        for (int j = lane; j < sv.nvec; j += 32) mine += Vec<InT>::count_ge(sv.vec(j), t2);
+        mine = Vec<InT>::count_fold(mine);
     }
+    SLC_MARK(18);
     uint32_t incl = mine;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -292,16 +383,15 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
 #pragma unroll 1
         for (int j = lane; j < sv.nvec && pos < uint32_t(kLCap); j += 32) {
             const uint4 v = sv.vec(j);
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float x = Vec<InT>::get(v, e);
-                if (x > -INFINITY && f2key(x) >= tau) {
-                    if (pos < uint32_t(kLCap)) body->list[pos] = cand_word(f2key(x), sv.c0 + j * E + e);
-                    ++pos;
-                }
+#pragma unroll 1
+            for (uint32_t hit = Vec<InT>::mask_ge(v, t2); hit; hit &= hit - 1u) {
+                const int e = __ffs(hit) - 1;
+                if (pos < uint32_t(kLCap)) body->list[pos] = cand_word(f2key(Vec<InT>::get(v, e)), sv.c0 + j * E + e);
+                ++pos;
             }
         }
     }
+    SLC_MARK(19);
     // top-p rows without top-k: the unit's softmax mass at its maximum
     float zsum = 0.0f, zlow = 0.0f;
     if (ri.need_z && mx > -INFINITY && mx < INFINITY) {
@@ -334,6 +424,9 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
 }
 
 // ---------------------------------------------------------------- finishing
+// A row is finished once, by one warp, usually with none of this code in the
+// SM's instruction cache: a cold instruction costs far more than a hot one, so
+// the finishing code is kept short (loops rolled, helpers out of line).
 __device__ __forceinline__ int32_t status_of(uint32_t fl)
 {
     if (fl & kFlagNonFinite) return kRowNonFinite;
@@ -359,52 +452,48 @@ __device__ __forceinline__ SliceHdr ld_hdr(const SliceHdr* p)
     return h;
 }
 
-// The pick between the best two candidates in double precision (the exact
-// Gumbel-max score); logits read again, Philox words recomputed.
+// Exact (double-precision) Gumbel score of token v of the row, its logit read
+// again and its Philox word recomputed.
 template <typename InT>
-__device__ __noinline__ int settle_pair(const KernelParams& kp, const RowInfo& ri, uint32_t off_lo, uint32_t off_hi,
-                                        unsigned long long a, unsigned long long b)
+static __device__ __noinline__ double exact_score(const KernelParams& kp, const RowInfo& ri, uint32_t off_lo,
+                                                  uint32_t off_hi, int v)
 {
-    const int ia = cand_idx(a), ib = cand_idx(b);
     const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
-    const float xa = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + ia);
-    const float xb = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + ib);
-    const double sa = gumbel_score_f64(xa, ri.T, philox_word(rp, ia));
-    const double sb = gumbel_score_f64(xb, ri.T, philox_word(rp, ib));
-    return (sa > sb || (sa == sb && ia < ib)) ? ia : ib;
+    const float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    return gumbel_score_f64(x, ri.T, philox_word(rp, v));
 }
 
 // The pick from the best two candidates (composite keys; b may be 0): by their
-// fp32 scores when those are further apart than their error bound, else in
-// double precision.
+// fp32 scores when those are further apart than their error bound, else by the
+// exact scores.
 template <typename InT>
 __device__ __forceinline__ int pick_of(const KernelParams& kp, const RowInfo& ri, uint32_t off_lo, uint32_t off_hi,
                                        const K2& t)
 {
-    if (t.b == 0ull) return cand_idx(t.a);
+    const int ia = cand_idx(t.a);
+    if (t.b == 0ull) return ia;
     const float sa = gkey_score(t.a), sb = gkey_score(t.b);
-    if (sa - sb > settle_eps(sa, sb)) return cand_idx(t.a);
-    return settle_pair<InT>(kp, ri, off_lo, off_hi, t.a, t.b);
+    if (sa - sb > settle_eps(sa, sb)) return ia;
+    const int ib = cand_idx(t.b);
+    const double da = exact_score<InT>(kp, ri, off_lo, off_hi, ia);
+    const double db = exact_score<InT>(kp, ri, off_lo, off_hi, ib);
+    return (da > db || (da == db && ia < ib)) ? ia : ib;
 }
 
 __device__ __forceinline__ void finish_greedy(const SliceParams& P, int r)
 {
     const int lane = threadIdx.x & 31;
-    const int G = P.G;
-    const SliceHdr* hd = P.hdr + size_t(r) * G;
+    const SliceHdr* hd = P.hdr + size_t(r) * P.G;
     float m = -INFINITY;
     int mi = INT_MAX;
     uint32_t fl = 0;
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        const int b = lane + 32 * i;
-        if (b < G) {
-            const SliceHdr h = ld_hdr(hd + b);
-            fl |= h.flags;
-            if (h.mx > m || (h.mx == m && h.amax < mi)) {
-                m = h.mx;
-                mi = h.amax;
-            }
+#pragma unroll 1
+    for (int b = lane; b < P.G; b += 32) {
+        const SliceHdr h = ld_hdr(hd + b);
+        fl |= h.flags;
+        if (h.mx > m || (h.mx == m && h.amax < mi)) {
+            m = h.mx;
+            mi = h.amax;
         }
     }
     fl = warp_or(fl);
@@ -417,20 +506,16 @@ __device__ __forceinline__ void finish_plain(const SliceParams& P, const RowInfo
                                              uint32_t off_hi)
 {
     const int lane = threadIdx.x & 31;
-    const int G = P.G;
-    const SliceHdr* hd = P.hdr + size_t(r) * G;
-    const SliceBody* bd = P.body + size_t(r) * G;
+    const SliceHdr* hd = P.hdr + size_t(r) * P.G;
+    const SliceBody* bd = P.body + size_t(r) * P.G;
     K2 t{0ull, 0ull};
     uint32_t fl = 0;
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        const int b = lane + 32 * i;
-        if (b < G) {
-            fl |= __ldcg(&hd[b].flags);
-            const uint4 g = __ldcg(reinterpret_cast<const uint4*>(&bd[b].ga));
-            k2_insert(t, (static_cast<unsigned long long>(g.y) << 32) | g.x);
-            k2_insert(t, (static_cast<unsigned long long>(g.w) << 32) | g.z);
-        }
+#pragma unroll 1
+    for (int b = lane; b < P.G; b += 32) {
+        fl |= __ldcg(&hd[b].flags);
+        const uint4 g = __ldcg(reinterpret_cast<const uint4*>(&bd[b].ga));
+        k2_insert(t, (static_cast<unsigned long long>(g.y) << 32) | g.x);
+        k2_insert(t, (static_cast<unsigned long long>(g.w) << 32) | g.z);
     }
     fl = warp_or(fl);
     k2_warp_reduce(t);
@@ -440,76 +525,66 @@ __device__ __forceinline__ void finish_plain(const SliceParams& P, const RowInfo
     if (lane == 0) write_out(P.k, r, token, st);
 }
 
-// The digit d (0..255, bins[d] counts keys) where the count of keys in digits
-// >= d first reaches `target`; `above` gets the count in digits > d. Lane L
-// scans digits 255 - 8L down to 248 - 8L.
-__device__ __forceinline__ int hist_pick(const uint32_t* bins, uint32_t target, uint32_t& above)
+// The largest 16-bit prefix P with at least k keys >= P << 16 (so P << 16 is at
+// most the k-th largest key), found two bits at a time: count3(c1, c2, c3, n)
+// adds to n[i] how many of the lane's keys reach c_i, and the warp sums them.
+template <typename Count3>
+__device__ __forceinline__ uint32_t kth_prefix(uint32_t k, Count3 count3)
 {
-    const int lane = threadIdx.x & 31;
-    uint32_t c[8], s = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        c[q] = bins[255 - (lane * 8 + q)];
-        s += c[q];
+    uint32_t p = 0;
+#pragma unroll 1
+    for (int sh = 14; sh >= 0; sh -= 2) {
+        uint32_t n[3] = {0u, 0u, 0u};
+        count3((p | (1u << sh)) << 16, (p | (2u << sh)) << 16, (p | (3u << sh)) << 16, n);
+        const uint32_t n1 = __reduce_add_sync(0xffffffffu, n[0]);
+        const uint32_t n2 = __reduce_add_sync(0xffffffffu, n[1]);
+        const uint32_t n3 = __reduce_add_sync(0xffffffffu, n[2]);
+        p |= (n3 >= k ? 3u : n2 >= k ? 2u : n1 >= k ? 1u : 0u) << sh;
     }
-    uint32_t incl = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    uint32_t run = incl - s;
-    int dig = -1;
-    uint32_t abv = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        if (dig < 0 && run + c[q] >= target) {
-            dig = 255 - (lane * 8 + q);
-            abv = run;
-        }
-        run += c[q];
-    }
-    const uint32_t who = __ballot_sync(0xffffffffu, dig >= 0);
-    const int src = who ? __ffs(who) - 1 : 0;
-    above = __shfl_sync(0xffffffffu, abv, src);
-    return who ? __shfl_sync(0xffffffffu, dig, src) : 0;
+    return p << 16;
 }
 
-// A 16-bit prefix P with at least k of the row's sketch keys >= P << 16, and
-// P << 16 at most the k-th largest of them (the row holds at least k keys).
-// sk: the sketches of the row's slices, kSketch words each.
-static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, int G, const uint32_t (&msk)[kSPL], int k,
-                                                     uint32_t* bins)
+__device__ __forceinline__ void count3_key(uint32_t key, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t (&n)[3])
+{
+    n[0] += key >= c1 ? 1u : 0u;
+    n[1] += key >= c2 ? 1u : 0u;
+    n[2] += key >= c3 ? 1u : 0u;
+}
+
+// B for a top-k row: the 16-bit prefix of the k-th largest sketch key over the
+// row (the row holds at least k). sk: kSketch words per slice, meta[b].w of
+// them valid; each lane holds the keys of its slices in registers.
+static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t pre = 0, target = uint32_t(k);
-#pragma unroll 1
-    for (int level = 0; level < 2; ++level) {
-        for (int i = lane; i < 256; i += 32) bins[i] = 0;
-        __syncwarp();
-#pragma unroll 1
-        for (int i = 0; i < kSPL; ++i) {
-            const int b = lane + 32 * i;
-            if (b >= G) break;
-            for (uint32_t q = 0; q < msk[i]; ++q) {
-                const uint32_t key = sk[b * kSketch + q];
-                if (level == 1 && (key >> 24) != pre) continue;
-                atomicAdd(&bins[level == 0 ? (key >> 24) : ((key >> 16) & 255u)], 1u);
-            }
+    uint32_t key[kSPL * kSketch];
+#pragma unroll
+    for (int i = 0; i < kSPL; ++i) {
+        const int b = lane + 32 * i;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        uint32_t mb = 0;
+        if (b < G) {
+            lo = *reinterpret_cast<const uint4*>(sk + b * kSketch);
+            hi = *reinterpret_cast<const uint4*>(sk + b * kSketch + 4);
+            mb = meta[b].w;
         }
-        __syncwarp();
-        uint32_t above;
-        const int d = hist_pick(bins, target, above);
-        __syncwarp();
-        pre = level == 0 ? uint32_t(d) : (pre << 8) | uint32_t(d);
-        target -= above;
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int q = 0; q < kSketch; ++q) key[i * kSketch + q] = uint32_t(q) < mb ? w[q] : 0u;
     }
-    return pre << 16;
+    return kth_prefix(uint32_t(k), [&](uint32_t c1, uint32_t c2, uint32_t c3, uint32_t(&n)[3]) {
+        // four independent partial counts per threshold (short dependency chains)
+        uint32_t part[4][3] = {};
+#pragma unroll
+        for (int q = 0; q < kSPL * kSketch; ++q) count3_key(key[q], c1, c2, c3, part[q & 3]);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) n[j] = part[0][j] + part[1][j] + part[2][j] + part[3][j];
+    });
 }
 
 // Keep, stably and at the front, the words whose key reaches lo; returns how
 // many were kept.
-__device__ __forceinline__ int compact_ge(unsigned long long* c, int n, uint32_t lo)
+static __device__ __noinline__ int compact_ge(unsigned long long* c, int n, uint32_t lo)
 {
     const int lane = threadIdx.x & 31;
     int kept = 0;
@@ -527,6 +602,27 @@ __device__ __forceinline__ int compact_ge(unsigned long long* c, int n, uint32_t
     return kept;
 }
 
+// Keep (at the front, in their order) the candidates whose key's top 16 bits
+// reach those of the k-th largest key: the k largest words and their ties in
+// that 16-bit bin. Returns how many were kept.
+static __device__ __noinline__ int select_top(unsigned long long* c, int n, int k)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t lo = kth_prefix(uint32_t(k), [&](uint32_t c1, uint32_t c2, uint32_t c3, uint32_t(&m)[3]) {
+        uint32_t part[2][3] = {};
+        int i = lane;
+#pragma unroll 1
+        for (; i + 32 < n; i += 64) {
+            count3_key(cand_key(c[i]), c1, c2, c3, part[0]);
+            count3_key(cand_key(c[i + 32]), c1, c2, c3, part[1]);
+        }
+        if (i < n) count3_key(cand_key(c[i]), c1, c2, c3, part[0]);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) m[j] = part[0][j] + part[1][j];
+    });
+    return compact_ge(c, n, lo);
+}
+
 // The min-p threshold on the logit, m + T ln(min_p) in double precision,
 // rounded up to fp32 (x >= result exactly when x >= the double threshold).
 static __device__ __noinline__ float minp_threshold(float m, float T, float minp)
@@ -537,120 +633,6 @@ static __device__ __noinline__ float minp_threshold(float m, float T, float minp
     return t;
 }
 
-// The cuts over the sorted candidates of a truncated row, each keeping a prefix
-// (top-k, then top-p over the top-k set or the whole row, then min-p), and the
-// Gumbel pick over what is kept. Returns false when top-p reaches past the
-// candidates of a row without top-k or min-p (the exact path takes it).
-template <typename InT>
-__device__ __forceinline__ bool cut_and_pick(const SliceParams& P, const RowInfo& ri, int r, uint32_t off_lo,
-                                             uint32_t off_hi, const unsigned long long* cand, int C, float m,
-                                             float xthr, const SliceHdr (&h)[kSPL], const SliceBody* bd, int G)
-{
-    const int lane = threadIdx.x & 31;
-    const int nk = ri.do_topk ? ri.k : C;
-    int nkeep = nk;
-    if (ri.do_topp) {
-        // fixed-point masses (2^-40 units of exp((x - m) / T)); keep while the
-        // exclusive prefix mass is below p * Z
-        double Zq;
-        if (ri.do_topk) {
-            unsigned long long s = 0;
-            for (int i = lane; i < nk; i += 32) s += mass_q(key2f(cand_key(cand[i])), m, ri.invT);
-            Zq = double(warp_sum_u64(s));
-        } else {
-            double z = 0.0;
-#pragma unroll
-            for (int i = 0; i < kSPL; ++i) {
-                const int b = lane + 32 * i;
-                if (b < G && h[i].mx > -INFINITY) {
-                    const float zs = __ldcg(&bd[b].zs), zc = __ldcg(&bd[b].zc);
-                    z += (double(zs) + double(zc)) * double(exp2f((h[i].mx - m) * ri.s2));
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-            Zq = z * 0x1p40;
-        }
-        const double target = double(ri.p) * Zq;
-        unsigned long long base = 0;
-        int cut = nk;
-#pragma unroll 1
-        for (int i0 = 0; i0 < nk; i0 += 32) {
-            const int i = i0 + lane;
-            const unsigned long long q = i < nk ? mass_q(key2f(cand_key(cand[i])), m, ri.invT) : 0ull;
-            unsigned long long incl = q;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            const unsigned long long excl = base + incl - q;
-            const uint32_t sb = __ballot_sync(0xffffffffu, i < nk && i > 0 && !(double(excl) < target));
-            if (sb) {
-                cut = i0 + __ffs(sb) - 1;
-                break;
-            }
-            base += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (!ri.do_topk && !ri.do_minp && cut == nk) return false;  // the cut lies past the candidates
-        nkeep = cut;
-    }
-    if (ri.do_minp) {
-        int c = 0;
-        for (int i = lane; i < nkeep; i += 32) c += key2f(cand_key(cand[i])) >= xthr ? 1 : 0;
-        nkeep = min(nkeep, int(__reduce_add_sync(0xffffffffu, uint32_t(c))));
-    }
-    nkeep = max(nkeep, 1);
-    // Gumbel-max over the kept prefix
-    const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
-    K2 t{0ull, 0ull};
-#pragma unroll 1
-    for (int i = lane; i < nkeep; i += 32) {
-        const unsigned long long c = cand[i];
-        const int v = cand_idx(c);
-        k2_insert(t, gkey(score2(key2f(cand_key(c)), ri.s2, philox_word(rp, v)), v));
-    }
-    k2_warp_reduce(t);
-    const int token = pick_of<InT>(P.k, ri, off_lo, off_hi, t);
-    if (lane == 0) write_out(P.k, r, token, kRowOk);
-    return true;
-}
-
-// Sort 32 * Q words held Q per lane (word q * 32 + lane), descending (bitonic).
-template <int Q>
-__device__ __forceinline__ void warp_sort_regs(unsigned long long (&a)[Q])
-{
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int size = 2; size <= 32 * Q; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride >= 32) {
-                const int qs = stride >> 5;
-#pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    if ((q & qs) == 0) {
-                        const int q2 = q | qs;
-                        const bool desc = ((q * 32 + lane) & size) == 0;
-                        const unsigned long long x = a[q], y = a[q2];
-                        const bool sw = desc ? (x < y) : (x > y);
-                        a[q] = sw ? y : x;
-                        a[q2] = sw ? x : y;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < Q; ++q) {
-                    const bool desc = ((q * 32 + lane) & size) == 0;
-                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, a[q], stride);
-                    const bool keep_max = desc == ((lane & stride) == 0);
-                    a[q] = keep_max ? (a[q] > o ? a[q] : o) : (a[q] < o ? a[q] : o);
-                }
-            }
-        }
-    }
-}
-
 // Sort n words in warp-private shared memory, descending (bitonic through
 // shared memory, padded with zeros up to a power of two; the buffer holds it).
 static __device__ __noinline__ void warp_sort_smem(unsigned long long* a, int n)
@@ -658,12 +640,14 @@ static __device__ __noinline__ void warp_sort_smem(unsigned long long* a, int n)
     const int lane = threadIdx.x & 31;
     int np2 = 1;
     while (np2 < n) np2 <<= 1;
+#pragma unroll 1
     for (int i = n + lane; i < np2; i += 32) a[i] = 0ull;
     __syncwarp();
 #pragma unroll 1
     for (int size = 2; size <= np2; size <<= 1) {
 #pragma unroll 1
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll 1
             for (int t = lane; t < (np2 >> 1); t += 32) {
                 const int lo = ((t & ~(stride - 1)) << 1) | (t & (stride - 1));
                 const int hi = lo + stride;
@@ -679,21 +663,120 @@ static __device__ __noinline__ void warp_sort_smem(unsigned long long* a, int n)
     }
 }
 
-// Sort the warp's n candidates, descending.
-__device__ __forceinline__ void sort_cands(unsigned long long* c, int n)
+// The first `keep` of n distinct words in descending order, out[rank] = word:
+// each word's rank is the number of larger words, counted by its lane against
+// every word (broadcast reads, four partial counts).
+static __device__ __noinline__ void rank_sort(const unsigned long long* c, int n, unsigned long long* out, int keep)
 {
     const int lane = threadIdx.x & 31;
-    if (n <= 64) {
-        unsigned long long a[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) a[q] = q * 32 + lane < n ? c[q * 32 + lane] : 0ull;
-        warp_sort_regs<2>(a);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) c[q * 32 + lane] = a[q];
-        __syncwarp();
-    } else {
-        warp_sort_smem(c, n);
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + lane;
+        const unsigned long long w = i < n ? c[i] : ~0ull;
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        int j = 0;
+#pragma unroll 1
+        for (; j + 4 <= n; j += 4) {
+            r0 += c[j] > w ? 1 : 0;
+            r1 += c[j + 1] > w ? 1 : 0;
+            r2 += c[j + 2] > w ? 1 : 0;
+            r3 += c[j + 3] > w ? 1 : 0;
+        }
+#pragma unroll 1
+        for (; j < n; ++j) r0 += c[j] > w ? 1 : 0;
+        const int rank = r0 + r1 + r2 + r3;
+        if (i < n && rank < keep) out[rank] = w;
     }
+    __syncwarp();
+}
+
+// Inclusive warp scan of a 64-bit count.
+__device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    return v;
+}
+
+// The cuts over the sorted candidates of a truncated row, each keeping a prefix
+// (top-k, then top-p over the top-k set or the whole row, then min-p), and the
+// Gumbel pick over what is kept. Returns false when top-p reaches past the
+// candidates of a row without top-k or min-p (the exact path takes it).
+// hs / meta: the slices' staged headers and (tau, zs, zc, m) words.
+template <typename InT>
+static __device__ __noinline__ bool cut_and_pick(const SliceParams& P, const RowInfo& ri, int r, uint32_t off_lo,
+                                                 uint32_t off_hi, const unsigned long long* cand, int C, float m,
+                                                 float xthr, const SliceHdr* hs, const uint4* meta)
+{
+    const int lane = threadIdx.x & 31;
+    const int nk = ri.do_topk ? ri.k : C;
+    int nkeep = nk;
+    if (ri.do_topp) {
+        // fixed-point masses (2^-40 units of exp((x - m) / T)); keep while the
+        // exclusive prefix mass is below p * Z, i.e. below tq = ceil(p * Zq)
+        double Zq;
+        if (ri.do_topk) {
+            unsigned long long s = 0;
+#pragma unroll 1
+            for (int i = lane; i < nk; i += 32) s += mass_q(key2f(cand_key(cand[i])), m, ri.invT);
+            Zq = double(warp_sum_u64(s));
+        } else {
+            double z = 0.0;
+#pragma unroll 1
+            for (int b = lane; b < P.G; b += 32) {
+                const float mx = hs[b].mx;
+                if (mx > -INFINITY)
+                    z += (double(__uint_as_float(meta[b].y)) + double(__uint_as_float(meta[b].z))) *
+                         double(exp2f((mx - m) * ri.s2));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+            Zq = z * 0x1p40;
+        }
+        const unsigned long long tq = __double2ull_ru(double(ri.p) * Zq);
+        unsigned long long base = 0;
+        int cut = nk;
+#pragma unroll 1
+        for (int i0 = 0; i0 < nk; i0 += 32) {
+            const int i = i0 + lane;
+            const unsigned long long q = i < nk ? mass_q(key2f(cand_key(cand[i])), m, ri.invT) : 0ull;
+            const unsigned long long incl = warp_incl_u64(q);
+            const unsigned long long excl = base + incl - q;
+            const uint32_t sb = __ballot_sync(0xffffffffu, i < nk && i > 0 && !(excl < tq));
+            if (sb) {
+                cut = i0 + __ffs(sb) - 1;
+                break;
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (!ri.do_topk && !ri.do_minp && cut == nk) return false;  // the cut lies past the candidates
+        nkeep = cut;
+    }
+    if (ri.do_minp) {
+        int c = 0;
+#pragma unroll 1
+        for (int i = lane; i < nkeep; i += 32) c += key2f(cand_key(cand[i])) >= xthr ? 1 : 0;
+        nkeep = min(nkeep, int(__reduce_add_sync(0xffffffffu, uint32_t(c))));
+    }
+    nkeep = max(nkeep, 1);
+    SLC_MARK(14);
+    // Gumbel-max over the kept prefix
+    const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
+    K2 t{0ull, 0ull};
+#pragma unroll 1
+    for (int i = lane; i < nkeep; i += 32) {
+        const unsigned long long c = cand[i];
+        const int v = cand_idx(c);
+        k2_insert(t, gkey(score2(key2f(cand_key(c)), ri.s2, philox_word(rp, v)), v));
+    }
+    k2_warp_reduce(t);
+    const int token = pick_of<InT>(P.k, ri, off_lo, off_hi, t);
+    if (lane == 0) write_out(P.k, r, token, kRowOk);
+    return true;
 }
 
 __device__ __forceinline__ void cp_async_commit_wait()
@@ -701,120 +784,152 @@ __device__ __forceinline__ void cp_async_commit_wait()
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Keep (at the front, in their order) the candidates whose key's top 16 bits
-// reach those of the k-th largest key: the k largest words and their ties in
-// that 16-bit bin. Returns how many were kept.
-static __device__ __noinline__ int select_top(unsigned long long* c, int n, int k, uint32_t* bins)
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc)
 {
-    const int lane = threadIdx.x & 31;
-    uint32_t pre = 0, target = uint32_t(k);
-#pragma unroll 1
-    for (int level = 0; level < 2; ++level) {
-        for (int i = lane; i < 256; i += 32) bins[i] = 0;
-        __syncwarp();
-        for (int i = lane; i < n; i += 32) {
-            const uint32_t key = cand_key(c[i]);
-            if (level == 1 && (key >> 24) != pre) continue;
-            atomicAdd(&bins[level == 0 ? (key >> 24) : ((key >> 16) & 255u)], 1u);
-        }
-        __syncwarp();
-        uint32_t above;
-        const int d = hist_pick(bins, target, above);
-        __syncwarp();
-        pre = level == 0 ? uint32_t(d) : (pre << 8) | uint32_t(d);
-        target -= above;
-    }
-    return compact_ge(c, n, pre << 16);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
 }
 
-// Append the finite tokens of slice b whose key reaches B to the candidates,
-// reading the slice again from global memory.
+// Vector j of a slice that is not 16-byte aligned, or the ragged last one, read
+// element by element (-inf past the slice).
 template <typename InT>
-__device__ __noinline__ void reread_slice(const SliceParams& P, const RowInfo& ri, int b, uint32_t B,
-                                          unsigned long long* cand, int cap, uint32_t* count)
+static __device__ __noinline__ uint4 load_vec_slow(const InT* g, int j, int n)
 {
-    constexpr int E = Vec<InT>::E;
-    const int lane = threadIdx.x & 31;
-    const int V = int(P.k.vocab);
-    const int c0 = b * P.W;
-    const int n = min(P.W, V - c0);
     SliceView<InT> sv;
     sv.sm = nullptr;
-    sv.g = slice_ptr<InT>(P.k, ri.lrow, c0);
+    sv.g = g;
     sv.nb = 0;
-    sv.nvec = (n + E - 1) / E;
+    sv.nvec = 0;
     sv.n = n;
-    sv.c0 = c0;
-    const bool al = (reinterpret_cast<uintptr_t>(sv.g) & 15u) == 0;
-    const uint4* gv = reinterpret_cast<const uint4*>(sv.g);
-    for (int j = lane; j < sv.nvec; j += 32) {
-        const uint4 v = (al && (j + 1) * E <= n) ? __ldg(gv + j) : sv.vec(j);
+    sv.c0 = 0;
+    return sv.vec(j);
+}
+
+// Append to the candidates c[C0..) the finite tokens >= B (order key) of the
+// nre slices listed in re[], reading them again from global memory: 8 vectors
+// per lane in flight, counted, then written at their warp-wide positions.
+// Returns the new count (more than cap when they do not fit).
+template <typename InT>
+static __device__ __noinline__ int reread_slices(const SliceParams& P, const RowInfo& ri, const uint16_t* re,
+                                                 int nre, uint32_t B, unsigned long long* c, int C0, int cap)
+{
+    constexpr int E = Vec<InT>::E;
+    constexpr int U = 8;
+    const int lane = threadIdx.x & 31;
+    const int V = int(P.k.vocab);
+    const int nvW = (P.W + E - 1) / E;
+    const int total = nre * nvW;
+    // x >= tB exactly when x is not -inf and its key reaches B
+    const float tB = B < 0x00800000u ? -FLT_MAX : key2f(B);
+    const typename Vec<InT>::Thr t2 = Vec<InT>::thr(tB);
+    int C = C0;
+#pragma unroll 1
+    for (int base = 0; base < total; base += 32 * U) {
+        uint4 v[U];
+        int t0[U];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float x = Vec<InT>::get(v, e);
-            if (x > -INFINITY && f2key(x) >= B) {
-                const uint32_t pos = atomicAdd(count, 1u);
-                if (pos < uint32_t(cap)) cand[pos] = cand_word(f2key(x), c0 + j * E + e);
+        for (int u = 0; u < U; ++u) {
+            const int f = base + u * 32 + lane;
+            const int si = f / nvW;
+            const int j = f - si * nvW;
+            const int b = f < total ? int(re[si]) : 0;
+            const int c0 = b * P.W;
+            const int n = min(P.W, V - c0);
+            const InT* g = slice_ptr<InT>(P.k, ri.lrow, c0);
+            t0[u] = c0 + j * E;
+            v[u] = Vec<InT>::neg_inf();
+            if (f < total && j * E < n) {
+                if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0 && (j + 1) * E <= n)
+                    v[u] = __ldg(reinterpret_cast<const uint4*>(g) + j);
+                else
+                    v[u] = load_vec_slow<InT>(g, j, n);
             }
         }
+        uint32_t mine = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) mine += Vec<InT>::count_ge(v[u], t2);
+        mine = Vec<InT>::count_fold(mine);
+        SLC_MARK(15);
+        uint32_t incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        uint32_t pos = uint32_t(C) + incl - mine;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll 1
+            for (uint32_t hit = Vec<InT>::mask_ge(v[u], t2); hit; hit &= hit - 1u) {
+                const int e = __ffs(hit) - 1;
+                if (pos < uint32_t(cap)) c[pos] = cand_word(f2key(Vec<InT>::get(v[u], e)), t0[u] + e);
+                ++pos;
+            }
+        }
+        C += int(__shfl_sync(0xffffffffu, incl, 31));
     }
     __syncwarp();
+    return C;
 }
 
 // A truncated row from its slices' records. The warp's staging slot (idle at
-// this point) is its scratch: the slices' sketches, then their lists, which
-// become the candidates. All record loads go out in two rounds (headers and
-// sketches, then the lists that matter). Returns false when the row must take
-// the exact path (m out).
+// this point) is its scratch: the slices' headers, (tau, zs, zc, m) words and
+// sketches in one round of copies; then, over the sketches, the lists of the
+// slices that matter in a second round, which become the candidates. Returns
+// false when the row must take the exact path (m out).
 template <typename InT>
-__device__ __forceinline__ bool finish_trunc(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
-                                             uint32_t off_lo, uint32_t off_hi, unsigned char* scratch, float& m_out)
+static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
+                                                 uint32_t off_lo, uint32_t off_hi, unsigned char* scratch,
+                                                 float& m_out)
 {
     const int lane = threadIdx.x & 31;
     const int G = P.G;
     const SliceHdr* hd = P.hdr + size_t(r) * G;
     const SliceBody* bd = P.body + size_t(r) * G;
-    uint32_t* sk = reinterpret_cast<uint32_t*>(scratch);  // [G][kSketch]
-    unsigned long long* area = reinterpret_cast<unsigned long long*>(scratch + size_t(G) * kSketch * 4);
-    const int cap = int((size_t(kSlotBytes) - size_t(G) * kSketch * 4) / 8);
-    // round 1: headers and (tau, zs, zc, m) into registers, sketches into the scratch
+    SliceHdr* hs = reinterpret_cast<SliceHdr*>(scratch);            // [G]
+    uint4* meta = reinterpret_cast<uint4*>(scratch + size_t(G) * 16);  // [G]
+    uint32_t* sk = reinterpret_cast<uint32_t*>(scratch + size_t(G) * 32);  // [G][kSketch]
+    // with few slices every list comes in the first round too (after the
+    // sketches), and the candidates are gathered from there; otherwise the
+    // second round brings the lists that matter over the sketches
+    const bool one_round = false;
+    unsigned long long* lists = reinterpret_cast<unsigned long long*>(scratch + size_t(G) * 64);  // [G][kLCap]
+    unsigned long long* area = one_round ? lists : reinterpret_cast<unsigned long long*>(sk);
+    const int cap = int((size_t(kSlotBytes) - size_t(one_round ? 64 : 32) * G) / 8);
+    // round 1
+#pragma unroll 1
     for (int b = lane; b < G; b += 32) {
+        cp_async16(hs + b, hd + b);
+        cp_async16(meta + b, &bd[b].tau);
         cp_async16(sk + b * kSketch, &bd[b].sketch[0]);
         cp_async16(sk + b * kSketch + 4, &bd[b].sketch[4]);
     }
-    SliceHdr h[kSPL];
-    uint32_t tau[kSPL], msk[kSPL];
-    uint32_t fl = 0, nkeys = 0;
-    float m = -INFINITY;
-    int mi = INT_MAX;
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        const int b = lane + 32 * i;
-        h[i].mx = -INFINITY;
-        h[i].amax = INT_MAX;
-        h[i].flags = 0;
-        h[i].n = 0;
-        tau[i] = 0;
-        msk[i] = 0;
-        if (b < G) {
-            h[i] = ld_hdr(hd + b);
-            const uint4 t4 = __ldcg(reinterpret_cast<const uint4*>(&bd[b].tau));
-            tau[i] = t4.x;
-            msk[i] = t4.w;
+    if (one_round) {
+#pragma unroll 1
+        for (int i = lane; i < G * (kLCap / 2); i += 32) {
+            const int b = i / (kLCap / 2), e = 2 * (i - b * (kLCap / 2));
+            cp_async16(lists + b * kLCap + e, &bd[b].list[e]);
         }
     }
     cp_async_commit_wait();
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        fl |= h[i].flags;
-        nkeys += msk[i];
-        if (h[i].mx > m || (h[i].mx == m && h[i].amax < mi)) {
-            m = h[i].mx;
-            mi = h[i].amax;
+    __syncwarp();
+    SLC_MARK(7);
+    uint32_t fl = 0, nkeys = 0, taumax = 0;
+    float m = -INFINITY;
+    int mi = INT_MAX;
+#pragma unroll 1
+    for (int b = lane; b < G; b += 32) {
+        const SliceHdr h = hs[b];
+        fl |= h.flags;
+        nkeys += meta[b].w;
+        taumax = max(taumax, meta[b].x);
+        if (h.mx > m || (h.mx == m && h.amax < mi)) {
+            m = h.mx;
+            mi = h.amax;
         }
     }
     fl = warp_or(fl);
     nkeys = __reduce_add_sync(0xffffffffu, nkeys);
+    taumax = __reduce_max_sync(0xffffffffu, taumax);
     warp_max_idx(m, mi);
     m_out = m;
     const int32_t st = status_of(fl);
@@ -822,7 +937,6 @@ __device__ __forceinline__ bool finish_trunc(const SliceParams& P, WarpScratch& 
         if (lane == 0) write_out(P.k, r, -1, st);
         return true;
     }
-    __syncwarp();
     // the min-p threshold on the logit: m + T ln(min_p), rounded up to fp32
     float xthr = -INFINITY;
     if (ri.do_minp) xthr = minp_threshold(m, ri.T, ri.minp);
@@ -830,86 +944,103 @@ __device__ __forceinline__ bool finish_trunc(const SliceParams& P, WarpScratch& 
     uint32_t B;
     if (ri.do_topk) {
         if (ri.k > kKCap || nkeys < uint32_t(ri.k)) return false;
-        B = sketch_bound(sk, G, msk, ri.k, ws.hist);
+        B = sketch_bound(sk, meta, G, ri.k);
     } else if (ri.do_minp) {
         B = f2key(xthr);
     } else {
-        uint32_t t = 0;
-#pragma unroll
-        for (int i = 0; i < kSPL; ++i) t = max(t, tau[i]);
-        B = __reduce_max_sync(0xffffffffu, t);
+        B = taumax;
     }
     B = max(B, 1u);
-    // round 2: the lists of the slices that reach B and are complete above it,
-    // copied side by side (even lengths; a padding entry is cleared); the
-    // others are read again below
-    uint32_t need = 0, mine = 0;
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        const int b = lane + 32 * i;
-        if (b < G && h[i].mx != -INFINITY && f2key(h[i].mx) >= B) {
-            if (h[i].n == kOverflow || tau[i] > B) need |= 2u << (2 * i);  // read again
-            else {
-                need |= 1u << (2 * i);
-                mine += (h[i].n + 1u) & ~1u;
+    SLC_MARK(8);
+    __syncwarp();
+    // round 2 (or a gather from the staged lists): the lists of the slices that
+    // reach B and are complete above it, side by side; the others are read
+    // again below
+    uint32_t total = 0, nre = 0;
+    if (one_round) {
+        // in place: an entry only moves down
+#pragma unroll 1
+        for (int i0 = 0; i0 < G * kLCap; i0 += 32) {
+            const int i = i0 + lane;
+            const int b = i / kLCap, e = i - b * kLCap;
+            bool keep = false, again = false;
+            unsigned long long w = 0ull;
+            if (i < G * kLCap) {
+                const SliceHdr h = hs[b];
+                if (h.mx > -INFINITY && f2key(h.mx) >= B) {
+                    if (h.n == kOverflow || meta[b].x > B) again = e == 0;
+                    else if (uint32_t(e) < h.n) {
+                        w = lists[i];
+                        keep = cand_key(w) >= B;
+                    }
+                }
+            }
+            const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+            __syncwarp();
+            if (keep) area[total + __popc(bal & ((1u << lane) - 1u))] = w;
+            total += __popc(bal);
+            const uint32_t who = __ballot_sync(0xffffffffu, again);
+            const uint32_t at = nre + __popc(who & ((1u << lane) - 1u));
+            if (again && at < uint32_t(kReCap)) ws.re[at] = uint16_t(b);
+            nre += __popc(who);
+            __syncwarp();
+        }
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < (one_round ? 0 : G); c0 += 32) {
+        const int b = c0 + lane;
+        uint32_t n = 0;
+        bool again = false;
+        if (b < G) {
+            const SliceHdr h = hs[b];
+            if (h.mx > -INFINITY && f2key(h.mx) >= B) {
+                if (h.n == kOverflow || meta[b].x > B) again = true;
+                else n = h.n;
             }
         }
-    }
-    uint32_t incl = mine;
+        uint32_t incl = n;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    if (total > uint32_t(cap)) return false;
-    uint32_t pos = incl - mine;
-    uint32_t nre = 0;
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        const int b = lane + 32 * i;
-        if (need & (1u << (2 * i))) {
-            const uint32_t n2 = (h[i].n + 1u) & ~1u;
-            for (uint32_t e = 0; e < n2; e += 2) cp_async16(area + pos + e, &bd[b].list[e]);
-            pos += n2;
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
         }
-        nre += (need >> (2 * i + 1)) & 1u;
+        const uint32_t pos = total + incl - n;
+        if (pos + n <= uint32_t(cap)) {
+#pragma unroll 1
+            for (uint32_t e = 0; e < n; ++e) cp_async8(area + pos + e, &bd[b].list[e]);
+        }
+        const uint32_t who = __ballot_sync(0xffffffffu, again);
+        const uint32_t at = nre + __popc(who & ((1u << lane) - 1u));
+        if (again && at < uint32_t(kReCap)) ws.re[at] = uint16_t(b);
+        nre += __popc(who);
+        total += __shfl_sync(0xffffffffu, incl, 31);
     }
     cp_async_commit_wait();
-    pos = incl - mine;
-#pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
-        if (need & (1u << (2 * i))) {
-            if (h[i].n & 1u) area[pos + h[i].n] = 0ull;
-            pos += (h[i].n + 1u) & ~1u;
-        }
-    }
     __syncwarp();
-    int C = compact_ge(area, int(total), B);
-    // slices whose lists are not complete above B, read again
-    if (__reduce_add_sync(0xffffffffu, nre) > uint32_t(kReCap)) return false;
-    if (lane == 0) ws.n = uint32_t(C);
-#pragma unroll 1
-    for (int i = 0; i < kSPL; ++i) {
-        const uint32_t who = __ballot_sync(0xffffffffu, (need >> (2 * i + 1)) & 1u);
-        for (uint32_t w2 = who; w2; w2 &= w2 - 1) {
-            __syncwarp();
-            reread_slice<InT>(P, ri, (__ffs(w2) - 1) + 32 * i, B, area, cap, &ws.n);
-        }
-    }
-    __syncwarp();
-    C = int(ws.n);
+    if (total > uint32_t(cap) || nre > uint32_t(kReCap)) return false;
+    int C = one_round ? int(total) : compact_ge(area, int(total), B);
+    SLC_MARK(9);
+    if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap);
+    SLC_MARK(10);
     if (C > cap) return false;
     if (ri.do_topk && C < ri.k) return false;
-    // top-k: bring the k largest to the front first when there are many more
-    if (ri.do_topk && C > 64 && C > ri.k) C = select_top(area, C, ri.k, ws.hist);
-    if (C > 64) {
+    const unsigned long long* sorted = area;
+    if (C <= kRankSortMax && 2 * C <= cap) {
+        // sorted copy after the candidates; a top-k row keeps only its k largest
+        const int keep = ri.do_topk ? ri.k : C;
+        rank_sort(area, C, area + C, keep);
+        sorted = area + C;
+        C = keep;
+    } else {
+        // top-k: bring the k largest to the front first
+        if (ri.do_topk && C > ri.k) C = select_top(area, C, ri.k);
         int np2 = 1;
         while (np2 < C) np2 <<= 1;
         if (np2 > cap) return false;
+        warp_sort_smem(area, C);
     }
-    sort_cands(area, C);
-    return cut_and_pick<InT>(P, ri, r, off_lo, off_hi, area, C, m, xthr, h, bd, G);
+    SLC_MARK(11);
+    return cut_and_pick<InT>(P, ri, r, off_lo, off_hi, sorted, C, m, xthr, hs, meta);
 }
 
 // ---------------------------------------------------------------- exact path (whole CTA)
@@ -1097,8 +1228,8 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
 // Wait for the warp's slot, summarise the unit into its record (row r, slice s).
 template <typename InT>
 __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo& ri, uint64_t* bar,
-                                             const unsigned char* slot, uint32_t parity, int r, int s,
-                                             uint32_t off_lo, uint32_t off_hi)
+                                             const unsigned char* slot, uint16_t* q, uint4* qw, uint32_t parity, int r,
+                                             int s, uint32_t off_lo, uint32_t off_hi)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -1111,6 +1242,7 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
         extra = kFlagTimeout;
         mbar_wait_bounded(bar, parity, kDrainPolls);
     }
+    SLC_MARK(3);
     if (ri.cls == kClsErr) return;
     const int c0 = s * P.W;
     const int n_el = min(P.W, int(kp.vocab) - c0);
@@ -1131,15 +1263,9 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
     if (!extra) {
         if (ri.cls == kClsGreedy) {
             float lm;
-            int li;
-            uint32_t f;
-            lane_max<InT>(sv, lm, li, f);
-            hdr.flags = warp_or(f);
-            warp_max_idx(lm, li);
-            hdr.mx = lm;
-            hdr.amax = li;
+            unit_max<InT>(sv, hdr.mx, hdr.amax, hdr.flags, lm);
         } else if (ri.cls == kClsPlain) {
-            unit_plain<InT>(sv, ri, off_lo, off_hi, g, hdr.flags);
+            unit_plain<InT>(sv, ri, off_lo, off_hi, q, qw, g, hdr.flags);
         } else {
             unit_trunc<InT>(sv, ri, hdr, body);
         }
@@ -1179,29 +1305,71 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
     extern __shared__ __align__(128) unsigned char smem[];
     SliceShared& sh = *reinterpret_cast<SliceShared*>(smem);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    unsigned char* slot = smem + kHead + size_t(wid) * kSlotBytes;
-    uint64_t* bar = &sh.full[wid];
     WarpScratch& ws = sh.ws[wid];
     const KernelParams& kp = P.k;
     const int NC = int(gridDim.x);
     const int stride = NC * kW;
-    int u = int(blockIdx.x) + wid * NC;  // round-robin over CTAs first
-    // the copy of this warp's first unit goes out before anything else
+    SLC_MARK(0);
+    // slot s of the CTA stages its units blockIdx.x + s * NC (+ k * stride):
+    // round-robin over CTAs first. The copy of its first unit goes out before
+    // anything else.
     if (lane == 0) {
-        mbar_init(bar, 1);
+        const int u0 = int(blockIdx.x) + wid * NC;
+        mbar_init(&sh.full[wid], 1);
         fence_mbar_init();
-        if (u < P.n_units) issue_unit<InT>(P, bar, slot, u);
+        if (u0 < P.n_units) issue_unit<InT>(P, &sh.full[wid], smem + kHead + size_t(wid) * kSlotBytes, u0);
     }
     if (tid == 0) sh.n_exact = 0;
     const uint64_t off = kp.philox_offset_dev ? *kp.philox_offset_dev : kp.philox_offset;
     const uint32_t off_lo = uint32_t(off), off_hi = uint32_t(off >> 32);
-    __syncthreads();  // n_exact is set before any warp can queue a row
+    // which slot this warp serves: the CTA's first units, by their cost (plain
+    // rows far above truncated ones, those above greedy ones), dealt over the
+    // four schedulers (warp w runs on scheduler w % 4) in snake order
+    int sidx;
+    RowInfo ri0;  // the parameters of the row of the slot's first unit
+    {
+        const int ul = int(blockIdx.x) + (lane & (kW - 1)) * NC;
+        int cost = 0;
+        RowInfo mine{};
+        if (ul < P.n_units) {
+            mine = load_info(P, ul / P.G);
+            const uint8_t c = mine.cls;
+            cost = c == kClsPlain ? 3 : c == kClsTrunc ? 2 : c == kClsGreedy ? 1 : 0;
+        }
+        // rank among the 16 (cost descending, slot ascending)
+        int rank = 0;
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t same = __ballot_sync(0xffffffffu, lane < kW && cost == c);
+            rank += c > cost ? __popc(same) : c == cost ? __popc(same & lt) : 0;
+        }
+        const int row4 = rank >> 2, col = rank & 3;
+        const int w_of = row4 * 4 + ((row4 & 1) ? 3 - col : col);
+        const uint32_t hit = __ballot_sync(0xffffffffu, lane < kW && w_of == wid);
+        sidx = __ffs(hit) - 1;
+        uint32_t wmine[sizeof(RowInfo) / 4], w0[sizeof(RowInfo) / 4];
+        memcpy(wmine, &mine, sizeof(RowInfo));
+#pragma unroll
+        for (int q = 0; q < int(sizeof(RowInfo) / 4); ++q) w0[q] = __shfl_sync(0xffffffffu, wmine[q], sidx);
+        memcpy(&ri0, w0, sizeof(RowInfo));
+    }
+    unsigned char* slot = smem + kHead + size_t(sidx) * kSlotBytes;
+    uint64_t* bar = &sh.full[sidx];
+    int u = int(blockIdx.x) + sidx * NC;
+    __syncthreads();  // barriers initialised, n_exact set before any warp can queue a row
+    SLC_MARK(1);
     uint32_t parity = 0;
+    bool first = true;
 #pragma unroll 1
     while (u < P.n_units) {
         const int r = u / P.G, s = u - r * P.G;
-        const RowInfo ri = load_info(P, r);
-        process_unit<InT>(P, ri, bar, slot, parity, r, s, off_lo, off_hi);
+        const RowInfo ri = first ? ri0 : load_info(P, r);
+        first = false;
+        SLC_MARK(2);
+        SLC_UCLS(ri.cls);
+        process_unit<InT>(P, ri, bar, slot, ws.q, ws.qw, parity, r, s, off_lo, off_hi);
+        SLC_MARK(5);
         parity ^= 1u;
         const int un = u + stride;
         if (ri.cls == kClsErr) {
@@ -1213,10 +1381,13 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
             uint32_t old = 0;
             if (lane == 0) old = atom_add_acq_rel(&P.cnt[size_t(r) * kCntStride], 1u);
             old = __shfl_sync(0xffffffffu, old, 0);
+            SLC_MARK(6);
             if (old == uint32_t(P.G - 1)) {
                 __syncwarp();
                 float m;
+                SLC_TAG(ri.cls);
                 const bool done = finish_row<InT>(P, ws, ri, r, off_lo, off_hi, slot, m);
+                SLC_MARK(12);
                 if (lane == 0) {
                     P.cnt[size_t(r) * kCntStride] = 0;
                     if (!done) {
@@ -1235,6 +1406,7 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
         }
         u = un;
     }
+    SLC_MARK(13);
     // rows the candidate lists could not settle
     __syncthreads();
     const int ne = sh.n_exact;

@@ -61,13 +61,14 @@ namespace slc {
 constexpr int kT = 512;                 // threads per CTA
 constexpr int kW = kT / 32;             // warps per CTA
 constexpr int kMaxRows = 256;           // rows the slice kernel takes
-constexpr int kMaxSlices = 256;         // slices per row
+constexpr int kMaxSlices = 128;         // slices per row
 constexpr int kSPL = kMaxSlices / 32;   // slices per lane when finishing
 constexpr int kSketch = 8;              // lane maxima a truncated unit exposes
 constexpr int kLCap = 16;               // list entries one record holds
-constexpr int kCandCap = 256;           // a finishing warp's candidate buffer
 constexpr int kKCap = 128;              // largest top-k the lists settle
 constexpr int kReCap = 16;              // slices a finishing warp may read again
+constexpr int kRankSortMax = 256;       // candidates sorted by counting ranks (more: bitonic)
+constexpr int kOneRoundRoom = 192;      // candidate words a one-round finish keeps free after the lists
 constexpr int kSlotBytes = 10240;       // a warp's staging slot
 constexpr int kMinUnit = 2048;          // smallest unit, in elements (unless the row is narrower)
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
@@ -126,8 +127,8 @@ struct alignas(16) RowInfo {
 };
 
 struct alignas(16) WarpScratch {
-    unsigned long long cand[kCandCap];  // candidates of a row being finished
-    uint32_t hist[256];                 // bins of the k-th key search
+    uint16_t q[kSlotBytes / 16];        // plain units: vectors the cheap bound let through
+    uint4 qw[2 * 32];                   // Philox words of the first 32 queued vectors
     uint32_t n;                         // candidates listed
     uint32_t nre;                       // slices to read again
     uint16_t re[kReCap];
@@ -178,18 +179,60 @@ template <>
 struct Vec<uint16_t> {
     static constexpr int E = 8;
     __device__ static __forceinline__ float get(const uint4& r, int e) { return ElemTraits<uint16_t>::get(r, e); }
-    // maximum (NaN ignored) and whether a NaN is present
-    __device__ static __forceinline__ float vmax(const uint4& r, bool& nan)
+    // running maximum in packed form, NaN-propagating (four bf16x2 lanes)
+    __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+    using Acc = uint4;
+    __device__ static __forceinline__ Acc acc_init() { return neg_inf(); }
+    __device__ static __forceinline__ uint32_t hmax_nan(uint32_t a, uint32_t b)
     {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
-        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&r.z);
-        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&r.w);
-        const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
-        const __nv_bfloat162 mn = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
-        const float n0 = __low2float(mn), n1 = __high2float(mn);
-        nan = (n0 != n0) || (n1 != n1);
-        return fmaxf(__low2float(m), __high2float(m));
+        const __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                             *reinterpret_cast<const __nv_bfloat162*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    __device__ static __forceinline__ void acc_add(Acc& a, const uint4& v)
+    {
+        a.x = hmax_nan(a.x, v.x);
+        a.y = hmax_nan(a.y, v.y);
+        a.z = hmax_nan(a.z, v.z);
+        a.w = hmax_nan(a.w, v.w);
+    }
+    // the maximum, or NaN when one was seen
+    __device__ static __forceinline__ float acc_max(const Acc& a)
+    {
+        const uint32_t m = hmax_nan(hmax_nan(a.x, a.y), hmax_nan(a.z, a.w));
+        const float lo = __uint_as_float(m << 16), hi = __uint_as_float(m & 0xFFFF0000u);
+        return (lo != lo || hi != hi) ? __uint_as_float(0x7FFFFFFFu) : fmaxf(lo, hi);
+    }
+    __device__ static __forceinline__ __nv_bfloat162 bf2(uint32_t w)
+    {
+        __nv_bfloat162 r;
+        memcpy(&r, &w, 4);
+        return r;
+    }
+    // whether some element equals m (a non-NaN bf16 value; -0 equals +0)
+    __device__ static __forceinline__ bool has(const uint4& v, float m)
+    {
+        const __nv_bfloat162 m2 = __float2bfloat162_rn(m);
+        return (__heq2_mask(bf2(v.x), m2) | __heq2_mask(bf2(v.y), m2) | __heq2_mask(bf2(v.z), m2) |
+                __heq2_mask(bf2(v.w), m2)) != 0u;
+    }
+    // elements >= t (a bf16 value), as two 16-bit counts in one word: add the
+    // words of up to 16383 vectors, then fold them with count_fold
+    using Thr = __nv_bfloat162;
+    __device__ static __forceinline__ Thr thr(float t) { return __float2bfloat162_rn(t); }
+    __device__ static __forceinline__ uint32_t count_ge(const uint4& v, Thr t2)
+    {
+        return (__hge2_mask(bf2(v.x), t2) & 0x10001u) + (__hge2_mask(bf2(v.y), t2) & 0x10001u) +
+               (__hge2_mask(bf2(v.z), t2) & 0x10001u) + (__hge2_mask(bf2(v.w), t2) & 0x10001u);
+    }
+    __device__ static __forceinline__ uint32_t count_fold(uint32_t c) { return (c & 0xFFFFu) + (c >> 16); }
+    // bit e set when element e >= t
+    __device__ static __forceinline__ uint32_t mask_ge(const uint4& v, Thr t2)
+    {
+        const uint32_t m0 = __hge2_mask(bf2(v.x), t2), m1 = __hge2_mask(bf2(v.y), t2);
+        const uint32_t m2 = __hge2_mask(bf2(v.z), t2), m3 = __hge2_mask(bf2(v.w), t2);
+        return ((m0 & 1u) | ((m0 >> 15) & 2u)) | (((m1 & 1u) | ((m1 >> 15) & 2u)) << 2) |
+               (((m2 & 1u) | ((m2 >> 15) & 2u)) << 4) | (((m3 & 1u) | ((m3 >> 15) & 2u)) << 6);
     }
 };
 
@@ -197,12 +240,43 @@ template <>
 struct Vec<float> {
     static constexpr int E = 4;
     __device__ static __forceinline__ float get(const uint4& r, int e) { return ElemTraits<float>::get(r, e); }
-    __device__ static __forceinline__ float vmax(const uint4& r, bool& nan)
+    __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+    using Acc = float4;
+    __device__ static __forceinline__ Acc acc_init() { return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY); }
+    __device__ static __forceinline__ float fmax_nan(float a, float b)
     {
-        const float a = __uint_as_float(r.x), b = __uint_as_float(r.y);
-        const float c = __uint_as_float(r.z), d = __uint_as_float(r.w);
-        nan = (a != a) || (b != b) || (c != c) || (d != d);
-        return fmaxf(fmaxf(a, b), fmaxf(c, d));
+        float r;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+        return r;
+    }
+    __device__ static __forceinline__ void acc_add(Acc& a, const uint4& v)
+    {
+        a.x = fmax_nan(a.x, __uint_as_float(v.x));
+        a.y = fmax_nan(a.y, __uint_as_float(v.y));
+        a.z = fmax_nan(a.z, __uint_as_float(v.z));
+        a.w = fmax_nan(a.w, __uint_as_float(v.w));
+    }
+    __device__ static __forceinline__ float acc_max(const Acc& a)
+    {
+        return fmax_nan(fmax_nan(a.x, a.y), fmax_nan(a.z, a.w));
+    }
+    __device__ static __forceinline__ bool has(const uint4& v, float m)
+    {
+        return __uint_as_float(v.x) == m || __uint_as_float(v.y) == m || __uint_as_float(v.z) == m ||
+               __uint_as_float(v.w) == m;
+    }
+    using Thr = float;
+    __device__ static __forceinline__ Thr thr(float t) { return t; }
+    __device__ static __forceinline__ uint32_t count_ge(const uint4& v, Thr t)
+    {
+        return uint32_t(__uint_as_float(v.x) >= t) + uint32_t(__uint_as_float(v.y) >= t) +
+               uint32_t(__uint_as_float(v.z) >= t) + uint32_t(__uint_as_float(v.w) >= t);
+    }
+    __device__ static __forceinline__ uint32_t count_fold(uint32_t c) { return c; }
+    __device__ static __forceinline__ uint32_t mask_ge(const uint4& v, Thr t)
+    {
+        return uint32_t(__uint_as_float(v.x) >= t) | (uint32_t(__uint_as_float(v.y) >= t) << 1) |
+               (uint32_t(__uint_as_float(v.z) >= t) << 2) | (uint32_t(__uint_as_float(v.w) >= t) << 3);
     }
 };
 

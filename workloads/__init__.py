@@ -18,6 +18,10 @@ The five named workloads stand in for the LM-head outputs the pages measured
 * ``penalties`` N=128, V=128000 fp32 logits ~ 2*N(0,1); per row 0..4096 prior ids
                 drawn Zipf(1.2) over V; presence 0.5, frequency 0.3, repetition 1.1,
                 min_p 0.05, T=1.0; fp32 probs and logprobs returned.
+* ``ablation_*`` the per-family ablation at N=64, V=128000 bf16 (the mixed
+                logits, every row T=1.0): plain, then + top_k=50 and top_p=0.9,
+                then + min_p=0.05, then + presence / frequency / repetition
+                penalties over Zipf(1.2) histories.
 * ``forks``     256 base rows x V=256000 bf16 logits ~ 2*Student-t(3); per base row
                 T ~ U[0,1.5] (10% exactly 0), top_k in {-1,20,50,1000}, top_p ~
                 U[0.5,1], min_p in {0,0.05}, 25% seeded with a u64 seed; each base row
@@ -43,6 +47,8 @@ __all__ = [
     "penalties",
     "forks",
     "random_batch",
+    "ablation",
+    "ABLATION_STAGES",
     "WORKLOADS",
     "make",
 ]
@@ -267,6 +273,35 @@ def random_batch(seed: int, n: int, v: int, dtype: str = "f32", *, stride_pad: i
     return b
 
 
+ABLATION_STAGES = ("plain", "topkp", "minp", "penalties")
+
+
+def ablation(stage: str, seed: int = 2, n: int = 64, v: int = 128000, max_hist: int = 4096) -> SamplerBatch:
+    """The per-family ablation at N=64, V=128000 bf16 (the mixed workload's logits):
+    every row T=1.0; ``topkp`` adds top_k=50 and top_p=0.9; ``minp`` also
+    min_p=0.05; ``penalties`` also presence 0.5, frequency 0.3, repetition 1.1
+    over a 0..4096-token Zipf(1.2) history per row."""
+    if stage not in ABLATION_STAGES:
+        raise ValueError(stage)
+    base = mixed(seed, n, v)
+    ones = np.ones(n)
+    kw = {}
+    upto = ABLATION_STAGES.index(stage)
+    if upto >= 1:
+        kw.update(top_k=np.full(n, 50, np.int32), top_p=_f32(0.9 * ones))
+    if upto >= 2:
+        kw.update(min_p=_f32(0.05 * ones))
+    if upto >= 3:
+        rng = np.random.Generator(np.random.PCG64(seed + 100))
+        lens = rng.integers(0, max_hist + 1, size=n)
+        offs = np.zeros(n + 1, np.int32)
+        offs[1:] = np.cumsum(lens)
+        kw.update(presence=_f32(0.5 * ones), frequency=_f32(0.3 * ones), repetition=_f32(1.1 * ones),
+                  hist_offsets=offs, hist_ids=_zipf_ids(rng, int(offs[-1]), 1.2, v))
+    return SamplerBatch(f"ablation_{stage}", base.logits, "bf16", v, n, _f32(ones), notes={"stage": stage},
+                        **kw)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "mixed": mixed,
@@ -274,6 +309,10 @@ WORKLOADS = {
     "latency32": lambda: latency(32),
     "penalties": penalties,
     "forks": forks,
+    "ablation_plain": lambda: ablation("plain"),
+    "ablation_topkp": lambda: ablation("topkp"),
+    "ablation_minp": lambda: ablation("minp"),
+    "ablation_penalties": lambda: ablation("penalties"),
 }
 
 
