@@ -37,7 +37,7 @@ struct SliceWorkspace {
 constexpr int kSliceMaxRows = 256;
 constexpr int kSliceMaxSlices = 128;
 constexpr size_t kSliceHdrBytes = 16;
-constexpr size_t kSliceBodyBytes = 192;
+constexpr size_t kSliceBodyBytes = 448;
 constexpr int kSliceCntStride = 32;  // 32-bit words between two rows' counters
 
 // True when this library's kernels load on the current device.

@@ -57,7 +57,10 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     ri.do_minp = ri.minp > 0.0f;
     ri.need_z = ri.do_topp && !ri.do_topk;
     ri.m = uint8_t(ri.do_topk ? min(ri.k, kSketch) : kSketch);
-    ri.pad0 = ri.pad1 = 0;
+    // the list threshold: the k-th largest lane maximum on a top-k row with
+    // k <= kKComplete (the list then holds the unit's top k), else the m-th
+    ri.mt = uint8_t(ri.do_topk && ri.k <= kKComplete ? ri.k : ri.m);
+    ri.pad1 = 0;
     if (bad) ri.cls = kClsErr;
     else if (greedy) ri.cls = kClsGreedy;
     else if (!ri.do_topk && !ri.do_topp && !ri.do_minp) ri.cls = kClsPlain;
@@ -335,7 +338,7 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
 // ---------------------------------------------------------------- truncated unit
 template <typename InT>
 __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowInfo& ri, SliceHdr& hdr_out,
-                                           SliceBody* body)
+                                           SliceBody* body, uint32_t* q)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -344,51 +347,68 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     uint32_t flags;
     unit_max<InT>(sv, mx, amax, flags, lm);
     SLC_MARK(4);
-    // the sketch: the m largest lane maxima (order keys, descending); tau is the
-    // smallest of them, so at least m tokens reach tau
+    // the sketch: the m largest lane maxima (order keys, descending), from each
+    // lane's rank among the 32 (ties by lane); tau, the mt-th largest (or the
+    // smallest finite one), so that at least mt tokens reach it
     const uint32_t lkey = lm > -INFINITY ? f2key(lm) : 0u;
-    uint32_t left = lkey, tau = 0, m = 0;
-#pragma unroll 1
-    for (int q = 0; q < int(ri.m); ++q) {
-        const uint32_t top = __reduce_max_sync(0xffffffffu, left);
-        if (top == 0) break;
-        tau = top;
-        if (lane == 0) body->sketch[q] = top;
-        ++m;
-        const uint32_t holder = __ballot_sync(0xffffffffu, left == top);
-        if (lane == __ffs(holder) - 1) left = 0;
+    uint32_t rank = 0;
+#pragma unroll
+    for (int o = 0; o < 32; ++o) {
+        const uint32_t ok = __shfl_sync(0xffffffffu, lkey, o);
+        rank += (ok > lkey || (ok == lkey && o < lane)) ? 1u : 0u;
     }
+    const uint32_t nfin = __popc(__ballot_sync(0xffffffffu, lkey != 0u));
+    const uint32_t m = min(uint32_t(ri.m), nfin);
+    if (lkey != 0u && rank < m) body->sketch[rank] = lkey;
+    const uint32_t tr = min(uint32_t(ri.mt), nfin);
+    const uint32_t at = __ballot_sync(0xffffffffu, tr > 0u && rank == tr - 1u);
+    uint32_t tau = at ? __shfl_sync(0xffffffffu, lkey, __ffs(at) - 1) : 0u;
     tau = max(tau, 1u);  // -inf (key 0 here) is never listed
     SLC_MARK(17);
     // list every finite token whose key reaches tau (x >= t as floats, -0 and
-    // +0 alike, as the keys): only lanes whose maximum reaches it hold any
+    // +0 alike, as the keys): one pass queues the vectors holding any (only
+    // lanes whose maximum reaches tau can) with their bit masks, in order; the
+    // list is then written from the queue, a vector per lane
     const float t = key2f(tau);
     const typename Vec<InT>::Thr t2 = Vec<InT>::thr(t);
-    uint32_t mine = 0;
-    if (lkey >= tau) {
-#pragma unroll 2
-        for (int j = lane; j < sv.nvec; j += 32) mine += Vec<InT>::count_ge(sv.vec(j), t2);
-        mine = Vec<InT>::count_fold(mine);
+    uint32_t total = 0;
+    int nq = 0;
+#pragma unroll 1
+    for (int j0 = 0; j0 < sv.nvec; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t hit = (j < sv.nvec && lkey >= tau) ? Vec<InT>::mask_ge(sv.vec(j), t2) : 0u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, hit != 0u);
+        const int at = nq + __popc(bal & ((1u << lane) - 1u));
+        if (hit && at < kTQCap) q[at] = (uint32_t(j) << 8) | hit;
+        nq += __popc(bal);
+        total += __reduce_add_sync(0xffffffffu, uint32_t(__popc(hit)));
     }
     SLC_MARK(18);
-    uint32_t incl = mine;
+    if (total <= uint32_t(kLCap)) {  // else the list is not kept (overflow)
+        __syncwarp();
+        uint32_t base = 0;
+#pragma unroll 1
+        for (int i0 = 0; i0 < nq; i0 += 32) {
+            const int i = i0 + lane;
+            const uint32_t w = i < nq ? q[i] : 0u;
+            const uint32_t c = __popc(w & 255u);
+            uint32_t incl = c;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    uint32_t pos = incl - mine;
-    if (mine && pos < uint32_t(kLCap)) {
-#pragma unroll 1
-        for (int j = lane; j < sv.nvec && pos < uint32_t(kLCap); j += 32) {
-            const uint4 v = sv.vec(j);
-#pragma unroll 1
-            for (uint32_t hit = Vec<InT>::mask_ge(v, t2); hit; hit &= hit - 1u) {
-                const int e = __ffs(hit) - 1;
-                if (pos < uint32_t(kLCap)) body->list[pos] = cand_word(f2key(Vec<InT>::get(v, e)), sv.c0 + j * E + e);
-                ++pos;
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
             }
+            uint32_t pos = base + incl - c;
+            if (c) {
+                const int j = int(w >> 8);
+                const uint4 v = sv.vec(j);
+#pragma unroll 1
+                for (uint32_t hit = w & 255u; hit; hit &= hit - 1u) {
+                    const int e = __ffs(hit) - 1;
+                    body->list[pos++] = cand_word(f2key(Vec<InT>::get(v, e)), sv.c0 + j * E + e);
+                }
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
     SLC_MARK(19);
@@ -888,13 +908,8 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
     SliceHdr* hs = reinterpret_cast<SliceHdr*>(scratch);            // [G]
     uint4* meta = reinterpret_cast<uint4*>(scratch + size_t(G) * 16);  // [G]
     uint32_t* sk = reinterpret_cast<uint32_t*>(scratch + size_t(G) * 32);  // [G][kSketch]
-    // with few slices every list comes in the first round too (after the
-    // sketches), and the candidates are gathered from there; otherwise the
-    // second round brings the lists that matter over the sketches
-    const bool one_round = false;
-    unsigned long long* lists = reinterpret_cast<unsigned long long*>(scratch + size_t(G) * 64);  // [G][kLCap]
-    unsigned long long* area = one_round ? lists : reinterpret_cast<unsigned long long*>(sk);
-    const int cap = int((size_t(kSlotBytes) - size_t(one_round ? 64 : 32) * G) / 8);
+    unsigned long long* area = reinterpret_cast<unsigned long long*>(sk);  // the lists, over the sketches
+    const int cap = int((size_t(kSlotBytes) - size_t(32) * G) / 8);
     // round 1
 #pragma unroll 1
     for (int b = lane; b < G; b += 32) {
@@ -902,13 +917,6 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
         cp_async16(meta + b, &bd[b].tau);
         cp_async16(sk + b * kSketch, &bd[b].sketch[0]);
         cp_async16(sk + b * kSketch + 4, &bd[b].sketch[4]);
-    }
-    if (one_round) {
-#pragma unroll 1
-        for (int i = lane; i < G * (kLCap / 2); i += 32) {
-            const int b = i / (kLCap / 2), e = 2 * (i - b * (kLCap / 2));
-            cp_async16(lists + b * kLCap + e, &bd[b].list[e]);
-        }
     }
     cp_async_commit_wait();
     __syncwarp();
@@ -953,48 +961,20 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
     B = max(B, 1u);
     SLC_MARK(8);
     __syncwarp();
-    // round 2 (or a gather from the staged lists): the lists of the slices that
-    // reach B and are complete above it, side by side; the others are read
-    // again below
+    // round 2: the lists of the slices that reach B and are complete above it
+    // (or, on a top-k row with k <= kKComplete, complete for the row's top k),
+    // side by side; the others are read again below
+    const bool topk_complete = ri.do_topk && ri.k <= kKComplete;
     uint32_t total = 0, nre = 0;
-    if (one_round) {
-        // in place: an entry only moves down
 #pragma unroll 1
-        for (int i0 = 0; i0 < G * kLCap; i0 += 32) {
-            const int i = i0 + lane;
-            const int b = i / kLCap, e = i - b * kLCap;
-            bool keep = false, again = false;
-            unsigned long long w = 0ull;
-            if (i < G * kLCap) {
-                const SliceHdr h = hs[b];
-                if (h.mx > -INFINITY && f2key(h.mx) >= B) {
-                    if (h.n == kOverflow || meta[b].x > B) again = e == 0;
-                    else if (uint32_t(e) < h.n) {
-                        w = lists[i];
-                        keep = cand_key(w) >= B;
-                    }
-                }
-            }
-            const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-            __syncwarp();
-            if (keep) area[total + __popc(bal & ((1u << lane) - 1u))] = w;
-            total += __popc(bal);
-            const uint32_t who = __ballot_sync(0xffffffffu, again);
-            const uint32_t at = nre + __popc(who & ((1u << lane) - 1u));
-            if (again && at < uint32_t(kReCap)) ws.re[at] = uint16_t(b);
-            nre += __popc(who);
-            __syncwarp();
-        }
-    }
-#pragma unroll 1
-    for (int c0 = 0; c0 < (one_round ? 0 : G); c0 += 32) {
+    for (int c0 = 0; c0 < G; c0 += 32) {
         const int b = c0 + lane;
         uint32_t n = 0;
         bool again = false;
         if (b < G) {
             const SliceHdr h = hs[b];
             if (h.mx > -INFINITY && f2key(h.mx) >= B) {
-                if (h.n == kOverflow || meta[b].x > B) again = true;
+                if (h.n == kOverflow || (meta[b].x > B && !topk_complete)) again = true;
                 else n = h.n;
             }
         }
@@ -1018,7 +998,7 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
     cp_async_commit_wait();
     __syncwarp();
     if (total > uint32_t(cap) || nre > uint32_t(kReCap)) return false;
-    int C = one_round ? int(total) : compact_ge(area, int(total), B);
+    int C = compact_ge(area, int(total), B);
     SLC_MARK(9);
     if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap);
     SLC_MARK(10);
@@ -1267,7 +1247,7 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
         } else if (ri.cls == kClsPlain) {
             unit_plain<InT>(sv, ri, off_lo, off_hi, q, qw, g, hdr.flags);
         } else {
-            unit_trunc<InT>(sv, ri, hdr, body);
+            unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
         }
     }
     hdr.flags |= extra;

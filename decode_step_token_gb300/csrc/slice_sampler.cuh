@@ -64,11 +64,12 @@ constexpr int kMaxRows = 256;           // rows the slice kernel takes
 constexpr int kMaxSlices = 128;         // slices per row
 constexpr int kSPL = kMaxSlices / 32;   // slices per lane when finishing
 constexpr int kSketch = 8;              // lane maxima a truncated unit exposes
-constexpr int kLCap = 16;               // list entries one record holds
+constexpr int kLCap = 48;               // list entries one record holds
+constexpr int kKComplete = 32;          // top-k rows up to this k list each unit's top k
+constexpr int kTQCap = 320;             // vectors a truncated unit queues (more: the list overflows)
 constexpr int kKCap = 128;              // largest top-k the lists settle
 constexpr int kReCap = 16;              // slices a finishing warp may read again
 constexpr int kRankSortMax = 256;       // candidates sorted by counting ranks (more: bitonic)
-constexpr int kOneRoundRoom = 192;      // candidate words a one-round finish keeps free after the lists
 constexpr int kSlotBytes = 10240;       // a warp's staging slot
 constexpr int kMinUnit = 2048;          // smallest unit, in elements (unless the row is narrower)
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
@@ -123,11 +124,12 @@ struct alignas(16) RowInfo {
     uint32_t stream, key_lo, key_hi;
     int32_t lrow;
     uint8_t cls, do_topk, do_topp, do_minp;
-    uint8_t need_z, m, pad0, pad1;
+    uint8_t need_z, m, mt, pad1;
 };
 
 struct alignas(16) WarpScratch {
-    uint16_t q[kSlotBytes / 16];        // plain units: vectors the cheap bound let through
+    uint16_t q[kSlotBytes / 16];        // plain units: vectors the cheap bound let through;
+                                        // truncated units: (vector << 8 | mask) words
     uint4 qw[2 * 32];                   // Philox words of the first 32 queued vectors
     uint32_t n;                         // candidates listed
     uint32_t nre;                       // slices to read again
@@ -156,6 +158,7 @@ constexpr size_t kSmemBytes = kHead + size_t(kW) * kSlotBytes;
 constexpr size_t kMaxSmem = 227 * 1024;
 static_assert(kSmemBytes <= kMaxSmem, "shared memory per CTA");
 static_assert(kSlotBytes >= 1024 * 8, "a free slot holds 1024 candidates");
+static_assert(kTQCap * 4 <= int(sizeof(WarpScratch::q)) && kTQCap > kLCap, "truncated-unit queue");
 
 // ---------------------------------------------------------------- small helpers
 __device__ __forceinline__ void warp_max_idx(float& m, int& i)

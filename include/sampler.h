@@ -207,7 +207,7 @@ int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_
  * Allocation-free sampling step. None of the pages has a counterpart: the
  * sampler they describe always owns its buffers. This entry point takes no
  * handle and allocates nothing. Its workspace (per-row arrival counters and
- * per-(row, slice) records, 3.3 MiB) is an array in the library's own device
+ * per-(row, slice) records, 3.6 MiB) is an array in the library's own device
  * memory, one copy per device. It runs the same kernel sampler_sample uses for
  * small batches and returns the same tokens. Every launch leaves the counters
  * at zero, and a row whose wait gave up (SAMPLER_ROW_TIMEOUT) leaves no state
