@@ -216,3 +216,55 @@ def sample(batch, rows: Optional[Sequence[int]] = None, want_probs: Optional[boo
     if rc != 0:
         raise RuntimeError(f"oracle_sample failed ({rc})")
     return OracleResult(tokens, status, diag, probs, logprobs)
+
+
+class LogprobOutputs:
+    """Per-row logprob outputs without the [N, V] tensors: the sampled token's
+    logprob, and the top_n tokens with theirs (ids -1 and logprob -inf past the
+    tokens the distribution gives any mass; NaN / -1 on error rows)."""
+
+    def __init__(self, token_logprob, top_ids, top_logprobs):
+        self.token_logprob = token_logprob
+        self.top_ids = top_ids
+        self.top_logprobs = top_logprobs
+
+
+def logprob_outputs(batch, result: OracleResult, top_n: int, unscaled: bool = False,
+                    rows: Optional[Sequence[int]] = None) -> LogprobOutputs:
+    """The logprobs a request gets back with its token (manual-sglang-101, "Logprobs
+    are temperature-scaled"): by default those of the distribution the row was
+    sampled from, log_softmax(x / T) over its kept set (T := 1 on greedy rows);
+    ``unscaled`` asks for log_softmax(x) over the whole vocabulary instead (the
+    page's original-logprob switch). x is the penalised fp32 row; the sums run in
+    double. The kept set is the one ``sample(..., want_probs=True)`` returned
+    (logprobs > -inf); ``result`` must come from such a call on the same rows.
+    The top_n order is (logprob desc, index asc)."""
+    idx = np.arange(batch.n_rows) if rows is None else np.asarray(rows)
+    n_out = len(idx)
+    tok = np.full(n_out, np.nan, np.float64)
+    ids = np.full((n_out, top_n), -1, np.int32)
+    lps = np.full((n_out, top_n), np.nan, np.float64)
+    for j, r in enumerate(idx):
+        if int(result.status[j]) != 0:
+            continue
+        _, x = penalized_logits(batch, int(r))
+        x = x.astype(np.float64)
+        if unscaled:
+            keep = x > -np.inf
+            T = 1.0
+        else:
+            keep = result.logprobs[j] > -np.inf
+            T = float(np.float32(batch.temperature[r]))
+            if T < 1e-5:
+                T = 1.0
+        y = np.where(keep, x / T, -np.inf)
+        ymax = y[keep].max()
+        lse = ymax + np.log(np.exp(y[keep] - ymax).sum())
+        lp = np.where(keep, y - lse, -np.inf)
+        tok[j] = lp[int(result.tokens[j])]
+        order = sorted(np.nonzero(keep)[0].tolist(), key=lambda v: (-x[v], v))[:top_n]
+        lps[j, :] = -np.inf
+        for q, v in enumerate(order):
+            ids[j, q] = v
+            lps[j, q] = lp[v]
+    return LogprobOutputs(tok, ids, lps)
