@@ -12,14 +12,15 @@ from typing import Optional
 
 from . import _binding as abi
 from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHORT_WAITS, SAMPLER_DTYPE_BF16,
-                       SAMPLER_DTYPE_F32, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK, load_library,
-                       sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
-                       sampler_destroy, sampler_sample, sampler_sample_host,
-                       sampler_sample_noalloc, sampler_status_string, sampler_get_stat)
+                       SAMPLER_DTYPE_F32, SAMPLER_MAX_TOP_N, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
+                       load_library, sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
+                       sampler_destroy, sampler_logprob_out_t, sampler_sample, sampler_sample_host,
+                       sampler_sample_logprobs, sampler_sample_noalloc, sampler_status_string,
+                       sampler_get_stat)
 
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
-           "sampler_sample_host", "sampler_sample_noalloc", "sampler_destroy",
-           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS",
+           "sampler_sample_host", "sampler_sample_noalloc", "sampler_sample_logprobs", "sampler_destroy",
+           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "sampler_logprob_out_t",
            "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
 
 
@@ -120,6 +121,21 @@ class Sampler:
 
     def sample(self, stream: Optional[int] = None, **kw) -> None:
         self.sample_args(self.make_args(**kw), stream)
+
+    def sample_logprobs_args(self, args: sampler_args_t, top_n: int = 0, unscaled: bool = False,
+                             out_token_logprob=None, out_top_ids=None, out_top_logprobs=None,
+                             stream: Optional[int] = None) -> None:
+        """sampler_sample_logprobs: the step plus per-row logprob outputs (device
+        tensors: out_token_logprob [N] fp32, out_top_ids / out_top_logprobs
+        [N, top_n] int32 / fp32)."""
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        lp = sampler_logprob_out_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob),
+                                   _ptr(out_top_ids), _ptr(out_top_logprobs))
+        rc = sampler_sample_logprobs(self._h, args, lp, stream)
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_sample_logprobs")
 
     def stat(self, which: int = 0, reset: bool = False) -> int:
         """A device diagnostic counter (synchronizes the device)."""

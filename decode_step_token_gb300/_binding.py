@@ -38,9 +38,10 @@ SAMPLER_CREATE_SHORT_WAITS = 4
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
             "sampler_status_string", "sampler_abi_version", "sampler_get_stat",
-            "sampler_sample_noalloc")
+            "sampler_sample_noalloc", "sampler_sample_logprobs")
 SAMPLER_STAT_EXACT_ROWS = 0
 SAMPLER_NOALLOC_MAX_ROWS = 64
+SAMPLER_MAX_TOP_N = 16
 
 
 class sampler_config_t(ctypes.Structure):
@@ -87,6 +88,16 @@ class sampler_args_t(ctypes.Structure):
     ]
 
 
+class sampler_logprob_out_t(ctypes.Structure):
+    _fields_ = [
+        ("top_n", ctypes.c_int32),
+        ("unscaled", ctypes.c_int32),
+        ("out_token_logprob", _P),
+        ("out_top_ids", _P),
+        ("out_top_logprobs", _P),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -115,6 +126,9 @@ def load_library(path: str = LIB):
             lib.sampler_get_stat.restype = ctypes.c_int
             lib.sampler_sample_noalloc.argtypes = [ctypes.POINTER(sampler_args_t), _P]
             lib.sampler_sample_noalloc.restype = ctypes.c_int
+            lib.sampler_sample_logprobs.argtypes = [_P, ctypes.POINTER(sampler_args_t),
+                                                    ctypes.POINTER(sampler_logprob_out_t), _P]
+            lib.sampler_sample_logprobs.restype = ctypes.c_int
             lib.sampler_abi_version.argtypes = []
             lib.sampler_abi_version.restype = ctypes.c_uint32
             _lib = lib
@@ -134,6 +148,12 @@ def sampler_sample(h, args: sampler_args_t, stream: int) -> int:
 
 def sampler_sample_host(h, args: sampler_args_t, stream: int) -> int:
     return load_library().sampler_sample_host(h, ctypes.byref(args), _P(stream))
+
+
+def sampler_sample_logprobs(h, args: sampler_args_t, lp, stream: int) -> int:
+    """lp: a sampler_logprob_out_t or None."""
+    return load_library().sampler_sample_logprobs(h, ctypes.byref(args), ctypes.byref(lp) if lp is not None else None,
+                                                  _P(stream))
 
 
 def sampler_sample_noalloc(args: sampler_args_t, stream: int) -> int:

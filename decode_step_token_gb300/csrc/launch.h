@@ -37,7 +37,7 @@ struct SliceWorkspace {
 constexpr int kSliceMaxRows = 256;
 constexpr int kSliceMaxSlices = 128;
 constexpr size_t kSliceHdrBytes = 16;
-constexpr size_t kSliceBodyBytes = 448;
+constexpr size_t kSliceBodyBytes = 464;
 constexpr int kSliceCntStride = 32;  // 32-bit words between two rows' counters
 
 // True when this library's kernels load on the current device.
@@ -51,8 +51,9 @@ bool slice_geometry(int64_t n_rows, int64_t vocab, int esize, int sms, SliceGeom
 int slice_prepare(int dtype, size_t smem);
 
 // Enqueue one slice-kernel launch. max_polls bounds each wait on a staging copy.
-int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWorkspace& ws, uint32_t max_polls,
-                 cudaStream_t stream);
+// lp: per-row logprob outputs (NULL: none)
+int slice_launch(const sampler_args_t* a, const sampler_logprob_out_t* lp, const SliceGeometry& g,
+                 const SliceWorkspace& ws, uint32_t max_polls, cudaStream_t stream);
 
 // ---------------------------------------------------------------- fork-group kernel
 // Everything the slice kernel does not take.

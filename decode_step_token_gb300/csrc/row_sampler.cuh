@@ -86,6 +86,12 @@ struct KernelParams {
     float* out_logprobs;
     int32_t* out_status;
     int32_t slice_len;  // elements per CTA, a multiple of 8
+    // per-row logprob outputs of sampler_sample_logprobs (slice kernel only)
+    float* out_tok_lp;
+    int32_t* out_top_ids;
+    float* out_top_lp;
+    int32_t top_n;
+    int32_t lp_unscaled;
 };
 
 // ------------------------------------------------------------------ records

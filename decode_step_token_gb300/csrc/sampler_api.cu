@@ -85,7 +85,9 @@ int launch_group(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
     return dst::group_launch(a, gg, h->grp_occ[slot], stream);
 }
 
-int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
+// lp: per-row logprob outputs, offered on the slice kernel only (the caller has
+// checked that the call takes it)
+int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const sampler_logprob_out_t* lp = nullptr)
 {
     dst::SliceGeometry g;
     if (slice_takes(a) && a->n_rows <= h->slice_rows &&
@@ -95,9 +97,18 @@ int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
             if (dst::slice_prepare(a->dtype, g.smem) != SAMPLER_OK) return SAMPLER_ERR_CUDA;
             h->slice_smem_set[slot] = g.smem;
         }
-        return dst::slice_launch(a, g, h->slice_ws, h->max_polls, stream);
+        return dst::slice_launch(a, lp, g, h->slice_ws, h->max_polls, stream);
     }
+    if (lp) return SAMPLER_ERR_UNSUPPORTED;
     return launch_group(h, a, stream);
+}
+
+// Whether a call with logprob outputs takes the slice kernel (host-visible facts).
+bool slice_would_take(sampler_t h, const sampler_args_t* a)
+{
+    dst::SliceGeometry g;
+    return slice_takes(a) && a->n_rows <= h->slice_rows &&
+           dst::slice_geometry(a->n_rows, a->vocab, esize_of(a->dtype), h->num_sms, &g);
 }
 
 int check_args(sampler_t h, const sampler_args_t* a)
@@ -194,7 +205,7 @@ int noalloc_grant_smem(int dev, int dtype, size_t smem)
 
 extern "C" {
 
-uint32_t sampler_abi_version(void) { return (1u << 16) | 1u; }
+uint32_t sampler_abi_version(void) { return (1u << 16) | 2u; }
 
 int sampler_get_stat(sampler_t h, int which, uint64_t* value, int reset)
 {
@@ -306,6 +317,23 @@ int sampler_sample(sampler_t h, const sampler_args_t* a, sampler_stream_t stream
     return launch(h, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int sampler_sample_logprobs(sampler_t h, const sampler_args_t* a, const sampler_logprob_out_t* lp,
+                            sampler_stream_t stream)
+{
+    int rc = check_args(h, a);
+    if (rc != SAMPLER_OK) return rc;
+    if (lp) {
+        if (lp->top_n < 0 || lp->top_n > SAMPLER_MAX_TOP_N) return SAMPLER_ERR_UNSUPPORTED;
+        if (lp->top_n > 0 && (!lp->out_top_ids || !lp->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
+        if (!lp->out_token_logprob && lp->top_n == 0) lp = nullptr;  // nothing asked
+    }
+    if (a->n_rows == 0) return SAMPLER_OK;
+    DeviceGuard guard;
+    if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    if (lp && !slice_would_take(h, a)) return SAMPLER_ERR_UNSUPPORTED;
+    return launch(h, a, reinterpret_cast<cudaStream_t>(stream), lp);
+}
+
 int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
 {
     if (!a) return SAMPLER_ERR_NULL_ARG;
@@ -333,7 +361,7 @@ int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
     ws.hdr = d.scratch + kNoAllocCounterBytes;
     ws.body = d.scratch + kNoAllocCounterBytes + kNoAllocHdrBytes;
     ws.stats = nullptr;
-    return dst::slice_launch(a, g, ws, kMaxPolls, stream);
+    return dst::slice_launch(a, nullptr, g, ws, kMaxPolls, stream);
 }
 
 int sampler_sample_host(sampler_t h, const sampler_args_t* a, sampler_stream_t stream_)

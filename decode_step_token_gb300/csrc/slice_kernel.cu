@@ -69,8 +69,8 @@ int slice_prepare(int dtype, size_t smem)
     return SAMPLER_OK;
 }
 
-int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWorkspace& ws, uint32_t max_polls,
-                 cudaStream_t stream)
+int slice_launch(const sampler_args_t* a, const sampler_logprob_out_t* lp, const SliceGeometry& g,
+                 const SliceWorkspace& ws, uint32_t max_polls, cudaStream_t stream)
 {
     slc::SliceParams p;
     std::memset(&p, 0, sizeof p);
@@ -95,6 +95,13 @@ int slice_launch(const sampler_args_t* a, const SliceGeometry& g, const SliceWor
     k.philox_offset_dev = a->philox_offset_dev;
     k.out_tokens = a->out_tokens;
     k.out_status = a->out_status;
+    if (lp) {
+        k.out_tok_lp = lp->out_token_logprob;
+        k.top_n = lp->top_n;
+        k.out_top_ids = lp->top_n > 0 ? lp->out_top_ids : nullptr;
+        k.out_top_lp = lp->top_n > 0 ? lp->out_top_logprobs : nullptr;
+        k.lp_unscaled = lp->unscaled ? 1 : 0;
+    }
     p.n_rows = int(a->n_rows);
     p.G = g.G;
     p.W = g.W;

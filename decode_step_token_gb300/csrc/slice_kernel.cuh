@@ -60,11 +60,20 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     // the list threshold: the k-th largest lane maximum on a top-k row with
     // k <= kKComplete (the list then holds the unit's top k), else the m-th
     ri.mt = uint8_t(ri.do_topk && ri.k <= kKComplete ? ri.k : ri.m);
-    ri.pad1 = 0;
+    ri.greedy = greedy ? 1 : 0;
+    const bool trunc = ri.do_topk || ri.do_topp || ri.do_minp;
+    ri.lp = (kp.out_tok_lp != nullptr || kp.top_n > 0) ? 1 : 0;
     if (bad) ri.cls = kClsErr;
-    else if (greedy) ri.cls = kClsGreedy;
-    else if (!ri.do_topk && !ri.do_topp && !ri.do_minp) ri.cls = kClsPlain;
+    else if (greedy) ri.cls = (ri.lp && trunc) ? kClsTrunc : kClsGreedy;  // outputs over the kept set at T := 1
+    else if (!trunc) ri.cls = kClsPlain;
     else ri.cls = kClsTrunc;
+    // the logprob outputs: over the kept set at T (scaled, truncated rows: from
+    // the finisher's candidates), else over the whole row at T_out, from masses
+    // the units keep; every unit lists at least its top n
+    ri.s2o = kp.lp_unscaled ? 1.4426950408889634f : ri.s2;
+    ri.need_zo = (ri.lp && (kp.lp_unscaled || ri.cls != kClsTrunc)) ? 1 : 0;
+    if (ri.lp && kp.top_n > 0) ri.mt = uint8_t(max(int(ri.mt), kp.top_n));
+    ri.pad2 = ri.pad3 = 0;
     return ri;
 }
 
@@ -336,6 +345,34 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
 }
 
 // ---------------------------------------------------------------- truncated unit
+// Sum over the unit of exp2((x - mx) * s2) (Kahan per lane, double across the
+// warp), as a high and a low fp32 part.
+template <typename InT>
+__device__ __noinline__ void unit_mass(const SliceView<InT>& sv, float mx, float s2, float& hi, float& lo)
+{
+    constexpr int E = Vec<InT>::E;
+    const int lane = threadIdx.x & 31;
+    float zs = 0.0f, zc = 0.0f;  // Kahan: the sum is zs - zc
+#pragma unroll 1
+    for (int j = lane; j < sv.nvec; j += 32) {
+        const uint4 v = sv.vec(j);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float x = Vec<InT>::get(v, e);
+            if (!(x > -INFINITY)) continue;
+            const float term = exp2f((x - mx) * s2) - zc;
+            const float sum = zs + term;
+            zc = (sum - zs) - term;
+            zs = sum;
+        }
+    }
+    double z = double(zs) - double(zc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    hi = float(z);
+    lo = float(z - double(hi));
+}
+
 template <typename InT>
 __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowInfo& ri, SliceHdr& hdr_out,
                                            SliceBody* body, uint32_t* q)
@@ -348,8 +385,8 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     unit_max<InT>(sv, mx, amax, flags, lm);
     SLC_MARK(4);
     // the sketch: the m largest lane maxima (order keys, descending), from each
-    // lane's rank among the 32 (ties by lane); tau, the mt-th largest (or the
-    // smallest finite one), so that at least mt tokens reach it
+    // lane's rank among the 32 (ties by lane); tau, the mt-th largest, so that at
+    // least mt tokens reach it and the unit's mt largest all do
     const uint32_t lkey = lm > -INFINITY ? f2key(lm) : 0u;
     uint32_t rank = 0;
 #pragma unroll
@@ -360,8 +397,9 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     const uint32_t nfin = __popc(__ballot_sync(0xffffffffu, lkey != 0u));
     const uint32_t m = min(uint32_t(ri.m), nfin);
     if (lkey != 0u && rank < m) body->sketch[rank] = lkey;
-    const uint32_t tr = min(uint32_t(ri.mt), nfin);
-    const uint32_t at = __ballot_sync(0xffffffffu, tr > 0u && rank == tr - 1u);
+    // (a unit with fewer finite lane maxima than mt lists every finite token: only
+    // then is its list sure to hold its top mt)
+    const uint32_t at = __ballot_sync(0xffffffffu, nfin >= uint32_t(ri.mt) && rank == uint32_t(ri.mt) - 1u);
     uint32_t tau = at ? __shfl_sync(0xffffffffu, lkey, __ffs(at) - 1) : 0u;
     tau = max(tau, 1u);  // -inf (key 0 here) is never listed
     SLC_MARK(17);
@@ -369,7 +407,7 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     // +0 alike, as the keys): one pass queues the vectors holding any (only
     // lanes whose maximum reaches tau can) with their bit masks, in order; the
     // list is then written from the queue, a vector per lane
-    const float t = key2f(tau);
+    const float t = tau < 0x00800000u ? -FLT_MAX : key2f(tau);  // x >= t: finite and key >= tau
     const typename Vec<InT>::Thr t2 = Vec<InT>::thr(t);
     uint32_t total = 0;
     int nq = 0;
@@ -412,31 +450,23 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
         }
     }
     SLC_MARK(19);
-    // top-p rows without top-k: the unit's softmax mass at its maximum
+    // top-p rows without top-k: the unit's softmax mass at its maximum (at T);
+    // logprob outputs over the whole row: the same at the outputs' temperature
     float zsum = 0.0f, zlow = 0.0f;
-    if (ri.need_z && mx > -INFINITY && mx < INFINITY) {
-        float zs = 0.0f, zc = 0.0f;  // Kahan: the sum is zs - zc
-#pragma unroll 1
-        for (int j = lane; j < sv.nvec; j += 32) {
-            const uint4 v = sv.vec(j);
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float x = Vec<InT>::get(v, e);
-                if (!(x > -INFINITY)) continue;
-                const float term = exp2f((x - mx) * ri.s2) - zc;
-                const float sum = zs + term;
-                zc = (sum - zs) - term;
-                zs = sum;
-            }
-        }
-        double z = double(zs) - double(zc);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-        zsum = float(z);
-        zlow = float(z - double(zsum));
-    }
+    const bool fin = mx > -INFINITY && mx < INFINITY;
+    if (ri.need_z && fin) unit_mass<InT>(sv, mx, ri.s2, zsum, zlow);
     if (lane == 0)
         *reinterpret_cast<uint4*>(&body->tau) = make_uint4(tau, __float_as_uint(zsum), __float_as_uint(zlow), m);
+    if (ri.need_zo) {
+        float os = 0.0f, ol = 0.0f;
+        if (ri.need_z && ri.s2o == ri.s2) {
+            os = zsum;
+            ol = zlow;
+        } else if (fin) {
+            unit_mass<InT>(sv, mx, ri.s2o, os, ol);
+        }
+        if (lane == 0) *reinterpret_cast<uint4*>(&body->zos) = make_uint4(__float_as_uint(os), __float_as_uint(ol), 0u, 0u);
+    }
     hdr_out.mx = mx;
     hdr_out.amax = amax;
     hdr_out.flags = flags;
@@ -500,7 +530,7 @@ __device__ __forceinline__ int pick_of(const KernelParams& kp, const RowInfo& ri
     return (da > db || (da == db && ia < ib)) ? ia : ib;
 }
 
-__device__ __forceinline__ void finish_greedy(const SliceParams& P, int r)
+__device__ __forceinline__ void finish_greedy(const SliceParams& P, int r, int& tok, int32_t& st)
 {
     const int lane = threadIdx.x & 31;
     const SliceHdr* hd = P.hdr + size_t(r) * P.G;
@@ -518,12 +548,14 @@ __device__ __forceinline__ void finish_greedy(const SliceParams& P, int r)
     }
     fl = warp_or(fl);
     warp_max_idx(m, mi);
-    if (lane == 0) write_out(P.k, r, mi, status_of(fl));
+    st = status_of(fl);
+    tok = st ? -1 : mi;
+    if (lane == 0) write_out(P.k, r, mi, st);
 }
 
 template <typename InT>
 __device__ __forceinline__ void finish_plain(const SliceParams& P, const RowInfo& ri, int r, uint32_t off_lo,
-                                             uint32_t off_hi)
+                                             uint32_t off_hi, int& tok, int32_t& st_out)
 {
     const int lane = threadIdx.x & 31;
     const SliceHdr* hd = P.hdr + size_t(r) * P.G;
@@ -543,6 +575,8 @@ __device__ __forceinline__ void finish_plain(const SliceParams& P, const RowInfo
     int token = -1;
     if (!st) token = pick_of<InT>(P.k, ri, off_lo, off_hi, t);
     if (lane == 0) write_out(P.k, r, token, st);
+    tok = token;
+    st_out = st;
 }
 
 // The largest 16-bit prefix P with at least k keys >= P << 16 (so P << 16 is at
@@ -653,6 +687,41 @@ static __device__ __noinline__ float minp_threshold(float m, float T, float minp
     return t;
 }
 
+// ---- per-row logprob outputs
+constexpr float kLn2 = 0.6931471805599453f;
+
+// An error row: NaN logprobs, ids -1 (lane 0 and the first top_n lanes write).
+__device__ __forceinline__ void lp_write_error(const KernelParams& kp, int r)
+{
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && kp.out_tok_lp) kp.out_tok_lp[r] = __uint_as_float(0x7FC00000u);
+    if (lane < kp.top_n) {
+        kp.out_top_ids[size_t(r) * kp.top_n + lane] = -1;
+        kp.out_top_lp[size_t(r) * kp.top_n + lane] = __uint_as_float(0x7FC00000u);
+    }
+}
+
+// The outputs of row r from its sorted candidates (the first nc of `srt`, all
+// of them carrying mass), its maximum m, log2 of its mass lz2 (both at the
+// outputs' temperature, scale s2o) and the sampled token's logit xt.
+__device__ __forceinline__ void lp_write(const KernelParams& kp, int r, const unsigned long long* srt, int nc,
+                                         float m, float s2o, float lz2, float xt)
+{
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && kp.out_tok_lp) kp.out_tok_lp[r] = ((xt - m) * s2o - lz2) * kLn2;
+    if (lane < kp.top_n) {
+        int id = -1;
+        float lp = -INFINITY;
+        if (lane < nc) {
+            const unsigned long long c = srt[lane];
+            id = cand_idx(c);
+            lp = ((key2f(cand_key(c)) - m) * s2o - lz2) * kLn2;
+        }
+        kp.out_top_ids[size_t(r) * kp.top_n + lane] = id;
+        kp.out_top_lp[size_t(r) * kp.top_n + lane] = lp;
+    }
+}
+
 // Sort n words in warp-private shared memory, descending (bitonic through
 // shared memory, padded with zeros up to a power of two; the buffer holds it).
 static __device__ __noinline__ void warp_sort_smem(unsigned long long* a, int n)
@@ -730,7 +799,7 @@ __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v
 template <typename InT>
 static __device__ __noinline__ bool cut_and_pick(const SliceParams& P, const RowInfo& ri, int r, uint32_t off_lo,
                                                  uint32_t off_hi, const unsigned long long* cand, int C, float m,
-                                                 float xthr, const SliceHdr* hs, const uint4* meta)
+                                                 float xthr, const SliceHdr* hs, const uint4* meta, int& tok_out)
 {
     const int lane = threadIdx.x & 31;
     const int nk = ri.do_topk ? ri.k : C;
@@ -784,18 +853,42 @@ static __device__ __noinline__ bool cut_and_pick(const SliceParams& P, const Row
     }
     nkeep = max(nkeep, 1);
     SLC_MARK(14);
-    // Gumbel-max over the kept prefix
-    const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
-    K2 t{0ull, 0ull};
+    int token;
+    if (ri.greedy) {
+        token = cand_idx(cand[0]);  // a greedy row here only for its logprob outputs
+    } else {
+        // Gumbel-max over the kept prefix
+        const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
+        K2 t{0ull, 0ull};
 #pragma unroll 1
-    for (int i = lane; i < nkeep; i += 32) {
-        const unsigned long long c = cand[i];
-        const int v = cand_idx(c);
-        k2_insert(t, gkey(score2(key2f(cand_key(c)), ri.s2, philox_word(rp, v)), v));
+        for (int i = lane; i < nkeep; i += 32) {
+            const unsigned long long c = cand[i];
+            const int v = cand_idx(c);
+            k2_insert(t, gkey(score2(key2f(cand_key(c)), ri.s2, philox_word(rp, v)), v));
+        }
+        k2_warp_reduce(t);
+        token = pick_of<InT>(P.k, ri, off_lo, off_hi, t);
     }
-    k2_warp_reduce(t);
-    const int token = pick_of<InT>(P.k, ri, off_lo, off_hi, t);
     if (lane == 0) write_out(P.k, r, token, kRowOk);
+    tok_out = token;
+    if (ri.lp && !P.k.lp_unscaled) {
+        // the kept set's mass at the outputs' temperature, and the token's logit
+        double z = 0.0;
+        float xt = 0.0f;
+#pragma unroll 1
+        for (int i = lane; i < nkeep; i += 32) {
+            const unsigned long long c = cand[i];
+            const float x = key2f(cand_key(c));
+            z += double(exp2f((x - m) * ri.s2o));
+            if (cand_idx(c) == token) xt = x;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            z += __shfl_xor_sync(0xffffffffu, z, off);
+            xt += __shfl_xor_sync(0xffffffffu, xt, off);
+        }
+        lp_write(P.k, r, cand, min(nkeep, P.k.top_n), m, ri.s2o, log2f(float(z)), xt);
+    }
     return true;
 }
 
@@ -899,7 +992,7 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
 template <typename InT>
 static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
                                                  uint32_t off_lo, uint32_t off_hi, unsigned char* scratch,
-                                                 float& m_out)
+                                                 float& m_out, int& tok, int32_t& st_out)
 {
     const int lane = threadIdx.x & 31;
     const int G = P.G;
@@ -941,8 +1034,11 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
     warp_max_idx(m, mi);
     m_out = m;
     const int32_t st = status_of(fl);
+    st_out = st;
+    tok = -1;
     if (st) {
         if (lane == 0) write_out(P.k, r, -1, st);
+        if (ri.lp) lp_write_error(P.k, r);
         return true;
     }
     // the min-p threshold on the logit: m + T ln(min_p), rounded up to fp32
@@ -1020,7 +1116,118 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
         warp_sort_smem(area, C);
     }
     SLC_MARK(11);
-    return cut_and_pick<InT>(P, ri, r, off_lo, off_hi, sorted, C, m, xthr, hs, meta);
+    return cut_and_pick<InT>(P, ri, r, off_lo, off_hi, sorted, C, m, xthr, hs, meta, tok);
+}
+
+// The logprob outputs of row r over its whole vocabulary at the outputs'
+// temperature (untruncated rows, and every row when they are unscaled): the mass
+// from the units' records, the top n from their lists (each unit lists at least
+// its top n, so a list that did not overflow holds every token of the row's top
+// n in its slice). `token` is the sampled one; st its status.
+template <typename InT>
+static __device__ __noinline__ bool finish_lp_row(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
+                                                  int token, int32_t st, unsigned char* scratch, float& m_out)
+{
+    const int lane = threadIdx.x & 31;
+    const KernelParams& kp = P.k;
+    if (st) {
+        lp_write_error(kp, r);
+        return true;
+    }
+    const int G = P.G;
+    const int n = kp.top_n;
+    const SliceHdr* hd = P.hdr + size_t(r) * G;
+    const SliceBody* bd = P.body + size_t(r) * G;
+    SliceHdr* hs = reinterpret_cast<SliceHdr*>(scratch);                   // [G]
+    uint4* meta = reinterpret_cast<uint4*>(scratch + size_t(G) * 16);        // [G] (tau, zs, zc, m)
+    uint4* zo = reinterpret_cast<uint4*>(scratch + size_t(G) * 32);          // [G] (zos, zoc, -, -)
+    uint32_t* sk = reinterpret_cast<uint32_t*>(scratch + size_t(G) * 48);    // [G][kSketch]
+    unsigned long long* area = reinterpret_cast<unsigned long long*>(sk);  // the lists, over the sketches
+    const int cap = int((size_t(kSlotBytes) - size_t(48) * G) / 8);
+#pragma unroll 1
+    for (int b = lane; b < G; b += 32) {
+        cp_async16(hs + b, hd + b);
+        cp_async16(meta + b, &bd[b].tau);
+        cp_async16(zo + b, &bd[b].zos);
+        cp_async16(sk + b * kSketch, &bd[b].sketch[0]);
+        cp_async16(sk + b * kSketch + 4, &bd[b].sketch[4]);
+    }
+    cp_async_commit_wait();
+    __syncwarp();
+    float m = -INFINITY;
+    uint32_t nkeys = 0;
+#pragma unroll 1
+    for (int b = lane; b < G; b += 32) {
+        m = fmaxf(m, hs[b].mx);
+        nkeys += meta[b].w;
+    }
+    m = __shfl_sync(0xffffffffu, key2f(__reduce_max_sync(0xffffffffu, f2key(m))), 0);
+    m_out = m;
+    nkeys = __reduce_add_sync(0xffffffffu, nkeys);
+    double z = 0.0;
+#pragma unroll 1
+    for (int b = lane; b < G; b += 32) {
+        const float mx = hs[b].mx;
+        if (mx > -INFINITY)
+            z += (double(__uint_as_float(zo[b].x)) + double(__uint_as_float(zo[b].y))) *
+                 double(exp2f((mx - m) * ri.s2o));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    const float lz2 = log2f(float(z));
+    const float xt = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + token);
+    int C = 0;
+    if (n > 0) {
+        // B: the 16-bit prefix of the n-th largest sketch key (all listed tokens
+        // when the sketches hold fewer)
+        uint32_t B = nkeys >= uint32_t(n) ? sketch_bound(sk, meta, G, n) : 1u;
+        B = max(B, 1u);
+        __syncwarp();
+        uint32_t total = 0, nre = 0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < G; c0 += 32) {
+            const int b = c0 + lane;
+            uint32_t cnt = 0;
+            bool again = false;
+            if (b < G) {
+                const SliceHdr h = hs[b];
+                if (h.mx > -INFINITY && f2key(h.mx) >= B) {
+                    if (h.n == kOverflow) again = true;
+                    else cnt = h.n;
+                }
+            }
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const uint32_t pos = total + incl - cnt;
+            if (pos + cnt <= uint32_t(cap)) {
+#pragma unroll 1
+                for (uint32_t e = 0; e < cnt; ++e) cp_async8(area + pos + e, &bd[b].list[e]);
+            }
+            const uint32_t who = __ballot_sync(0xffffffffu, again);
+            const uint32_t at = nre + __popc(who & ((1u << lane) - 1u));
+            if (again && at < uint32_t(kReCap)) ws.re[at] = uint16_t(b);
+            nre += __popc(who);
+            total += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        cp_async_commit_wait();
+        __syncwarp();
+        bool ok = total <= uint32_t(cap) && nre <= uint32_t(kReCap);
+        if (ok) {
+            C = compact_ge(area, int(total), B);
+            if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap);
+            ok = C <= cap && 2 * C <= cap && C <= kRankSortMax;
+        }
+        if (!ok) return false;  // more candidates than the lists settle here (ties): the exact path
+        rank_sort(area, C, area + C, min(C, n));
+        area += C;
+        C = min(C, n);
+    }
+    lp_write(kp, r, area, C, m, ri.s2o, lz2, xt);
+    return true;
 }
 
 // ---------------------------------------------------------------- exact path (whole CTA)
@@ -1173,19 +1380,38 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
         if (double(f) < th) f = nextafterf(f, INFINITY);
         xthr = f;
     }
+    // the pick (greedy rows: the maximum, lowest index) and the kept set's mass
+    // and size at the outputs' temperature (logprob outputs over the kept set)
+    const bool lp_kept = ri.lp && !kp.lp_unscaled && ri.cls == kClsTrunc;
     const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
     K2 t{0ull, 0ull};
+    double z = 0.0;
+    uint32_t nk = 0;
     for (int v = tid; v < V; v += kT) {
         const float x = row_x<InT>(kp, ri.lrow, v);
         if (!(x > -INFINITY)) continue;
-        if (hb && !in_prefix(f2key(x), v, bk, bi)) continue;
-        if (ri.do_minp && !(x >= xthr)) continue;
-        k2_insert(t, gkey(score2(x, ri.s2, philox_word(rp, v)), v));
+        const bool kept = !(hb && !in_prefix(f2key(x), v, bk, bi)) && !(ri.do_minp && !(x >= xthr));
+        if (ri.lp && (kept || !lp_kept)) {
+            z += double(exp2f((x - m) * ri.s2o));
+            ++nk;
+        }
+        if (!kept) continue;
+        if (ri.greedy) k2_insert(t, cand_word(f2key(x), v));
+        else k2_insert(t, gkey(score2(x, ri.s2, philox_word(rp, v)), v));
     }
     k2_warp_reduce(t);
     if (lane == 0) {
         sh.red_k[2 * wid] = t.a;
         sh.red_k[2 * wid + 1] = t.b;
+    }
+    if (ri.lp) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+        nk = __reduce_add_sync(0xffffffffu, nk);
+        if (lane == 0) {
+            sh.red_d[wid] = z;
+            sh.red_i[wid] = int(nk);
+        }
     }
     __syncthreads();
     if (wid == 0) {
@@ -1195,11 +1421,55 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
             a.b = sh.red_k[2 * lane + 1];
         }
         k2_warp_reduce(a);
-        const int token = pick_of<InT>(kp, ri, off_lo, off_hi, a);
+        const int token = ri.greedy ? cand_idx(a.a) : pick_of<InT>(kp, ri, off_lo, off_hi, a);
         if (lane == 0) {
             write_out(kp, r, token, kRowOk);
             if (P.stats) atomicAdd(P.stats, 1ull);
+            sh.sel_idx = token;
         }
+    }
+    __syncthreads();
+    if (!ri.lp) return;
+    // logprob outputs: the first n of the kept set (or of the row) in (value desc,
+    // index asc) order, from the n-th of that order; the kept set is a prefix of it
+    double zt = 0.0;
+    int nkt = 0;
+    for (int w = 0; w < kW; ++w) {
+        zt += sh.red_d[w];
+        nkt += sh.red_i[w];
+    }
+    const int token = sh.sel_idx;
+    const int n = min(kp.top_n, nkt);
+    __syncthreads();
+    if (tid == 0) sh.lp_cnt = 0;
+    uint32_t nkey = 0;
+    int nidx = 0;
+    if (n > 0) cta_select<InT>(sh, kp, ri, V, false, false, 0u, 0, m, (unsigned long long)n, nkey, nidx);
+    __syncthreads();
+    if (n > 0) {
+        for (int v = tid; v < V; v += kT) {
+            const float x = row_x<InT>(kp, ri.lrow, v);
+            if (x > -INFINITY && in_prefix(f2key(x), v, nkey, nidx)) {
+                const int q = atomicAdd(&sh.lp_cnt, 1);
+                if (q < kMaxTopN) sh.lp_list[q] = cand_word(f2key(x), v);
+            }
+        }
+    }
+    __syncthreads();
+    if (wid == 0) {
+        // rank the (at most n) collected words: word `lane` goes to its rank
+        const int c = min(sh.lp_cnt, n);
+        unsigned long long w = 0ull;
+        int rank = 0;
+        if (lane < c) {
+            w = sh.lp_list[lane];
+            for (int j = 0; j < c; ++j) rank += sh.lp_list[j] > w ? 1 : 0;
+        }
+        __syncwarp();
+        if (lane < c) sh.lp_list[rank] = w;
+        __syncwarp();
+        const float xt = row_x<InT>(kp, ri.lrow, token);
+        lp_write(kp, r, sh.lp_list, c, m, ri.s2o, log2f(float(zt)), xt);
     }
     __syncthreads();
 }
@@ -1244,8 +1514,11 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
         if (ri.cls == kClsGreedy) {
             float lm;
             unit_max<InT>(sv, hdr.mx, hdr.amax, hdr.flags, lm);
+            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
         } else if (ri.cls == kClsPlain) {
             unit_plain<InT>(sv, ri, off_lo, off_hi, q, qw, g, hdr.flags);
+            __syncwarp();
+            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
         } else {
             unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
         }
@@ -1260,22 +1533,29 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
     }
 }
 
-// Finish row r (this warp's arrival completed it); scratch: the warp's idle
-// staging slot. Returns false when the row is left for the exact path.
+// Finish row r (this warp's arrival completed it), and its logprob outputs when
+// they are asked; scratch: the warp's idle staging slot. Returns false when the
+// row is left for the exact path (m: the row maximum).
 template <typename InT>
 __device__ __noinline__ bool finish_row(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
                                         uint32_t off_lo, uint32_t off_hi, unsigned char* scratch, float& m)
 {
     m = -INFINITY;
+    int tok = -1;
+    int32_t st = 0;
     if (ri.cls == kClsGreedy) {
-        finish_greedy(P, r);
-        return true;
+        finish_greedy(P, r, tok, st);
+    } else if (ri.cls == kClsPlain) {
+        finish_plain<InT>(P, ri, r, off_lo, off_hi, tok, st);
+    } else if (!finish_trunc<InT>(P, ws, ri, r, off_lo, off_hi, scratch, m, tok, st)) {
+        return false;
     }
-    if (ri.cls == kClsPlain) {
-        finish_plain<InT>(P, ri, r, off_lo, off_hi);
-        return true;
+    // outputs over the whole row (untruncated rows; every row when unscaled)
+    if (ri.lp && (P.k.lp_unscaled || ri.cls != kClsTrunc)) {
+        __syncwarp();
+        return finish_lp_row<InT>(P, ws, ri, r, tok, st, scratch, m);
     }
-    return finish_trunc<InT>(P, ws, ri, r, off_lo, off_hi, scratch, m);
+    return true;
 }
 
 // ---------------------------------------------------------------- the kernel

@@ -66,6 +66,7 @@ constexpr int kSPL = kMaxSlices / 32;   // slices per lane when finishing
 constexpr int kSketch = 8;              // lane maxima a truncated unit exposes
 constexpr int kLCap = 48;               // list entries one record holds
 constexpr int kKComplete = 32;          // top-k rows up to this k list each unit's top k
+constexpr int kMaxTopN = 16;            // largest top_n of the logprob outputs
 constexpr int kTQCap = 320;             // vectors a truncated unit queues (more: the list overflows)
 constexpr int kKCap = 128;              // largest top-k the lists settle
 constexpr int kReCap = 16;              // slices a finishing warp may read again
@@ -98,6 +99,9 @@ struct alignas(16) SliceBody {
     float zs;       // top-p rows without top-k: sum of exp((x - mx) / T) over the unit
     float zc;       // its low-order part (the sum is zs + zc)
     uint32_t m;     // entries of the sketch
+    float zos;      // logprob outputs over the whole row: sum of exp((x - mx) / T_out)
+    float zoc;      // its low-order part
+    uint32_t zpad0, zpad1;
     uint32_t sketch[kSketch];        // truncated rows: largest lane maxima (order keys, descending)
     unsigned long long list[kLCap];  // truncated rows: cand_word of each listed token
 };
@@ -123,8 +127,12 @@ struct alignas(16) RowInfo {
     int32_t k;
     uint32_t stream, key_lo, key_hi;
     int32_t lrow;
+    float s2o;     // log2(e) / T of the logprob outputs (1 when unscaled)
     uint8_t cls, do_topk, do_topp, do_minp;
-    uint8_t need_z, m, mt, pad1;
+    uint8_t need_z, m, mt, greedy;
+    uint8_t lp;    // logprob outputs requested
+    uint8_t need_zo;  // the units keep the row's softmax mass at the outputs' temperature
+    uint8_t pad2, pad3;
 };
 
 struct alignas(16) WarpScratch {
@@ -149,6 +157,9 @@ struct alignas(16) SliceShared {
     int32_t red_i[kW];
     unsigned long long red_k[2 * kW];
     unsigned long long sel_prefix, sel_wabove, sel_target;
+    double red_d[kW];
+    unsigned long long lp_list[kMaxTopN];
+    int32_t lp_cnt;
     int32_t sel_idx;
     int32_t pad;
 };

@@ -261,6 +261,19 @@ def test_plain_rows_ignore_their_neighbours_parameters(sampler):
     assert np.array_equal(g1.tokens[plain], g2.tokens[plain])
 
 
+@pytest.mark.parametrize("k", [5, 20, 32])
+def test_masked_rows_with_few_finite_lanes(sampler, k):
+    """Rows masked to -inf except one 8-token vector in 32: each slice then has a
+    single finite lane maximum, fewer than the top k its list must hold."""
+    b = workloads.random_batch(77 + k, 6, 40000, "bf16", mix="topk")
+    x = workloads.bf16_bits_to_f32(b.logits).reshape(b.n_rows, -1).copy()
+    vec = np.arange(x.shape[1]) // 8
+    x[:, (vec % 32) != 0] = -np.inf
+    b = b.with_(logits=workloads.to_bf16_bits(x), top_k=np.full(6, k, np.int32),
+                top_p=np.ones(6, np.float32), min_p=np.zeros(6, np.float32))
+    _check(sampler, b, want_probs=False)
+
+
 def test_exact_path_runs_and_matches(sampler):
     """Rows the slice kernel's candidate lists cannot settle (top-k above their
     cap, top-p reaching past the lists, flat rows) take its exact path."""

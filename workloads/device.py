@@ -98,3 +98,28 @@ def run(sampler, batch, want_probs: Optional[bool] = None, device="cuda:0",
     get = lambda x: None if x is None else x.cpu().numpy()
     return GpuResult(get(d["out_tokens"]), get(d["out_status"]), get(d["out_probs"]),
                      get(d["out_logprobs"]))
+
+
+class GpuLogprobResult:
+    def __init__(self, tokens, status, token_logprob, top_ids, top_logprobs):
+        self.tokens, self.status = tokens, status
+        self.token_logprob, self.top_ids, self.top_logprobs = token_logprob, top_ids, top_logprobs
+
+
+def run_logprobs(sampler, batch, top_n: int, unscaled: bool = False, device="cuda:0",
+                 token_logprob: bool = True) -> GpuLogprobResult:
+    """One synchronous sampler_sample_logprobs call; results back on the host."""
+    import torch
+
+    d = to_device(batch, device, False)
+    N = batch.n_rows
+    tok_lp = torch.full((N,), 7.0, dtype=torch.float32, device=device) if token_logprob else None
+    ids = torch.full((N, max(top_n, 1)), -7, dtype=torch.int32, device=device)
+    lps = torch.full((N, max(top_n, 1)), 7.0, dtype=torch.float32, device=device)
+    sampler.sample_logprobs_args(sample_args(sampler, batch, d), top_n=top_n, unscaled=unscaled,
+                                 out_token_logprob=tok_lp, out_top_ids=ids if top_n else None,
+                                 out_top_logprobs=lps if top_n else None)
+    torch.cuda.synchronize()
+    return GpuLogprobResult(d["out_tokens"].cpu().numpy(), d["out_status"].cpu().numpy(),
+                            tok_lp.cpu().numpy() if tok_lp is not None else None,
+                            ids.cpu().numpy()[:, :top_n], lps.cpu().numpy()[:, :top_n])
