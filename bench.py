@@ -13,7 +13,9 @@ from those replays, and from a sustained run of at least half a second when
 the requested steps take less. `e2e` goes through the host-buffer C entry
 point; `roofline` is for the sampling kernel; `cpu_baseline` = the CPU oracle
 on a bounded sample at one thread and at every core; `ablation` times the
-per-family workloads (plain -> +top-k/top-p -> +min-p -> +penalties).
+per-family workloads (plain -> +top-k/top-p -> +min-p -> +penalties);
+`logprob_outputs` times the same step with the per-row logprob outputs
+(sampled token + top 5, scaled and unscaled).
 `--impl reference` times the CPU oracle itself (the only reference this
 sampler has), one row per step. Several GPUs run independent replicas (rows
 are independent: no collective).
@@ -372,6 +374,48 @@ def host_call_us(sampler, arg_blocks, stream, n=200):
     return stats_us(ts)
 
 
+class LogprobReplayer(Replayer):
+    """Replays of sampler_sample_logprobs calls (top_n logprobs per row)."""
+
+    def __init__(self, torch, sampler, arg_blocks, stream, lp_kw):
+        super().__init__(torch, sampler, arg_blocks, stream)
+        self.lp_kw = lp_kw
+
+    def graph(self, r):
+        if r not in self.graphs:
+            torch = self.torch
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(r):
+                        self.sampler.sample_logprobs_args(self.args[i], stream=torch.cuda.current_stream().cuda_stream,
+                                                          **self.lp_kw)
+            torch.cuda.synchronize()
+            self.graphs[r] = g
+        return self.graphs[r]
+
+
+def run_logprob_outputs(torch, sampler, rep, batch, dev, top_n, seconds):
+    """Median step time with the per-row logprob outputs (sampled token + top_n),
+    scaled and unscaled, on the same rotating inputs."""
+    N = batch.n_rows
+    out = {"top_n": top_n, "output_bytes_per_step": N * 4 + N * top_n * 8,
+           "materialised_bytes_per_step": 8 * N * batch.vocab}
+    for unscaled in (False, True):
+        kw = dict(top_n=top_n, unscaled=unscaled,
+                  out_token_logprob=torch.empty(N, dtype=torch.float32, device=dev),
+                  out_top_ids=torch.empty((N, top_n), dtype=torch.int32, device=dev),
+                  out_top_logprobs=torch.empty((N, top_n), dtype=torch.float32, device=dev))
+        lr = LogprobReplayer(torch, sampler, rep.args, rep.stream, kw)
+        with torch.cuda.stream(rep.stream):
+            for a in rep.args:
+                sampler.sample_logprobs_args(a, stream=rep.stream.cuda_stream, **kw)
+        torch.cuda.synchronize()
+        lr.run(lr.R * 2)
+        out["unscaled" if unscaled else "scaled"] = stats_us(sustained(lr, seconds))
+    return out
+
+
 def run_ablation(torch, pkg, wdev, dev, local, seconds):
     """Median step time of each per-family workload (plain -> +top-k/top-p ->
     +min-p -> +penalties) at N=64, V=128000 bf16."""
@@ -475,7 +519,9 @@ def run_ours(args):
                "sample": f"{nrows} rows of the same batch ({el:.1f} s, {cores} threads)",
                "one_thread": {"value": rps1, "unit": UNIT, "sample": f"{nrows1} rows ({el1:.1f} s)"}}
     abl = None
+    lpo = None
     if not args.no_ablation and args.workload == "mixed":
+        lpo = run_logprob_outputs(torch, sampler, rep, batch, dev, 5, args.ablation_seconds)
         abl = run_ablation(torch, pkg, wdev, dev, local, args.ablation_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -496,6 +542,7 @@ def run_ours(args):
         "exact_path_rows_per_step": exact_rows / args.steps,
         "clocks": clk,
         "ablation": abl,
+        "logprob_outputs": lpo,
         "kernel_hash": kernel_hash(),
         "first_tokens": tokens[:8].tolist(),
     }
