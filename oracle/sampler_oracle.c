@@ -163,19 +163,36 @@ typedef struct {
     const uint64_t* seed; const uint8_t* has_seed; const uint32_t* stream_id;
     const int32_t* hist_offsets; const int32_t* hist_ids;
     uint64_t global_seed; uint64_t philox_offset;
+    const uint32_t* vocab_mask; int64_t mask_stride;
 } oracle_in_t;
+
+/* Disallowed tokens of output row r's vocabulary bitmask become -inf: bit
+ * (v & 31) of word v >> 5 of the row's mask set means token v is allowed (the
+ * grammar's mask applied to the logits before sampling, manual-sglang-101,
+ * constrained decoding, step "Mask"). */
+static void apply_mask(const oracle_in_t* in, int64_t r, float* x)
+{
+    if (!in->vocab_mask) return;
+    const uint32_t* m = in->vocab_mask + r * in->mask_stride;
+    for (int64_t v = 0; v < in->vocab; ++v)
+        if (!((m[v >> 5] >> (v & 31)) & 1u)) x[v] = -INFINITY;
+}
 
 /* Load output row r's logits as fp32 and apply the penalties for the row's
  * history: count the occurrences c_v of each token, then for c_v > 0
  *   x = x > 0 ? x / rep : x * rep;  x = x - freq * c_v;  x = x - pres,
- * one fp32 operation per step. Returns ST_OK or ST_BAD_HISTORY. */
+ * one fp32 operation per step; then the row's vocabulary mask. Returns ST_OK
+ * or ST_BAD_HISTORY. */
 static int load_penalized_row(const oracle_in_t* in, int64_t r, float* x, int32_t* count,
                               float pres, float freq, float rep)
 {
     const int64_t V = in->vocab;
     const int64_t lrow = in->logit_row ? (int64_t)in->logit_row[r] : r;
     for (int64_t v = 0; v < V; ++v) x[v] = read_logit(in->logits, in->dtype, lrow * in->row_stride + v);
-    if (!in->hist_offsets) return ST_OK;
+    if (!in->hist_offsets) {
+        apply_mask(in, r, x);
+        return ST_OK;
+    }
     /* the library's documented per-row limit: counts are kept in 16 bits */
     if (in->hist_offsets[r + 1] - in->hist_offsets[r] > 65535) return ST_BAD_HISTORY;
     memset(count, 0, (size_t)V * sizeof(int32_t));
@@ -193,6 +210,7 @@ static int load_penalized_row(const oracle_in_t* in, int64_t r, float* x, int32_
         if (c > 0) xv = xv - pres;
         x[v] = xv;
     }
+    apply_mask(in, r, x);
     return ST_OK;
 }
 
@@ -354,6 +372,7 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
                   const float* repetition, const uint64_t* seed, const uint8_t* has_seed,
                   const uint32_t* stream_id, const int32_t* hist_offsets, const int32_t* hist_ids,
                   uint64_t global_seed, uint64_t philox_offset,
+                  const uint32_t* vocab_mask, int64_t mask_stride,
                   const int64_t* rows, int64_t n_out,
                   int32_t* out_tokens, int32_t* out_status, float* out_probs, float* out_logprobs,
                   double* out_diag, int nthreads)
@@ -363,7 +382,7 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
     if (hist_offsets && !hist_ids) return -1;
     oracle_in_t in = {logits, dtype, vocab, row_stride, logit_row, temperature, top_k, top_p, min_p,
                       presence, frequency, repetition, seed, has_seed, stream_id,
-                      hist_offsets, hist_ids, global_seed, philox_offset};
+                      hist_offsets, hist_ids, global_seed, philox_offset, vocab_mask, mask_stride};
     const int64_t n = rows ? n_out : n_rows;
     int failed = 0;
     (void)nthreads;
@@ -391,20 +410,31 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
     return failed ? -1 : 0;
 }
 
-/* The penalised fp32 logits of one row (the same code the sampler uses), for
- * checking the penalty arithmetic against hand-computed cases. Returns the row
- * status (ST_OK or ST_BAD_HISTORY). */
+/* The penalised (and masked) fp32 logits of output row out_row, whose logits
+ * are row `row` of `logits` (the same code the sampler uses), for checking the
+ * penalty arithmetic against hand-computed cases. Returns the row status
+ * (ST_OK or ST_BAD_HISTORY). */
 int oracle_penalized_logits(const void* logits, int dtype, int64_t vocab, int64_t row_stride,
                             int64_t row, float presence, float frequency, float repetition,
-                            const int32_t* hist_offsets, const int32_t* hist_ids, float* out_x)
+                            const int32_t* hist_offsets, const int32_t* hist_ids,
+                            const uint32_t* vocab_mask, int64_t mask_stride, int64_t out_row, float* out_x)
 {
     oracle_in_t in;
     memset(&in, 0, sizeof in);
-    in.logits = logits; in.dtype = dtype; in.vocab = vocab; in.row_stride = row_stride;
-    in.hist_offsets = hist_offsets; in.hist_ids = hist_ids;
+    int32_t* lr = (int32_t*)malloc((size_t)(out_row + 1) * sizeof(int32_t));
     int32_t* count = (int32_t*)malloc((size_t)vocab * sizeof(int32_t));
-    if (!count) return -1;
-    int st = load_penalized_row(&in, row, out_x, count, presence, frequency, repetition);
+    if (!lr || !count) {
+        free(lr);
+        free(count);
+        return -1;
+    }
+    lr[out_row] = (int32_t)row;
+    in.logits = logits; in.dtype = dtype; in.vocab = vocab; in.row_stride = row_stride;
+    in.logit_row = lr;
+    in.hist_offsets = hist_offsets; in.hist_ids = hist_ids;
+    in.vocab_mask = vocab_mask; in.mask_stride = mask_stride;
+    int st = load_penalized_row(&in, out_row, out_x, count, presence, frequency, repetition);
     free(count);
+    free(lr);
     return st;
 }

@@ -47,6 +47,7 @@ __all__ = [
     "penalties",
     "forks",
     "random_batch",
+    "vocab_mask",
     "ablation",
     "ABLATION_STAGES",
     "WORKLOADS",
@@ -84,6 +85,7 @@ class SamplerBatch:
     global_seed: int = 0
     philox_offset: int = 0
     want_probs: bool = False
+    vocab_mask: Optional[np.ndarray] = None  # [n_rows, ceil(vocab / 32)] uint32; bit set = allowed
     notes: dict = field(default_factory=dict)
 
     @property
@@ -271,6 +273,29 @@ def random_batch(seed: int, n: int, v: int, dtype: str = "f32", *, stride_pad: i
                     repetition=_f32(rng.uniform(0.8, 1.5, size=n)),
                     hist_offsets=offs, hist_ids=ids)
     return b
+
+
+def vocab_mask(seed: int, n: int, v: int, allowed: float = 0.1, full_rows: int = 1) -> np.ndarray:
+    """A grammar-style vocabulary bitmask [n, ceil(v / 32)] (bit v & 31 of word
+    v >> 5 set = token v allowed): runs of allowed tokens covering about
+    `allowed` of the vocabulary, plus scattered single tokens; the first
+    `full_rows` rows allow everything."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    words = (v + 31) // 32
+    out = np.zeros((n, words), np.uint32)
+    for r in range(n):
+        ok = np.zeros(words * 32, bool)
+        if r < full_rows:
+            ok[:v] = True
+        else:
+            target = max(1, int(allowed * v))
+            while ok[:v].sum() < target:
+                start = int(rng.integers(0, v))
+                ok[start:min(v, start + int(rng.integers(1, 200)))] = True
+                ok[rng.integers(0, v, size=8)] = True
+        bits = ok.reshape(words, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)
+        out[r] = bits.sum(axis=1).astype(np.uint32)
+    return out
 
 
 ABLATION_STAGES = ("plain", "topkp", "minp", "penalties")
