@@ -375,7 +375,7 @@ def host_call_us(sampler, arg_blocks, stream, n=200):
 
 
 class LogprobReplayer(Replayer):
-    """Replays of sampler_sample_logprobs calls (top_n logprobs per row)."""
+    """Replays of sampler_sample_ex calls (top_n logprobs per row)."""
 
     def __init__(self, torch, sampler, arg_blocks, stream, lp_kw):
         super().__init__(torch, sampler, arg_blocks, stream)
@@ -388,7 +388,7 @@ class LogprobReplayer(Replayer):
             with torch.cuda.stream(self.stream):
                 with torch.cuda.graph(g, stream=self.stream):
                     for i in range(r):
-                        self.sampler.sample_logprobs_args(self.args[i], stream=torch.cuda.current_stream().cuda_stream,
+                        self.sampler.sample_ex_args(self.args[i], stream=torch.cuda.current_stream().cuda_stream,
                                                           **self.lp_kw)
             torch.cuda.synchronize()
             self.graphs[r] = g
@@ -409,7 +409,7 @@ def run_logprob_outputs(torch, sampler, rep, batch, dev, top_n, seconds):
         lr = LogprobReplayer(torch, sampler, rep.args, rep.stream, kw)
         with torch.cuda.stream(rep.stream):
             for a in rep.args:
-                sampler.sample_logprobs_args(a, stream=rep.stream.cuda_stream, **kw)
+                sampler.sample_ex_args(a, stream=rep.stream.cuda_stream, **kw)
         torch.cuda.synchronize()
         lr.run(lr.R * 2)
         out["unscaled" if unscaled else "scaled"] = stats_us(sustained(lr, seconds))

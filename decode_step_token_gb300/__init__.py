@@ -14,13 +14,13 @@ from . import _binding as abi
 from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHORT_WAITS, SAMPLER_DTYPE_BF16,
                        SAMPLER_DTYPE_F32, SAMPLER_MAX_TOP_N, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
                        load_library, sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
-                       sampler_destroy, sampler_logprob_out_t, sampler_sample, sampler_sample_host,
-                       sampler_sample_logprobs, sampler_sample_noalloc, sampler_status_string,
+                       sampler_destroy, sampler_ext_t, sampler_sample, sampler_sample_host,
+                       sampler_sample_ex, sampler_sample_noalloc, sampler_status_string,
                        sampler_get_stat)
 
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
-           "sampler_sample_host", "sampler_sample_noalloc", "sampler_sample_logprobs", "sampler_destroy",
-           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "sampler_logprob_out_t",
+           "sampler_sample_host", "sampler_sample_noalloc", "sampler_sample_ex", "sampler_destroy",
+           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "sampler_ext_t",
            "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
 
 
@@ -122,20 +122,23 @@ class Sampler:
     def sample(self, stream: Optional[int] = None, **kw) -> None:
         self.sample_args(self.make_args(**kw), stream)
 
-    def sample_logprobs_args(self, args: sampler_args_t, top_n: int = 0, unscaled: bool = False,
-                             out_token_logprob=None, out_top_ids=None, out_top_logprobs=None,
-                             stream: Optional[int] = None) -> None:
-        """sampler_sample_logprobs: the step plus per-row logprob outputs (device
-        tensors: out_token_logprob [N] fp32, out_top_ids / out_top_logprobs
-        [N, top_n] int32 / fp32)."""
+    def sample_ex_args(self, args: sampler_args_t, top_n: int = 0, unscaled: bool = False,
+                       out_token_logprob=None, out_top_ids=None, out_top_logprobs=None,
+                       vocab_mask=None, mask_stride: Optional[int] = None,
+                       stream: Optional[int] = None) -> None:
+        """sampler_sample_ex: the step plus per-row logprob outputs (device tensors:
+        out_token_logprob [N] fp32, out_top_ids / out_top_logprobs [N, top_n]
+        int32 / fp32) and a vocabulary bitmask (device [N, words] int32/uint32)."""
         if stream is None:
             import torch
             stream = torch.cuda.current_stream(self.device).cuda_stream
-        lp = sampler_logprob_out_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob),
-                                   _ptr(out_top_ids), _ptr(out_top_logprobs))
-        rc = sampler_sample_logprobs(self._h, args, lp, stream)
+        if vocab_mask is not None and mask_stride is None:
+            mask_stride = int(vocab_mask.shape[-1])
+        ext = sampler_ext_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob), _ptr(out_top_ids),
+                            _ptr(out_top_logprobs), _ptr(vocab_mask), int(mask_stride or 0))
+        rc = sampler_sample_ex(self._h, args, ext, stream)
         if rc != SAMPLER_OK:
-            raise SamplerError(rc, "sampler_sample_logprobs")
+            raise SamplerError(rc, "sampler_sample_ex")
 
     def stat(self, which: int = 0, reset: bool = False) -> int:
         """A device diagnostic counter (synchronizes the device)."""

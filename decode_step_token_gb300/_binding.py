@@ -38,7 +38,7 @@ SAMPLER_CREATE_SHORT_WAITS = 4
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
             "sampler_status_string", "sampler_abi_version", "sampler_get_stat",
-            "sampler_sample_noalloc", "sampler_sample_logprobs")
+            "sampler_sample_noalloc", "sampler_sample_ex")
 SAMPLER_STAT_EXACT_ROWS = 0
 SAMPLER_NOALLOC_MAX_ROWS = 64
 SAMPLER_MAX_TOP_N = 16
@@ -88,13 +88,15 @@ class sampler_args_t(ctypes.Structure):
     ]
 
 
-class sampler_logprob_out_t(ctypes.Structure):
+class sampler_ext_t(ctypes.Structure):
     _fields_ = [
         ("top_n", ctypes.c_int32),
         ("unscaled", ctypes.c_int32),
         ("out_token_logprob", _P),
         ("out_top_ids", _P),
         ("out_top_logprobs", _P),
+        ("vocab_mask", _P),
+        ("mask_stride", ctypes.c_int64),
     ]
 
 
@@ -126,9 +128,8 @@ def load_library(path: str = LIB):
             lib.sampler_get_stat.restype = ctypes.c_int
             lib.sampler_sample_noalloc.argtypes = [ctypes.POINTER(sampler_args_t), _P]
             lib.sampler_sample_noalloc.restype = ctypes.c_int
-            lib.sampler_sample_logprobs.argtypes = [_P, ctypes.POINTER(sampler_args_t),
-                                                    ctypes.POINTER(sampler_logprob_out_t), _P]
-            lib.sampler_sample_logprobs.restype = ctypes.c_int
+            lib.sampler_sample_ex.argtypes = [_P, ctypes.POINTER(sampler_args_t), ctypes.POINTER(sampler_ext_t), _P]
+            lib.sampler_sample_ex.restype = ctypes.c_int
             lib.sampler_abi_version.argtypes = []
             lib.sampler_abi_version.restype = ctypes.c_uint32
             _lib = lib
@@ -150,10 +151,10 @@ def sampler_sample_host(h, args: sampler_args_t, stream: int) -> int:
     return load_library().sampler_sample_host(h, ctypes.byref(args), _P(stream))
 
 
-def sampler_sample_logprobs(h, args: sampler_args_t, lp, stream: int) -> int:
-    """lp: a sampler_logprob_out_t or None."""
-    return load_library().sampler_sample_logprobs(h, ctypes.byref(args), ctypes.byref(lp) if lp is not None else None,
-                                                  _P(stream))
+def sampler_sample_ex(h, args: sampler_args_t, ext, stream: int) -> int:
+    """ext: a sampler_ext_t or None."""
+    return load_library().sampler_sample_ex(h, ctypes.byref(args), ctypes.byref(ext) if ext is not None else None,
+                                            _P(stream))
 
 
 def sampler_sample_noalloc(args: sampler_args_t, stream: int) -> int:

@@ -51,8 +51,8 @@ bool slice_geometry(int64_t n_rows, int64_t vocab, int esize, int sms, SliceGeom
 int slice_prepare(int dtype, size_t smem);
 
 // Enqueue one slice-kernel launch. max_polls bounds each wait on a staging copy.
-// lp: per-row logprob outputs (NULL: none)
-int slice_launch(const sampler_args_t* a, const sampler_logprob_out_t* lp, const SliceGeometry& g,
+// ext: the step's extensions (NULL: none)
+int slice_launch(const sampler_args_t* a, const sampler_ext_t* ext, const SliceGeometry& g,
                  const SliceWorkspace& ws, uint32_t max_polls, cudaStream_t stream);
 
 // ---------------------------------------------------------------- fork-group kernel

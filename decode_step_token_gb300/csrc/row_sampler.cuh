@@ -86,12 +86,16 @@ struct KernelParams {
     float* out_logprobs;
     int32_t* out_status;
     int32_t slice_len;  // elements per CTA, a multiple of 8
-    // per-row logprob outputs of sampler_sample_logprobs (slice kernel only)
+    // per-row logprob outputs of sampler_sample_ex (slice kernel only)
     float* out_tok_lp;
     int32_t* out_top_ids;
     float* out_top_lp;
     int32_t top_n;
     int32_t lp_unscaled;
+    // vocabulary bitmask of sampler_sample_ex (slice kernel only): bit v & 31 of
+    // word v >> 5 of row r's mask set = token v allowed
+    const uint32_t* vocab_mask;
+    int64_t mask_stride;
 };
 
 // ------------------------------------------------------------------ records

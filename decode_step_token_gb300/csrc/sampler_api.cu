@@ -85,9 +85,9 @@ int launch_group(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
     return dst::group_launch(a, gg, h->grp_occ[slot], stream);
 }
 
-// lp: per-row logprob outputs, offered on the slice kernel only (the caller has
+// lp: the step's extensions, offered on the slice kernel only (the caller has
 // checked that the call takes it)
-int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const sampler_logprob_out_t* lp = nullptr)
+int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const sampler_ext_t* lp = nullptr)
 {
     dst::SliceGeometry g;
     if (slice_takes(a) && a->n_rows <= h->slice_rows &&
@@ -103,7 +103,7 @@ int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const samp
     return launch_group(h, a, stream);
 }
 
-// Whether a call with logprob outputs takes the slice kernel (host-visible facts).
+// Whether a call with extensions takes the slice kernel (host-visible facts).
 bool slice_would_take(sampler_t h, const sampler_args_t* a)
 {
     dst::SliceGeometry g;
@@ -317,21 +317,21 @@ int sampler_sample(sampler_t h, const sampler_args_t* a, sampler_stream_t stream
     return launch(h, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int sampler_sample_logprobs(sampler_t h, const sampler_args_t* a, const sampler_logprob_out_t* lp,
-                            sampler_stream_t stream)
+int sampler_sample_ex(sampler_t h, const sampler_args_t* a, const sampler_ext_t* ext, sampler_stream_t stream)
 {
     int rc = check_args(h, a);
     if (rc != SAMPLER_OK) return rc;
-    if (lp) {
-        if (lp->top_n < 0 || lp->top_n > SAMPLER_MAX_TOP_N) return SAMPLER_ERR_UNSUPPORTED;
-        if (lp->top_n > 0 && (!lp->out_top_ids || !lp->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
-        if (!lp->out_token_logprob && lp->top_n == 0) lp = nullptr;  // nothing asked
+    if (ext) {
+        if (ext->top_n < 0 || ext->top_n > SAMPLER_MAX_TOP_N) return SAMPLER_ERR_UNSUPPORTED;
+        if (ext->top_n > 0 && (!ext->out_top_ids || !ext->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
+        if (ext->vocab_mask && ext->mask_stride < (a->vocab + 31) / 32) return SAMPLER_ERR_UNSUPPORTED;
+        if (!ext->out_token_logprob && ext->top_n == 0 && !ext->vocab_mask) ext = nullptr;  // nothing asked
     }
     if (a->n_rows == 0) return SAMPLER_OK;
     DeviceGuard guard;
     if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
-    if (lp && !slice_would_take(h, a)) return SAMPLER_ERR_UNSUPPORTED;
-    return launch(h, a, reinterpret_cast<cudaStream_t>(stream), lp);
+    if (ext && !slice_would_take(h, a)) return SAMPLER_ERR_UNSUPPORTED;
+    return launch(h, a, reinterpret_cast<cudaStream_t>(stream), ext);
 }
 
 int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)

@@ -69,7 +69,7 @@ int slice_prepare(int dtype, size_t smem)
     return SAMPLER_OK;
 }
 
-int slice_launch(const sampler_args_t* a, const sampler_logprob_out_t* lp, const SliceGeometry& g,
+int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGeometry& g,
                  const SliceWorkspace& ws, uint32_t max_polls, cudaStream_t stream)
 {
     slc::SliceParams p;
@@ -101,6 +101,8 @@ int slice_launch(const sampler_args_t* a, const sampler_logprob_out_t* lp, const
         k.out_top_ids = lp->top_n > 0 ? lp->out_top_ids : nullptr;
         k.out_top_lp = lp->top_n > 0 ? lp->out_top_logprobs : nullptr;
         k.lp_unscaled = lp->unscaled ? 1 : 0;
+        k.vocab_mask = lp->vocab_mask;
+        k.mask_stride = lp->mask_stride;
     }
     p.n_rows = int(a->n_rows);
     p.G = g.G;

@@ -74,6 +74,7 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     ri.need_zo = (ri.lp && (kp.lp_unscaled || ri.cls != kClsTrunc)) ? 1 : 0;
     if (ri.lp && kp.top_n > 0) ri.mt = uint8_t(max(int(ri.mt), kp.top_n));
     ri.pad2 = ri.pad3 = 0;
+    ri.r = r;
     return ri;
 }
 
@@ -955,6 +956,11 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
                     v[u] = __ldg(reinterpret_cast<const uint4*>(g) + j);
                 else
                     v[u] = load_vec_slow<InT>(g, j, n);
+                if (P.k.vocab_mask) {
+                    const int tk = c0 + j * E;
+                    const uint32_t w = __ldg(P.k.vocab_mask + size_t(ri.r) * size_t(P.k.mask_stride) + (tk >> 5));
+                    v[u] = Vec<InT>::masked(v[u], (w >> (tk & 31)) & ((1u << E) - 1u));
+                }
             }
         }
         uint32_t mine = 0;
@@ -1270,9 +1276,12 @@ __device__ __forceinline__ int cta_excl_scan(int v, int& total, SliceShared& sh)
 }
 
 template <typename InT>
-__device__ __forceinline__ float row_x(const KernelParams& kp, int lrow, int v)
+__device__ __forceinline__ float row_x(const KernelParams& kp, const RowInfo& ri, int v)
 {
-    return ElemTraits<InT>::load(kp.logits, int64_t(lrow) * kp.row_stride + v);
+    const float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
+        return -INFINITY;
+    return x;
 }
 
 // The token closing the kept prefix: the first token (value desc, index asc)
@@ -1300,7 +1309,7 @@ __device__ void cta_select(SliceShared& sh, const KernelParams& kp, const RowInf
         const uint32_t prefix = uint32_t(sh.sel_prefix);
         const int shift = 24 - 8 * level;
         for (int v = tid; v < V; v += kT) {
-            const float x = row_x<InT>(kp, ri.lrow, v);
+            const float x = row_x<InT>(kp, ri, v);
             if (!(x > -INFINITY)) continue;
             const uint32_t key = f2key(x);
             if (dom && !in_prefix(key, v, dkey, didx)) continue;
@@ -1339,7 +1348,7 @@ __device__ void cta_select(SliceShared& sh, const KernelParams& kp, const RowInf
         const int v = v0 + tid;
         int c = 0;
         if (v < V) {
-            const float x = row_x<InT>(kp, ri.lrow, v);
+            const float x = row_x<InT>(kp, ri, v);
             const uint32_t key = f2key(x);
             c = (x > -INFINITY && key == K && (!dom || in_prefix(key, v, dkey, didx))) ? 1 : 0;
         }
@@ -1388,7 +1397,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
     double z = 0.0;
     uint32_t nk = 0;
     for (int v = tid; v < V; v += kT) {
-        const float x = row_x<InT>(kp, ri.lrow, v);
+        const float x = row_x<InT>(kp, ri, v);
         if (!(x > -INFINITY)) continue;
         const bool kept = !(hb && !in_prefix(f2key(x), v, bk, bi)) && !(ri.do_minp && !(x >= xthr));
         if (ri.lp && (kept || !lp_kept)) {
@@ -1448,7 +1457,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
     __syncthreads();
     if (n > 0) {
         for (int v = tid; v < V; v += kT) {
-            const float x = row_x<InT>(kp, ri.lrow, v);
+            const float x = row_x<InT>(kp, ri, v);
             if (x > -INFINITY && in_prefix(f2key(x), v, nkey, nidx)) {
                 const int q = atomicAdd(&sh.lp_cnt, 1);
                 if (q < kMaxTopN) sh.lp_list[q] = cand_word(f2key(x), v);
@@ -1468,7 +1477,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
         __syncwarp();
         if (lane < c) sh.lp_list[rank] = w;
         __syncwarp();
-        const float xt = row_x<InT>(kp, ri.lrow, token);
+        const float xt = row_x<InT>(kp, ri, token);
         lp_write(kp, r, sh.lp_list, c, m, ri.s2o, log2f(float(zt)), xt);
     }
     __syncthreads();
@@ -1503,6 +1512,19 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
     sv.nvec = (n_el + E - 1) / E;
     sv.n = n_el;
     sv.c0 = c0;
+    if (kp.vocab_mask && !extra) {
+        // the row's vocabulary mask: staged vectors are masked in place once,
+        // the others (a ragged tail, an unaligned slice) as they are read
+        sv.mw = kp.vocab_mask + size_t(r) * size_t(kp.mask_stride);
+        uint4* smv = reinterpret_cast<uint4*>(const_cast<unsigned char*>(slot));
+#pragma unroll 4
+        for (int j = lane; j < sv.nb; j += 32) {
+            const int t0 = c0 + j * E;
+            const uint32_t bits = (__ldg(sv.mw + (t0 >> 5)) >> (t0 & 31)) & ((1u << E) - 1u);
+            if (bits != (1u << E) - 1u) smv[j] = Vec<InT>::masked(smv[j], bits);
+        }
+        __syncwarp();
+    }
     SliceHdr hdr;
     hdr.mx = -INFINITY;
     hdr.amax = INT_MAX;

@@ -133,6 +133,7 @@ struct alignas(16) RowInfo {
     uint8_t lp;    // logprob outputs requested
     uint8_t need_zo;  // the units keep the row's softmax mass at the outputs' temperature
     uint8_t pad2, pad3;
+    int32_t r;     // the output row
 };
 
 struct alignas(16) WarpScratch {
@@ -195,6 +196,17 @@ struct Vec<uint16_t> {
     __device__ static __forceinline__ float get(const uint4& r, int e) { return ElemTraits<uint16_t>::get(r, e); }
     // running maximum in packed form, NaN-propagating (four bf16x2 lanes)
     __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+    // elements whose bit is clear become -inf
+    __device__ static __forceinline__ uint32_t mask_word(uint32_t w, uint32_t b2)
+    {
+        const uint32_t keep = ((b2 & 1u) ? 0x0000FFFFu : 0u) | ((b2 & 2u) ? 0xFFFF0000u : 0u);
+        return (w & keep) | (0xFF80FF80u & ~keep);
+    }
+    __device__ static __forceinline__ uint4 masked(const uint4& v, uint32_t bits)
+    {
+        return make_uint4(mask_word(v.x, bits), mask_word(v.y, bits >> 2), mask_word(v.z, bits >> 4),
+                          mask_word(v.w, bits >> 6));
+    }
     using Acc = uint4;
     __device__ static __forceinline__ Acc acc_init() { return neg_inf(); }
     __device__ static __forceinline__ uint32_t hmax_nan(uint32_t a, uint32_t b)
@@ -255,6 +267,11 @@ struct Vec<float> {
     static constexpr int E = 4;
     __device__ static __forceinline__ float get(const uint4& r, int e) { return ElemTraits<float>::get(r, e); }
     __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+    __device__ static __forceinline__ uint4 masked(const uint4& v, uint32_t bits)
+    {
+        return make_uint4((bits & 1u) ? v.x : 0xFF800000u, (bits & 2u) ? v.y : 0xFF800000u,
+                          (bits & 4u) ? v.z : 0xFF800000u, (bits & 8u) ? v.w : 0xFF800000u);
+    }
     using Acc = float4;
     __device__ static __forceinline__ Acc acc_init() { return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY); }
     __device__ static __forceinline__ float fmax_nan(float a, float b)
@@ -301,10 +318,12 @@ template <typename InT>
 struct SliceView {
     const uint4* sm;
     const InT* g;    // first element of the slice in global memory
-    int nb;          // staged vectors
+    int nb;          // staged vectors (already masked)
     int nvec;        // vectors covering the slice
     int n;           // elements in the slice
     int c0;          // first token of the slice
+    const uint32_t* mw = nullptr;  // vocabulary mask words (NULL: none) ...
+    int mbase = 0;                 // ... mw[0] being word mbase of the row's mask
 
     __device__ __forceinline__ uint4 vec(int j) const
     {
@@ -322,7 +341,15 @@ struct SliceView {
                 w[q] = i < n ? reinterpret_cast<const uint32_t*>(g)[i] : 0xFF800000u;
             }
         }
-        return make_uint4(w[0], w[1], w[2], w[3]);
+        const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+        return mw ? Vec<InT>::masked(v, mask_bits(j)) : v;
+    }
+    // the allowed-token bits of vector j (bit e: element e)
+    __device__ __forceinline__ uint32_t mask_bits(int j) const
+    {
+        constexpr int E = Vec<InT>::E;
+        const int t0 = c0 + j * E;
+        return (mw[(t0 >> 5) - mbase] >> (t0 & 31)) & ((1u << E) - 1u);
     }
 };
 

@@ -80,7 +80,7 @@ enum {
     SAMPLER_ERR_CUDA = -5,         /* a CUDA call failed (launch, copy, set-up) */
     SAMPLER_ERR_NO_DEVICE = -6,    /* no usable sm_100-family device */
     SAMPLER_ERR_NO_STAGING = -7,   /* sampler_sample_host on a handle made without staging */
-    SAMPLER_ERR_UNSUPPORTED = -8   /* a feature sampler_sample_noalloc or sampler_sample_logprobs
+    SAMPLER_ERR_UNSUPPORTED = -8   /* a feature sampler_sample_noalloc or sampler_sample_ex
                                       does not offer on these arguments */
 };
 
@@ -231,6 +231,8 @@ int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_
 int sampler_sample_noalloc(const sampler_args_t* args, sampler_stream_t stream);
 
 /*
+ * Extensions of one step (sampler_sample_ex).
+ *
  * Per-row logprob outputs without the [N, V] tensors: the sampled token's
  * logprob and the top_n tokens of the row with theirs. By default these are
  * the logprobs of the distribution the row was sampled from, log_softmax(x / T)
@@ -238,27 +240,38 @@ int sampler_sample_noalloc(const sampler_args_t* args, sampler_stream_t stream);
  * "manual-sglang-101" says returned logprobs are (section "Logprobs are
  * temperature-scaled"); `unscaled` asks for log_softmax(x) over the whole
  * vocabulary instead (that section's original-logprob switch). x is the row's
- * penalised logit. Top-n order: value descending, index ascending; past the
- * tokens the distribution gives any mass, ids are -1 and logprobs -inf. Error
- * rows get NaN logprobs and ids -1. Every pointer is a device pointer (on the
- * handle's device); out_top_* are [n_rows * top_n] row-major.
+ * penalised (and masked) logit. Top-n order: value descending, index
+ * ascending; past the tokens the distribution gives any mass, ids are -1 and
+ * logprobs -inf. Error rows get NaN logprobs and ids -1. out_top_* are
+ * [n_rows * top_n] row-major.
+ *
+ * Vocabulary bitmask: the grammar mask that the manual's constrained-decoding
+ * section applies to the logits before sampling (step "Mask"). Bit (v & 31) of
+ * word (v >> 5) of output row r's mask, vocab_mask[r * mask_stride + (v >> 5)],
+ * set means token v is allowed; a disallowed token's logit is -inf (after the
+ * penalties). A row with no allowed finite logit reports SAMPLER_ROW_ALL_NEG_INF.
+ *
+ * Every pointer is a device pointer on the handle's device.
  */
 #define SAMPLER_MAX_TOP_N 16
 typedef struct {
-    int32_t top_n;              /* 0 .. SAMPLER_MAX_TOP_N */
-    int32_t unscaled;           /* 0: log_softmax(x / T) over the kept set; 1: log_softmax(x) */
-    float* out_token_logprob;   /* [N] logprob of the sampled token; NULL = not reported */
-    int32_t* out_top_ids;       /* [N * top_n] (unused when top_n == 0) */
-    float* out_top_logprobs;    /* [N * top_n] */
-} sampler_logprob_out_t;
+    int32_t top_n;                /* 0 .. SAMPLER_MAX_TOP_N */
+    int32_t unscaled;             /* 0: log_softmax(x / T) over the kept set; 1: log_softmax(x) */
+    float* out_token_logprob;     /* [N] logprob of the sampled token; NULL = not reported */
+    int32_t* out_top_ids;         /* [N * top_n] (unused when top_n == 0) */
+    float* out_top_logprobs;      /* [N * top_n] */
+    const uint32_t* vocab_mask;   /* [N * mask_stride] words; NULL = every token allowed */
+    int64_t mask_stride;          /* words between rows' masks, >= ceil(vocab / 32) */
+} sampler_ext_t;
 
-/* sampler_sample plus the per-row logprob outputs of `lp` (NULL: none). Offered
- * on the small-batch path: at most 256 rows, no history and no materialised
- * probs / logprobs; other calls return SAMPLER_ERR_UNSUPPORTED with nothing
- * enqueued, as does top_n outside [0, SAMPLER_MAX_TOP_N]. The same capture and
- * device rules as sampler_sample apply. */
-int sampler_sample_logprobs(sampler_t h, const sampler_args_t* args, const sampler_logprob_out_t* lp,
-                            sampler_stream_t stream);
+/* sampler_sample plus the extensions of `ext` (NULL: none). Offered on the
+ * small-batch path: at most 256 rows, no history and no materialised probs /
+ * logprobs; other calls that ask for an extension return
+ * SAMPLER_ERR_UNSUPPORTED with nothing enqueued, as does top_n outside
+ * [0, SAMPLER_MAX_TOP_N] or a mask_stride below ceil(vocab / 32). The same
+ * capture and device rules as sampler_sample apply. */
+int sampler_sample_ex(sampler_t h, const sampler_args_t* args, const sampler_ext_t* ext,
+                      sampler_stream_t stream);
 
 /* Release the handle and its device memory. NULL is a no-op. */
 void sampler_destroy(sampler_t h);

@@ -1,5 +1,5 @@
 """Per-row logprob outputs (sampled token + top-n, scaled or unscaled) of
-sampler_sample_logprobs vs the oracle, element by element (needs a GB300)."""
+sampler_sample_ex vs the oracle, element by element (needs a GB300)."""
 import numpy as np
 import pytest
 
@@ -106,12 +106,12 @@ def test_unsupported_calls_are_refused(sampler):
     args = dev.sample_args(sampler, b, dd)
     out = torch.zeros(4, dtype=torch.float32, device="cuda")
     with pytest.raises(d.SamplerError) as e:
-        sampler.sample_logprobs_args(args, out_token_logprob=out)
+        sampler.sample_ex_args(args, out_token_logprob=out)
     assert e.value.code == -8
     b2 = workloads.random_batch(45, 4, 1000, "f32")
     args2 = dev.sample_args(sampler, b2, dev.to_device(b2))
     ids = torch.zeros((4, 17), dtype=torch.int32, device="cuda")
     lps = torch.zeros((4, 17), dtype=torch.float32, device="cuda")
     with pytest.raises(d.SamplerError) as e:
-        sampler.sample_logprobs_args(args2, top_n=17, out_top_ids=ids, out_top_logprobs=lps)
+        sampler.sample_ex_args(args2, top_n=17, out_top_ids=ids, out_top_logprobs=lps)
     assert e.value.code == -8

@@ -61,6 +61,7 @@ def to_device(batch, device="cuda:0", want_probs: Optional[bool] = None, copies:
         "out_status": torch.full((N,), -7, dtype=torch.int32, device=dev),
         "out_probs": torch.empty((N, V), dtype=torch.float32, device=dev) if want else None,
         "out_logprobs": torch.empty((N, V), dtype=torch.float32, device=dev) if want else None,
+        "vocab_mask": t(batch.vocab_mask.view(np.int32)) if batch.vocab_mask is not None else None,
     }
     return d
 
@@ -93,7 +94,10 @@ def run(sampler, batch, want_probs: Optional[bool] = None, device="cuda:0",
     import torch
 
     d = to_device(batch, device, want_probs, logits_offset_elems=logits_offset_elems)
-    sampler.sample_args(sample_args(sampler, batch, d))
+    if d["vocab_mask"] is not None:
+        sampler.sample_ex_args(sample_args(sampler, batch, d), vocab_mask=d["vocab_mask"])
+    else:
+        sampler.sample_args(sample_args(sampler, batch, d))
     torch.cuda.synchronize()
     get = lambda x: None if x is None else x.cpu().numpy()
     return GpuResult(get(d["out_tokens"]), get(d["out_status"]), get(d["out_probs"]),
@@ -108,7 +112,8 @@ class GpuLogprobResult:
 
 def run_logprobs(sampler, batch, top_n: int, unscaled: bool = False, device="cuda:0",
                  token_logprob: bool = True) -> GpuLogprobResult:
-    """One synchronous sampler_sample_logprobs call; results back on the host."""
+    """One synchronous sampler_sample_ex call with logprob outputs (and the batch's
+    vocabulary mask, if any); results back on the host."""
     import torch
 
     d = to_device(batch, device, False)
@@ -116,9 +121,9 @@ def run_logprobs(sampler, batch, top_n: int, unscaled: bool = False, device="cud
     tok_lp = torch.full((N,), 7.0, dtype=torch.float32, device=device) if token_logprob else None
     ids = torch.full((N, max(top_n, 1)), -7, dtype=torch.int32, device=device)
     lps = torch.full((N, max(top_n, 1)), 7.0, dtype=torch.float32, device=device)
-    sampler.sample_logprobs_args(sample_args(sampler, batch, d), top_n=top_n, unscaled=unscaled,
-                                 out_token_logprob=tok_lp, out_top_ids=ids if top_n else None,
-                                 out_top_logprobs=lps if top_n else None)
+    sampler.sample_ex_args(sample_args(sampler, batch, d), top_n=top_n, unscaled=unscaled,
+                           out_token_logprob=tok_lp, out_top_ids=ids if top_n else None,
+                           out_top_logprobs=lps if top_n else None, vocab_mask=d["vocab_mask"])
     torch.cuda.synchronize()
     return GpuLogprobResult(d["out_tokens"].cpu().numpy(), d["out_status"].cpu().numpy(),
                             tok_lp.cpu().numpy() if tok_lp is not None else None,
