@@ -62,13 +62,13 @@ def _load():
             lib.oracle_exp1.restype = ctypes.c_double
             lib.oracle_sample.argtypes = (
                 [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P]
-                + [P] * 10 + [P, P, ctypes.c_uint64, ctypes.c_uint64, P, ctypes.c_int64, P, ctypes.c_int64]
-                + [P] * 5 + [ctypes.c_int])
+                + [P] * 10 + [P, P, ctypes.c_uint64, ctypes.c_uint64, P, ctypes.c_int64, P, P, P]
+                + [P, ctypes.c_int64] + [P] * 5 + [ctypes.c_int])
             lib.oracle_sample.restype = ctypes.c_int
             lib.oracle_penalized_logits.argtypes = [
                 P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_float, ctypes.c_float, ctypes.c_float, P, P, P, ctypes.c_int64,
-                ctypes.c_int64, P]
+                P, P, P, ctypes.c_int64, P]
             lib.oracle_penalized_logits.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -118,10 +118,14 @@ def penalized_logits(batch, row: int):
     hoff = _arr(batch.hist_offsets, np.int32)
     hids = _arr(batch.hist_ids, np.int32)
     mask = _arr(batch.vocab_mask, np.uint32)
+    boff = _arr(batch.bias_offsets, np.int32)
+    bids = _arr(batch.bias_ids, np.int32)
+    bval = _arr(batch.bias_values, np.float32)
     rc = lib.oracle_penalized_logits(
         _ptr(logits), 1 if batch.dtype == "bf16" else 0, batch.vocab, batch.row_stride, lr,
         pick(batch.presence, 0.0), pick(batch.frequency, 0.0), pick(batch.repetition, 1.0),
-        _ptr(hoff), _ptr(hids), _ptr(mask), 0 if mask is None else mask.shape[1], row, _ptr(x))
+        _ptr(hoff), _ptr(hids), _ptr(mask), 0 if mask is None else mask.shape[1],
+        _ptr(boff), _ptr(bids), _ptr(bval), row, _ptr(x))
     if rc < 0:
         raise RuntimeError("oracle_penalized_logits failed")
     return rc, x
@@ -209,12 +213,16 @@ def sample(batch, rows: Optional[Sequence[int]] = None, want_probs: Optional[boo
     ]
     (lr, t, k, p, mp, pres, freq, rep, seed, has_seed, sid, hoff, hids) = keep
     mask = _arr(batch.vocab_mask, np.uint32)
+    boff = _arr(batch.bias_offsets, np.int32)
+    bids = _arr(batch.bias_ids, np.int32)
+    bval = _arr(batch.bias_values, np.float32)
     rc = lib.oracle_sample(
         _ptr(logits), dtype, batch.n_rows, V, batch.row_stride, _ptr(lr),
         _ptr(t), _ptr(k), _ptr(p), _ptr(mp), _ptr(pres), _ptr(freq), _ptr(rep),
         _ptr(seed), _ptr(has_seed), _ptr(sid), _ptr(hoff), _ptr(hids),
         ctypes.c_uint64(batch.global_seed), ctypes.c_uint64(batch.philox_offset),
         _ptr(mask), 0 if mask is None else mask.shape[1],
+        _ptr(boff), _ptr(bids), _ptr(bval),
         _ptr(rows_arr), n_out, _ptr(tokens), _ptr(status), _ptr(probs), _ptr(logprobs),
         _ptr(diag), int(nthreads))
     if rc != 0:

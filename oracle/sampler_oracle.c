@@ -164,7 +164,11 @@ typedef struct {
     const int32_t* hist_offsets; const int32_t* hist_ids;
     uint64_t global_seed; uint64_t philox_offset;
     const uint32_t* vocab_mask; int64_t mask_stride;
+    const int32_t* bias_offsets; const int32_t* bias_ids; const float* bias_values;
 } oracle_in_t;
+
+/* The library's documented per-row limit on logit_bias entries. */
+#define ORACLE_MAX_BIAS 64
 
 /* Disallowed tokens of output row r's vocabulary bitmask become -inf: bit
  * (v & 31) of word v >> 5 of the row's mask set means token v is allowed (the
@@ -189,6 +193,17 @@ static int load_penalized_row(const oracle_in_t* in, int64_t r, float* x, int32_
     const int64_t V = in->vocab;
     const int64_t lrow = in->logit_row ? (int64_t)in->logit_row[r] : r;
     for (int64_t v = 0; v < V; ++v) x[v] = read_logit(in->logits, in->dtype, lrow * in->row_stride + v);
+    /* logit_bias: each entry adds its value to its token's logit, in list order
+     * (one fp32 addition each), before the penalties */
+    if (in->bias_offsets) {
+        const int32_t b0 = in->bias_offsets[r], b1 = in->bias_offsets[r + 1];
+        if (b1 - b0 > ORACLE_MAX_BIAS) return ST_BAD_PARAM;
+        for (int32_t j = b0; j < b1; ++j) {
+            const int32_t id = in->bias_ids[j];
+            if (id < 0 || (int64_t)id >= V) return ST_BAD_PARAM;
+        }
+        for (int32_t j = b0; j < b1; ++j) x[in->bias_ids[j]] = x[in->bias_ids[j]] + in->bias_values[j];
+    }
     if (!in->hist_offsets) {
         apply_mask(in, r, x);
         return ST_OK;
@@ -373,6 +388,7 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
                   const uint32_t* stream_id, const int32_t* hist_offsets, const int32_t* hist_ids,
                   uint64_t global_seed, uint64_t philox_offset,
                   const uint32_t* vocab_mask, int64_t mask_stride,
+                  const int32_t* bias_offsets, const int32_t* bias_ids, const float* bias_values,
                   const int64_t* rows, int64_t n_out,
                   int32_t* out_tokens, int32_t* out_status, float* out_probs, float* out_logprobs,
                   double* out_diag, int nthreads)
@@ -382,7 +398,8 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
     if (hist_offsets && !hist_ids) return -1;
     oracle_in_t in = {logits, dtype, vocab, row_stride, logit_row, temperature, top_k, top_p, min_p,
                       presence, frequency, repetition, seed, has_seed, stream_id,
-                      hist_offsets, hist_ids, global_seed, philox_offset, vocab_mask, mask_stride};
+                      hist_offsets, hist_ids, global_seed, philox_offset, vocab_mask, mask_stride,
+                      bias_offsets, bias_ids, bias_values};
     const int64_t n = rows ? n_out : n_rows;
     int failed = 0;
     (void)nthreads;
@@ -417,7 +434,9 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
 int oracle_penalized_logits(const void* logits, int dtype, int64_t vocab, int64_t row_stride,
                             int64_t row, float presence, float frequency, float repetition,
                             const int32_t* hist_offsets, const int32_t* hist_ids,
-                            const uint32_t* vocab_mask, int64_t mask_stride, int64_t out_row, float* out_x)
+                            const uint32_t* vocab_mask, int64_t mask_stride,
+                            const int32_t* bias_offsets, const int32_t* bias_ids, const float* bias_values,
+                            int64_t out_row, float* out_x)
 {
     oracle_in_t in;
     memset(&in, 0, sizeof in);
@@ -433,6 +452,7 @@ int oracle_penalized_logits(const void* logits, int dtype, int64_t vocab, int64_
     in.logit_row = lr;
     in.hist_offsets = hist_offsets; in.hist_ids = hist_ids;
     in.vocab_mask = vocab_mask; in.mask_stride = mask_stride;
+    in.bias_offsets = bias_offsets; in.bias_ids = bias_ids; in.bias_values = bias_values;
     int st = load_penalized_row(&in, out_row, out_x, count, presence, frequency, repetition);
     free(count);
     free(lr);

@@ -48,6 +48,7 @@ __all__ = [
     "forks",
     "random_batch",
     "vocab_mask",
+    "logit_bias",
     "ablation",
     "ABLATION_STAGES",
     "WORKLOADS",
@@ -86,6 +87,9 @@ class SamplerBatch:
     philox_offset: int = 0
     want_probs: bool = False
     vocab_mask: Optional[np.ndarray] = None  # [n_rows, ceil(vocab / 32)] uint32; bit set = allowed
+    bias_offsets: Optional[np.ndarray] = None  # [n_rows + 1] int32: logit_bias entries of row r are
+    bias_ids: Optional[np.ndarray] = None      # bias_ids / bias_values[bias_offsets[r] .. [r + 1])
+    bias_values: Optional[np.ndarray] = None
     notes: dict = field(default_factory=dict)
 
     @property
@@ -296,6 +300,23 @@ def vocab_mask(seed: int, n: int, v: int, allowed: float = 0.1, full_rows: int =
         bits = ok.reshape(words, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)
         out[r] = bits.sum(axis=1).astype(np.uint32)
     return out
+
+
+def logit_bias(seed: int, n: int, v: int, max_per_row: int = 64, scale: float = 5.0):
+    """Per-row logit_bias lists in CSR form (offsets, ids, values): 0..max_per_row
+    entries per row, ids uniform over the vocabulary with a few repeats, values
+    ~ scale * N(0,1) with some -inf (banned) and some large (forced) entries."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = rng.integers(0, max_per_row + 1, size=n)
+    offs = np.zeros(n + 1, np.int32)
+    offs[1:] = np.cumsum(lens)
+    ids = rng.integers(0, v, size=int(offs[-1])).astype(np.int32)
+    rep_at = rng.random(ids.size) < 0.05
+    ids[1:][rep_at[1:]] = ids[:-1][rep_at[1:]]  # repeated ids add up
+    vals = (rng.standard_normal(ids.size) * scale).astype(np.float32)
+    vals[rng.random(ids.size) < 0.05] = -np.inf
+    vals[rng.random(ids.size) < 0.02] = np.float32(50.0)
+    return offs, ids, vals
 
 
 ABLATION_STAGES = ("plain", "topkp", "minp", "penalties")
