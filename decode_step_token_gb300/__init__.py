@@ -125,17 +125,20 @@ class Sampler:
     def sample_ex_args(self, args: sampler_args_t, top_n: int = 0, unscaled: bool = False,
                        out_token_logprob=None, out_top_ids=None, out_top_logprobs=None,
                        vocab_mask=None, mask_stride: Optional[int] = None,
+                       bias_offsets=None, bias_ids=None, bias_values=None,
                        stream: Optional[int] = None) -> None:
         """sampler_sample_ex: the step plus per-row logprob outputs (device tensors:
         out_token_logprob [N] fp32, out_top_ids / out_top_logprobs [N, top_n]
-        int32 / fp32) and a vocabulary bitmask (device [N, words] int32/uint32)."""
+        int32 / fp32), a vocabulary bitmask (device [N, words] int32/uint32) and
+        logit_bias lists (device CSR: offsets [N + 1], ids, fp32 values)."""
         if stream is None:
             import torch
             stream = torch.cuda.current_stream(self.device).cuda_stream
         if vocab_mask is not None and mask_stride is None:
             mask_stride = int(vocab_mask.shape[-1])
         ext = sampler_ext_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob), _ptr(out_top_ids),
-                            _ptr(out_top_logprobs), _ptr(vocab_mask), int(mask_stride or 0))
+                            _ptr(out_top_logprobs), _ptr(vocab_mask), int(mask_stride or 0),
+                            _ptr(bias_offsets), _ptr(bias_ids), _ptr(bias_values))
         rc = sampler_sample_ex(self._h, args, ext, stream)
         if rc != SAMPLER_OK:
             raise SamplerError(rc, "sampler_sample_ex")

@@ -42,6 +42,7 @@ EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_
 SAMPLER_STAT_EXACT_ROWS = 0
 SAMPLER_NOALLOC_MAX_ROWS = 64
 SAMPLER_MAX_TOP_N = 16
+SAMPLER_MAX_BIAS = 64
 
 
 class sampler_config_t(ctypes.Structure):
@@ -97,6 +98,9 @@ class sampler_ext_t(ctypes.Structure):
         ("out_top_logprobs", _P),
         ("vocab_mask", _P),
         ("mask_stride", ctypes.c_int64),
+        ("bias_offsets", _P),
+        ("bias_ids", _P),
+        ("bias_values", _P),
     ]
 
 

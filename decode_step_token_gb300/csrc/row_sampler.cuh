@@ -96,6 +96,10 @@ struct KernelParams {
     // word v >> 5 of row r's mask set = token v allowed
     const uint32_t* vocab_mask;
     int64_t mask_stride;
+    // logit_bias of sampler_sample_ex (slice kernel only), CSR by output row
+    const int32_t* bias_offsets;
+    const int32_t* bias_ids;
+    const float* bias_values;
 };
 
 // ------------------------------------------------------------------ records

@@ -325,7 +325,9 @@ int sampler_sample_ex(sampler_t h, const sampler_args_t* a, const sampler_ext_t*
         if (ext->top_n < 0 || ext->top_n > SAMPLER_MAX_TOP_N) return SAMPLER_ERR_UNSUPPORTED;
         if (ext->top_n > 0 && (!ext->out_top_ids || !ext->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
         if (ext->vocab_mask && ext->mask_stride < (a->vocab + 31) / 32) return SAMPLER_ERR_UNSUPPORTED;
-        if (!ext->out_token_logprob && ext->top_n == 0 && !ext->vocab_mask) ext = nullptr;  // nothing asked
+        if (ext->bias_offsets && (!ext->bias_ids || !ext->bias_values)) return SAMPLER_ERR_NULL_ARG;
+        if (!ext->out_token_logprob && ext->top_n == 0 && !ext->vocab_mask && !ext->bias_offsets)
+            ext = nullptr;  // nothing asked
     }
     if (a->n_rows == 0) return SAMPLER_OK;
     DeviceGuard guard;

@@ -14,6 +14,7 @@ static_assert(slc::kMaxRows <= slc::kT, "one thread per row classifies the batch
 static_assert(slc::kHead < slc::kMaxSmem, "shared-memory head");
 
 static_assert(kSliceMaxRows == slc::kMaxRows && kSliceMaxSlices == slc::kMaxSlices, "slice limits");
+static_assert(slc::kMaxTopN == SAMPLER_MAX_TOP_N && slc::kMaxBias == SAMPLER_MAX_BIAS, "extension limits");
 static_assert(kSliceHdrBytes == sizeof(slc::SliceHdr) && kSliceBodyBytes == sizeof(slc::SliceBody),
               "slice record sizes");
 static_assert(kSliceCntStride == slc::kCntStride, "counter stride");
@@ -103,6 +104,9 @@ int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGe
         k.lp_unscaled = lp->unscaled ? 1 : 0;
         k.vocab_mask = lp->vocab_mask;
         k.mask_stride = lp->mask_stride;
+        k.bias_offsets = lp->bias_offsets;
+        k.bias_ids = lp->bias_ids;
+        k.bias_values = lp->bias_values;
     }
     p.n_rows = int(a->n_rows);
     p.G = g.G;

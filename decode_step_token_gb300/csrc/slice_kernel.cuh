@@ -48,6 +48,17 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     if (!(ri.minp >= 0.0f && ri.minp <= 1.0f)) bad = true;
     if (!isfinite(pres) || !isfinite(freq)) bad = true;
     if (!(rep > 0.0f) || isinf(rep)) bad = true;
+    if (kp.bias_offsets) {  // logit_bias: at most kMaxBias entries, every id in the vocabulary
+        const int b0 = kp.bias_offsets[r], b1 = kp.bias_offsets[r + 1];
+        if (b1 - b0 > kMaxBias || b1 < b0) {
+            bad = true;
+        } else {
+            for (int j = b0; j < b1; ++j) {
+                const int id = kp.bias_ids[j];
+                if (id < 0 || int64_t(id) >= V) bad = true;
+            }
+        }
+    }
     const bool greedy = T < 1e-5f;
     ri.T = greedy ? 1.0f : T;
     ri.invT = 1.0f / ri.T;
@@ -185,6 +196,95 @@ __device__ __forceinline__ void unit_max(const SliceView<InT>& sv, float& mx, in
     int li = INT_MAX;
     if (mx > -INFINITY && lm == mx) li = lane_find<InT>(sv, lm);
     amax = __reduce_min_sync(0xffffffffu, li);
+}
+
+// ---------------------------------------------------------------- logit_bias
+// Row r's logit of token v after its bias entries (one fp32 addition each, in
+// list order) and its vocabulary mask: one thread's view, for the few tokens
+// read again one by one.
+template <typename InT>
+__device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowInfo& ri, int v)
+{
+    float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
+        return -INFINITY;
+    if (kp.bias_offsets) {
+        const int b1 = kp.bias_offsets[ri.r + 1];
+        for (int j = kp.bias_offsets[ri.r]; j < b1; ++j)
+            if (kp.bias_ids[j] == v) x = x + kp.bias_values[j];
+    }
+    return x;
+}
+
+// The row's biased tokens in [lo, hi) with their biased, masked logits (each
+// token once), written to xi / xv; returns how many (at most kMaxBias). Warp-wide.
+template <typename InT>
+__device__ __noinline__ int row_extras(const KernelParams& kp, const RowInfo& ri, int lo, int hi, int32_t* xi,
+                                       float* xv)
+{
+    const int lane = threadIdx.x & 31;
+    const int b0 = kp.bias_offsets[ri.r];
+    const int L = kp.bias_offsets[ri.r + 1] - b0;
+    int cnt = 0;
+#pragma unroll 1
+    for (int e0 = 0; e0 < L; e0 += 32) {
+        const int e = e0 + lane;
+        const int id = e < L ? kp.bias_ids[b0 + e] : -1;
+        bool first = e < L && id >= lo && id < hi;
+        for (int j = 0; first && j < e; ++j) first = kp.bias_ids[b0 + j] != id;  // its first entry
+        float x = 0.0f;
+        if (first) x = biased_logit<InT>(kp, ri, id);
+        const uint32_t bal = __ballot_sync(0xffffffffu, first);
+        if (first) {
+            const int at = cnt + __popc(bal & ((1u << lane) - 1u));
+            xi[at] = id;
+            xv[at] = x;
+        }
+        cnt += __popc(bal);
+    }
+    __syncwarp();
+    return cnt;
+}
+
+// Whether token v is among the n biased tokens xi.
+__device__ __forceinline__ bool is_extra(const int32_t* xi, int n, int v)
+{
+    for (int q = 0; q < n; ++q)
+        if (xi[q] == v) return true;
+    return false;
+}
+
+// Flags of the extras' values (NaN or +inf: non-finite; finite: any finite).
+__device__ __forceinline__ uint32_t extras_flags(const float* xv, int n)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t f = 0;
+    for (int q = lane; q < n; q += 32) {
+        const float x = xv[q];
+        if (x != x || x == INFINITY) f |= kFlagNonFinite;
+        if (x > -INFINITY && x < INFINITY) f |= kFlagAnyFinite;
+    }
+    return warp_or(f);
+}
+
+// Merge the extras into a unit maximum (value desc, index asc; NaN ignored).
+__device__ __forceinline__ void extras_max(const int32_t* xi, const float* xv, int n, float& mx, int& amax)
+{
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY;
+    int mi = INT_MAX;
+    for (int q = lane; q < n; q += 32) {
+        const float x = xv[q];
+        if (x > m || (x == m && xi[q] < mi)) {
+            m = x;
+            mi = xi[q];
+        }
+    }
+    warp_max_idx(m, mi);
+    if (m > mx || (m == mx && mi < amax)) {
+        mx = m;
+        amax = mi;
+    }
 }
 
 // ---------------------------------------------------------------- plain unit
@@ -349,7 +449,8 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
 // Sum over the unit of exp2((x - mx) * s2) (Kahan per lane, double across the
 // warp), as a high and a low fp32 part.
 template <typename InT>
-__device__ __noinline__ void unit_mass(const SliceView<InT>& sv, float mx, float s2, float& hi, float& lo)
+__device__ __noinline__ void unit_mass(const SliceView<InT>& sv, float mx, float s2, float& hi, float& lo,
+                                       const float* xv = nullptr, int nx = 0)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -368,6 +469,8 @@ __device__ __noinline__ void unit_mass(const SliceView<InT>& sv, float mx, float
         }
     }
     double z = double(zs) - double(zc);
+    for (int q = lane; q < nx; q += 32)  // biased tokens (read as -inf above)
+        if (xv[q] > -INFINITY) z += double(exp2f((xv[q] - mx) * s2));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     hi = float(z);
@@ -376,7 +479,8 @@ __device__ __noinline__ void unit_mass(const SliceView<InT>& sv, float mx, float
 
 template <typename InT>
 __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowInfo& ri, SliceHdr& hdr_out,
-                                           SliceBody* body, uint32_t* q)
+                                           SliceBody* body, uint32_t* q, const int32_t* xi = nullptr,
+                                           const float* xv = nullptr, int nx = 0)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -384,6 +488,13 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     int amax;
     uint32_t flags;
     unit_max<InT>(sv, mx, amax, flags, lm);
+    // biased tokens (read as -inf by sv) count in the maximum, the flags, the
+    // list and the mass, not in the lane maxima: the sketch and tau keep their
+    // meaning (tokens of the unit that reach them)
+    if (nx) {
+        flags |= extras_flags(xv, nx);
+        extras_max(xi, xv, nx, mx, amax);
+    }
     SLC_MARK(4);
     // the sketch: the m largest lane maxima (order keys, descending), from each
     // lane's rank among the 32 (ties by lane); tau, the mt-th largest, so that at
@@ -423,8 +534,22 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
         total += __reduce_add_sync(0xffffffffu, uint32_t(__popc(hit)));
     }
     SLC_MARK(18);
+    uint32_t xcount = 0;  // biased tokens that reach tau, listed after the others
+    for (int q0 = 0; q0 < nx; q0 += 32) {
+        const bool in = q0 + lane < nx && xv[q0 + lane] >= t;
+        xcount += __popc(__ballot_sync(0xffffffffu, in));
+    }
+    const uint32_t total_nx = total;
+    total += xcount;
     if (total <= uint32_t(kLCap)) {  // else the list is not kept (overflow)
         __syncwarp();
+        uint32_t xbase = total_nx;
+        for (int q0 = 0; q0 < nx; q0 += 32) {
+            const bool in = q0 + lane < nx && xv[q0 + lane] >= t;
+            const uint32_t bal = __ballot_sync(0xffffffffu, in);
+            if (in) body->list[xbase + __popc(bal & ((1u << lane) - 1u))] = cand_word(f2key(xv[q0 + lane]), xi[q0 + lane]);
+            xbase += __popc(bal);
+        }
         uint32_t base = 0;
 #pragma unroll 1
         for (int i0 = 0; i0 < nq; i0 += 32) {
@@ -455,7 +580,7 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     // logprob outputs over the whole row: the same at the outputs' temperature
     float zsum = 0.0f, zlow = 0.0f;
     const bool fin = mx > -INFINITY && mx < INFINITY;
-    if (ri.need_z && fin) unit_mass<InT>(sv, mx, ri.s2, zsum, zlow);
+    if (ri.need_z && fin) unit_mass<InT>(sv, mx, ri.s2, zsum, zlow, xv, nx);
     if (lane == 0)
         *reinterpret_cast<uint4*>(&body->tau) = make_uint4(tau, __float_as_uint(zsum), __float_as_uint(zlow), m);
     if (ri.need_zo) {
@@ -464,7 +589,7 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
             os = zsum;
             ol = zlow;
         } else if (fin) {
-            unit_mass<InT>(sv, mx, ri.s2o, os, ol);
+            unit_mass<InT>(sv, mx, ri.s2o, os, ol, xv, nx);
         }
         if (lane == 0) *reinterpret_cast<uint4*>(&body->zos) = make_uint4(__float_as_uint(os), __float_as_uint(ol), 0u, 0u);
     }
@@ -510,7 +635,7 @@ static __device__ __noinline__ double exact_score(const KernelParams& kp, const 
                                                   uint32_t off_hi, int v)
 {
     const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
-    const float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    const float x = biased_logit<InT>(kp, ri, v);
     return gumbel_score_f64(x, ri.T, philox_word(rp, v));
 }
 
@@ -924,7 +1049,8 @@ static __device__ __noinline__ uint4 load_vec_slow(const InT* g, int j, int n)
 // Returns the new count (more than cap when they do not fit).
 template <typename InT>
 static __device__ __noinline__ int reread_slices(const SliceParams& P, const RowInfo& ri, const uint16_t* re,
-                                                 int nre, uint32_t B, unsigned long long* c, int C0, int cap)
+                                                 int nre, uint32_t B, unsigned long long* c, int C0, int cap,
+                                                 int32_t* xi, float* xv)
 {
     constexpr int E = Vec<InT>::E;
     constexpr int U = 8;
@@ -935,6 +1061,9 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
     // x >= tB exactly when x is not -inf and its key reaches B
     const float tB = B < 0x00800000u ? -FLT_MAX : key2f(B);
     const typename Vec<InT>::Thr t2 = Vec<InT>::thr(tB);
+    // logit_bias: the row's biased tokens are taken apart (their raw logits
+    // skipped below, their biased values appended at the end)
+    const int nx = P.k.bias_offsets ? row_extras<InT>(P.k, ri, 0, V, xi, xv) : 0;
     int C = C0;
 #pragma unroll 1
     for (int base = 0; base < total; base += 32 * U) {
@@ -963,10 +1092,19 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
                 }
             }
         }
+        uint32_t hits[U];
         uint32_t mine = 0;
 #pragma unroll
-        for (int u = 0; u < U; ++u) mine += Vec<InT>::count_ge(v[u], t2);
-        mine = Vec<InT>::count_fold(mine);
+        for (int u = 0; u < U; ++u) {
+            uint32_t h = Vec<InT>::mask_ge(v[u], t2);
+            if (nx)
+                for (uint32_t b2 = h; b2; b2 &= b2 - 1u) {
+                    const int e = __ffs(b2) - 1;
+                    if (is_extra(xi, nx, t0[u] + e)) h &= ~(1u << e);
+                }
+            hits[u] = h;
+            mine += __popc(h);
+        }
         SLC_MARK(15);
         uint32_t incl = mine;
 #pragma unroll
@@ -978,13 +1116,26 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
 #pragma unroll
         for (int u = 0; u < U; ++u) {
 #pragma unroll 1
-            for (uint32_t hit = Vec<InT>::mask_ge(v[u], t2); hit; hit &= hit - 1u) {
+            for (uint32_t hit = hits[u]; hit; hit &= hit - 1u) {
                 const int e = __ffs(hit) - 1;
                 if (pos < uint32_t(cap)) c[pos] = cand_word(f2key(Vec<InT>::get(v[u], e)), t0[u] + e);
                 ++pos;
             }
         }
         C += int(__shfl_sync(0xffffffffu, incl, 31));
+    }
+    // the biased tokens of the slices read again that reach B
+    for (int q0 = 0; q0 < nx; q0 += 32) {
+        const int q = q0 + lane;
+        bool in = false;
+        if (q < nx && xv[q] >= tB) {
+            const int b = xi[q] / P.W;
+            for (int i = 0; i < nre; ++i) in |= int(re[i]) == b;
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, in);
+        const uint32_t pos = uint32_t(C) + __popc(bal & ((1u << lane) - 1u));
+        if (in && pos < uint32_t(cap)) c[pos] = cand_word(f2key(xv[q]), xi[q]);
+        C += __popc(bal);
     }
     __syncwarp();
     return C;
@@ -1102,7 +1253,7 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
     if (total > uint32_t(cap) || nre > uint32_t(kReCap)) return false;
     int C = compact_ge(area, int(total), B);
     SLC_MARK(9);
-    if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap);
+    if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap, ws.xi, ws.xv);
     SLC_MARK(10);
     if (C > cap) return false;
     if (ri.do_topk && C < ri.k) return false;
@@ -1181,7 +1332,7 @@ static __device__ __noinline__ bool finish_lp_row(const SliceParams& P, WarpScra
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float lz2 = log2f(float(z));
-    const float xt = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + token);
+    const float xt = biased_logit<InT>(kp, ri, token);
     int C = 0;
     if (n > 0) {
         // B: the 16-bit prefix of the n-th largest sketch key (all listed tokens
@@ -1224,7 +1375,7 @@ static __device__ __noinline__ bool finish_lp_row(const SliceParams& P, WarpScra
         bool ok = total <= uint32_t(cap) && nre <= uint32_t(kReCap);
         if (ok) {
             C = compact_ge(area, int(total), B);
-            if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap);
+            if (nre) C = reread_slices<InT>(P, ri, ws.re, int(nre), B, area, C, cap, ws.xi, ws.xv);
             ok = C <= cap && 2 * C <= cap && C <= kRankSortMax;
         }
         if (!ok) return false;  // more candidates than the lists settle here (ties): the exact path
@@ -1275,13 +1426,44 @@ __device__ __forceinline__ int cta_excl_scan(int v, int& total, SliceShared& sh)
     return before + s - v;
 }
 
+// Token v of the row: masked, and biased from the CTA's table (set up by
+// cta_bias_setup) when the row carries logit_bias.
 template <typename InT>
-__device__ __forceinline__ float row_x(const KernelParams& kp, const RowInfo& ri, int v)
+__device__ __forceinline__ float row_x(const KernelParams& kp, const RowInfo& ri, int v, const SliceShared& sh)
 {
     const float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
     if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
         return -INFINITY;
+    if (sh.bx_n && ((sh.bx_bits[v >> 5] >> (v & 31)) & 1u))
+        for (int q = 0; q < sh.bx_n; ++q)
+            if (sh.bx_i[q] == v) return sh.bx_v[q];
     return x;
+}
+
+// The row's logit_bias for the CTA's exact path: its biased tokens (warp 0)
+// and their bitmap in the idle staging slots.
+template <typename InT>
+__device__ __forceinline__ void cta_bias_setup(SliceShared& sh, unsigned char* slots, const KernelParams& kp,
+                                               const RowInfo& ri)
+{
+    const int tid = threadIdx.x, V = int(kp.vocab);
+    if (!kp.bias_offsets) {
+        if (tid == 0) sh.bx_n = 0;
+        __syncthreads();
+        return;
+    }
+    uint32_t* bits = reinterpret_cast<uint32_t*>(slots);
+    for (int w = tid; w < (V + 31) / 32; w += kT) bits[w] = 0u;
+    if (tid < 32) {
+        const int n = row_extras<InT>(kp, ri, 0, V, sh.bx_i, sh.bx_v);
+        if (tid == 0) {
+            sh.bx_n = n;
+            sh.bx_bits = bits;
+        }
+    }
+    __syncthreads();
+    for (int q = tid; q < sh.bx_n; q += kT) atomicOr(&bits[sh.bx_i[q] >> 5], 1u << (sh.bx_i[q] & 31));
+    __syncthreads();
 }
 
 // The token closing the kept prefix: the first token (value desc, index asc)
@@ -1309,7 +1491,7 @@ __device__ void cta_select(SliceShared& sh, const KernelParams& kp, const RowInf
         const uint32_t prefix = uint32_t(sh.sel_prefix);
         const int shift = 24 - 8 * level;
         for (int v = tid; v < V; v += kT) {
-            const float x = row_x<InT>(kp, ri, v);
+            const float x = row_x<InT>(kp, ri, v, sh);
             if (!(x > -INFINITY)) continue;
             const uint32_t key = f2key(x);
             if (dom && !in_prefix(key, v, dkey, didx)) continue;
@@ -1348,7 +1530,7 @@ __device__ void cta_select(SliceShared& sh, const KernelParams& kp, const RowInf
         const int v = v0 + tid;
         int c = 0;
         if (v < V) {
-            const float x = row_x<InT>(kp, ri, v);
+            const float x = row_x<InT>(kp, ri, v, sh);
             const uint32_t key = f2key(x);
             c = (x > -INFINITY && key == K && (!dom || in_prefix(key, v, dkey, didx))) ? 1 : 0;
         }
@@ -1365,12 +1547,13 @@ __device__ void cta_select(SliceShared& sh, const KernelParams& kp, const RowInf
 }
 
 template <typename InT>
-__device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P, int r, const RowInfo& ri, float m,
-                                           uint32_t off_lo, uint32_t off_hi)
+__device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots, const SliceParams& P, int r,
+                                           const RowInfo& ri, float m, uint32_t off_lo, uint32_t off_hi)
 {
     const KernelParams& kp = P.k;
     const int V = int(kp.vocab);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    cta_bias_setup<InT>(sh, slots, kp, ri);
     uint32_t bk = 0;
     int bi = 0;
     bool hb = false;
@@ -1397,7 +1580,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
     double z = 0.0;
     uint32_t nk = 0;
     for (int v = tid; v < V; v += kT) {
-        const float x = row_x<InT>(kp, ri, v);
+        const float x = row_x<InT>(kp, ri, v, sh);
         if (!(x > -INFINITY)) continue;
         const bool kept = !(hb && !in_prefix(f2key(x), v, bk, bi)) && !(ri.do_minp && !(x >= xthr));
         if (ri.lp && (kept || !lp_kept)) {
@@ -1457,7 +1640,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
     __syncthreads();
     if (n > 0) {
         for (int v = tid; v < V; v += kT) {
-            const float x = row_x<InT>(kp, ri, v);
+            const float x = row_x<InT>(kp, ri, v, sh);
             if (x > -INFINITY && in_prefix(f2key(x), v, nkey, nidx)) {
                 const int q = atomicAdd(&sh.lp_cnt, 1);
                 if (q < kMaxTopN) sh.lp_list[q] = cand_word(f2key(x), v);
@@ -1477,7 +1660,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
         __syncwarp();
         if (lane < c) sh.lp_list[rank] = w;
         __syncwarp();
-        const float xt = row_x<InT>(kp, ri, token);
+        const float xt = row_x<InT>(kp, ri, token, sh);
         lp_write(kp, r, sh.lp_list, c, m, ri.s2o, log2f(float(zt)), xt);
     }
     __syncthreads();
@@ -1487,8 +1670,9 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, const SliceParams& P
 // Wait for the warp's slot, summarise the unit into its record (row r, slice s).
 template <typename InT>
 __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo& ri, uint64_t* bar,
-                                             const unsigned char* slot, uint16_t* q, uint4* qw, uint32_t parity, int r,
-                                             int s, uint32_t off_lo, uint32_t off_hi)
+                                             const unsigned char* slot, uint16_t* q, uint4* qw, int32_t* xi,
+                                             float* xv, uint32_t parity, int r, int s, uint32_t off_lo,
+                                             uint32_t off_hi)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -1525,6 +1709,28 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
         }
         __syncwarp();
     }
+    int nx = 0;
+    if (kp.bias_offsets && !extra) {
+        // logit_bias: the unit's biased tokens are taken apart with their biased
+        // values; the view reads them as -inf (patched in the staged vectors)
+        nx = row_extras<InT>(kp, ri, c0, c0 + n_el, xi, xv);
+        uint32_t* smw = reinterpret_cast<uint32_t*>(const_cast<unsigned char*>(slot));
+        for (int i = lane; i < nx; i += 32) {
+            const int o = xi[i] - c0;
+            if (o / E < sv.nb) {
+                if (sizeof(InT) == 2) {
+                    const int sh = 16 * (o & 1);
+                    atomicOr(&smw[o >> 1], 0xFF80u << sh);
+                    atomicAnd(&smw[o >> 1], ~(0x007Fu << sh));
+                } else {
+                    smw[o] = 0xFF800000u;
+                }
+            }
+        }
+        __syncwarp();
+        sv.xi = xi;
+        sv.nx = nx;
+    }
     SliceHdr hdr;
     hdr.mx = -INFINITY;
     hdr.amax = INT_MAX;
@@ -1536,13 +1742,28 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
         if (ri.cls == kClsGreedy) {
             float lm;
             unit_max<InT>(sv, hdr.mx, hdr.amax, hdr.flags, lm);
-            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
+            if (nx) {
+                hdr.flags |= extras_flags(xv, nx);
+                extras_max(xi, xv, nx, hdr.mx, hdr.amax);
+            }
+            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         } else if (ri.cls == kClsPlain) {
             unit_plain<InT>(sv, ri, off_lo, off_hi, q, qw, g, hdr.flags);
+            if (nx) {  // the biased tokens, scored exactly
+                hdr.flags |= extras_flags(xv, nx);
+                const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
+                K2 t{0ull, 0ull};
+                for (int i = lane; i < nx; i += 32)
+                    if (xv[i] > -INFINITY && xv[i] < INFINITY)
+                        k2_insert(t, gkey(score2(xv[i], ri.s2, philox_word(rp, xi[i])), xi[i]));
+                k2_warp_reduce(t);
+                if (t.a) k2_insert(g, t.a);
+                if (t.b) k2_insert(g, t.b);
+            }
             __syncwarp();
-            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
+            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         } else {
-            unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q));
+            unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         }
     }
     hdr.flags |= extra;
@@ -1650,7 +1871,7 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
         first = false;
         SLC_MARK(2);
         SLC_UCLS(ri.cls);
-        process_unit<InT>(P, ri, bar, slot, ws.q, ws.qw, parity, r, s, off_lo, off_hi);
+        process_unit<InT>(P, ri, bar, slot, ws.q, ws.qw, ws.xi, ws.xv, parity, r, s, off_lo, off_hi);
         SLC_MARK(5);
         parity ^= 1u;
         const int un = u + stride;
@@ -1694,7 +1915,7 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
     const int ne = sh.n_exact;
     for (int q = 0; q < ne; ++q) {
         const int r = sh.exact_rows[q];
-        cta_exact_row<InT>(sh, P, r, load_info(P, r), sh.exact_m[q], off_lo, off_hi);
+        cta_exact_row<InT>(sh, smem + kHead, P, r, load_info(P, r), sh.exact_m[q], off_lo, off_hi);
     }
 }
 

@@ -67,6 +67,7 @@ constexpr int kSketch = 8;              // lane maxima a truncated unit exposes
 constexpr int kLCap = 48;               // list entries one record holds
 constexpr int kKComplete = 32;          // top-k rows up to this k list each unit's top k
 constexpr int kMaxTopN = 16;            // largest top_n of the logprob outputs
+constexpr int kMaxBias = 64;            // logit_bias entries a row may carry
 constexpr int kTQCap = 320;             // vectors a truncated unit queues (more: the list overflows)
 constexpr int kKCap = 128;              // largest top-k the lists settle
 constexpr int kReCap = 16;              // slices a finishing warp may read again
@@ -140,6 +141,8 @@ struct alignas(16) WarpScratch {
     uint16_t q[kSlotBytes / 16];        // plain units: vectors the cheap bound let through;
                                         // truncated units: (vector << 8 | mask) words
     uint4 qw[2 * 32];                   // Philox words of the first 32 queued vectors
+    int32_t xi[kMaxBias];               // logit_bias: the unit's biased tokens ...
+    float xv[kMaxBias];                 // ... and their biased (masked) logits
     uint32_t n;                         // candidates listed
     uint32_t nre;                       // slices to read again
     uint16_t re[kReCap];
@@ -159,6 +162,12 @@ struct alignas(16) SliceShared {
     unsigned long long red_k[2 * kW];
     unsigned long long sel_prefix, sel_wabove, sel_target;
     double red_d[kW];
+    // logit_bias on the exact path: the row's biased tokens, their values, and
+    // a bitmap of them (in the idle staging slots)
+    int32_t bx_i[kMaxBias];
+    float bx_v[kMaxBias];
+    int32_t bx_n;
+    uint32_t* bx_bits;
     unsigned long long lp_list[kMaxTopN];
     int32_t lp_cnt;
     int32_t sel_idx;
@@ -324,6 +333,8 @@ struct SliceView {
     int c0;          // first token of the slice
     const uint32_t* mw = nullptr;  // vocabulary mask words (NULL: none) ...
     int mbase = 0;                 // ... mw[0] being word mbase of the row's mask
+    const int32_t* xi = nullptr;   // biased tokens, read as -inf here (their biased
+    int nx = 0;                    // values are taken apart)
 
     __device__ __forceinline__ uint4 vec(int j) const
     {
@@ -341,8 +352,17 @@ struct SliceView {
                 w[q] = i < n ? reinterpret_cast<const uint32_t*>(g)[i] : 0xFF800000u;
             }
         }
-        const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
-        return mw ? Vec<InT>::masked(v, mask_bits(j)) : v;
+        uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+        if (mw) v = Vec<InT>::masked(v, mask_bits(j));
+        if (nx) {
+            uint32_t keep = (1u << E) - 1u;
+            for (int q = 0; q < nx; ++q) {
+                const int e = xi[q] - (c0 + j * E);
+                if (e >= 0 && e < E) keep &= ~(1u << e);
+            }
+            v = Vec<InT>::masked(v, keep);
+        }
+        return v;
     }
     // the allowed-token bits of vector j (bit e: element e)
     __device__ __forceinline__ uint32_t mask_bits(int j) const

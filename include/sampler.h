@@ -251,9 +251,18 @@ int sampler_sample_noalloc(const sampler_args_t* args, sampler_stream_t stream);
  * set means token v is allowed; a disallowed token's logit is -inf (after the
  * penalties). A row with no allowed finite logit reports SAMPLER_ROW_ALL_NEG_INF.
  *
+ * logit_bias: output row r's entries j in [bias_offsets[r], bias_offsets[r + 1])
+ * each add bias_values[j] to the logit of token bias_ids[j] (one fp32
+ * addition each, in list order, so a repeated token adds up), before the
+ * penalties and the mask. At most SAMPLER_MAX_BIAS entries per row; more, or an
+ * id outside [0, vocab), is SAMPLER_ROW_BAD_PARAM. The MLX help text on the
+ * manual lists logit_bias among the sampler's inputs without defining it; this
+ * is the reading taken.
+ *
  * Every pointer is a device pointer on the handle's device.
  */
 #define SAMPLER_MAX_TOP_N 16
+#define SAMPLER_MAX_BIAS 64
 typedef struct {
     int32_t top_n;                /* 0 .. SAMPLER_MAX_TOP_N */
     int32_t unscaled;             /* 0: log_softmax(x / T) over the kept set; 1: log_softmax(x) */
@@ -262,6 +271,9 @@ typedef struct {
     float* out_top_logprobs;      /* [N * top_n] */
     const uint32_t* vocab_mask;   /* [N * mask_stride] words; NULL = every token allowed */
     int64_t mask_stride;          /* words between rows' masks, >= ceil(vocab / 32) */
+    const int32_t* bias_offsets;  /* [N + 1] CSR offsets of the logit_bias entries; NULL = none */
+    const int32_t* bias_ids;      /* [bias_offsets[N]] tokens */
+    const float* bias_values;     /* [bias_offsets[N]] values */
 } sampler_ext_t;
 
 /* sampler_sample plus the extensions of `ext` (NULL: none). Offered on the

@@ -62,6 +62,9 @@ def to_device(batch, device="cuda:0", want_probs: Optional[bool] = None, copies:
         "out_probs": torch.empty((N, V), dtype=torch.float32, device=dev) if want else None,
         "out_logprobs": torch.empty((N, V), dtype=torch.float32, device=dev) if want else None,
         "vocab_mask": t(batch.vocab_mask.view(np.int32)) if batch.vocab_mask is not None else None,
+        "bias_offsets": t(batch.bias_offsets),
+        "bias_ids": t(batch.bias_ids),
+        "bias_values": t(batch.bias_values),
     }
     return d
 
@@ -83,6 +86,12 @@ def sample_args(sampler, batch, d, copy_index: int = 0, philox_offset: Optional[
         out_status=d["out_status"])
 
 
+def ext_kw(d):
+    """The mask and logit_bias arguments of sample_ex_args for device buffers `d`."""
+    return dict(vocab_mask=d["vocab_mask"], bias_offsets=d["bias_offsets"], bias_ids=d["bias_ids"],
+                bias_values=d["bias_values"])
+
+
 class GpuResult:
     def __init__(self, tokens, status, probs, logprobs):
         self.tokens, self.status, self.probs, self.logprobs = tokens, status, probs, logprobs
@@ -94,8 +103,8 @@ def run(sampler, batch, want_probs: Optional[bool] = None, device="cuda:0",
     import torch
 
     d = to_device(batch, device, want_probs, logits_offset_elems=logits_offset_elems)
-    if d["vocab_mask"] is not None:
-        sampler.sample_ex_args(sample_args(sampler, batch, d), vocab_mask=d["vocab_mask"])
+    if d["vocab_mask"] is not None or d["bias_offsets"] is not None:
+        sampler.sample_ex_args(sample_args(sampler, batch, d), **ext_kw(d))
     else:
         sampler.sample_args(sample_args(sampler, batch, d))
     torch.cuda.synchronize()
@@ -123,7 +132,7 @@ def run_logprobs(sampler, batch, top_n: int, unscaled: bool = False, device="cud
     lps = torch.full((N, max(top_n, 1)), 7.0, dtype=torch.float32, device=device)
     sampler.sample_ex_args(sample_args(sampler, batch, d), top_n=top_n, unscaled=unscaled,
                            out_token_logprob=tok_lp, out_top_ids=ids if top_n else None,
-                           out_top_logprobs=lps if top_n else None, vocab_mask=d["vocab_mask"])
+                           out_top_logprobs=lps if top_n else None, **ext_kw(d))
     torch.cuda.synchronize()
     return GpuLogprobResult(d["out_tokens"].cpu().numpy(), d["out_status"].cpu().numpy(),
                             tok_lp.cpu().numpy() if tok_lp is not None else None,
