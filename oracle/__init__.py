@@ -63,12 +63,12 @@ def _load():
             lib.oracle_sample.argtypes = (
                 [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P]
                 + [P] * 10 + [P, P, ctypes.c_uint64, ctypes.c_uint64, P, ctypes.c_int64, P, P, P]
-                + [P, ctypes.c_int64] + [P] * 5 + [ctypes.c_int])
+                + [P, P, P, ctypes.c_int] + [P, ctypes.c_int64] + [P] * 5 + [ctypes.c_int])
             lib.oracle_sample.restype = ctypes.c_int
             lib.oracle_penalized_logits.argtypes = [
                 P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_float, ctypes.c_float, ctypes.c_float, P, P, P, ctypes.c_int64,
-                P, P, P, ctypes.c_int64, P]
+                P, P, P, P, P, P, ctypes.c_int, ctypes.c_int64, P]
             lib.oracle_penalized_logits.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -121,11 +121,15 @@ def penalized_logits(batch, row: int):
     boff = _arr(batch.bias_offsets, np.int32)
     bids = _arr(batch.bias_ids, np.int32)
     bval = _arr(batch.bias_values, np.float32)
+    mtl = _arr(batch.min_tokens_left, np.int32)
+    soff = _arr(batch.stop_offsets, np.int32)
+    sids = _arr(batch.stop_ids, np.int32)
     rc = lib.oracle_penalized_logits(
         _ptr(logits), 1 if batch.dtype == "bf16" else 0, batch.vocab, batch.row_stride, lr,
         pick(batch.presence, 0.0), pick(batch.frequency, 0.0), pick(batch.repetition, 1.0),
         _ptr(hoff), _ptr(hids), _ptr(mask), 0 if mask is None else mask.shape[1],
-        _ptr(boff), _ptr(bids), _ptr(bval), row, _ptr(x))
+        _ptr(boff), _ptr(bids), _ptr(bval), _ptr(mtl), _ptr(soff), _ptr(sids),
+        1 if batch.sanitize_nan else 0, row, _ptr(x))
     if rc < 0:
         raise RuntimeError("oracle_penalized_logits failed")
     return rc, x
@@ -216,13 +220,17 @@ def sample(batch, rows: Optional[Sequence[int]] = None, want_probs: Optional[boo
     boff = _arr(batch.bias_offsets, np.int32)
     bids = _arr(batch.bias_ids, np.int32)
     bval = _arr(batch.bias_values, np.float32)
+    mtl = _arr(batch.min_tokens_left, np.int32)
+    soff = _arr(batch.stop_offsets, np.int32)
+    sids = _arr(batch.stop_ids, np.int32)
     rc = lib.oracle_sample(
         _ptr(logits), dtype, batch.n_rows, V, batch.row_stride, _ptr(lr),
         _ptr(t), _ptr(k), _ptr(p), _ptr(mp), _ptr(pres), _ptr(freq), _ptr(rep),
         _ptr(seed), _ptr(has_seed), _ptr(sid), _ptr(hoff), _ptr(hids),
         ctypes.c_uint64(batch.global_seed), ctypes.c_uint64(batch.philox_offset),
         _ptr(mask), 0 if mask is None else mask.shape[1],
-        _ptr(boff), _ptr(bids), _ptr(bval),
+        _ptr(boff), _ptr(bids), _ptr(bval), _ptr(mtl), _ptr(soff), _ptr(sids),
+        1 if batch.sanitize_nan else 0,
         _ptr(rows_arr), n_out, _ptr(tokens), _ptr(status), _ptr(probs), _ptr(logprobs),
         _ptr(diag), int(nthreads))
     if rc != 0:

@@ -165,10 +165,13 @@ typedef struct {
     uint64_t global_seed; uint64_t philox_offset;
     const uint32_t* vocab_mask; int64_t mask_stride;
     const int32_t* bias_offsets; const int32_t* bias_ids; const float* bias_values;
+    const int32_t* min_tokens_left; const int32_t* stop_offsets; const int32_t* stop_ids;
+    int sanitize_nan;
 } oracle_in_t;
 
-/* The library's documented per-row limit on logit_bias entries. */
+/* The library's documented per-row limits on logit_bias entries and stop tokens. */
 #define ORACLE_MAX_BIAS 64
+#define ORACLE_MAX_STOP 16
 
 /* Disallowed tokens of output row r's vocabulary bitmask become -inf: bit
  * (v & 31) of word v >> 5 of the row's mask set means token v is allowed (the
@@ -193,6 +196,10 @@ static int load_penalized_row(const oracle_in_t* in, int64_t r, float* x, int32_
     const int64_t V = in->vocab;
     const int64_t lrow = in->logit_row ? (int64_t)in->logit_row[r] : r;
     for (int64_t v = 0; v < V; ++v) x[v] = read_logit(in->logits, in->dtype, lrow * in->row_stride + v);
+    /* NaN sanitising (the manual's SGLANG_SANITIZE_NAN_LOGITS): a NaN logit is -inf */
+    if (in->sanitize_nan)
+        for (int64_t v = 0; v < V; ++v)
+            if (x[v] != x[v]) x[v] = -INFINITY;
     /* logit_bias: each entry adds its value to its token's logit, in list order
      * (one fp32 addition each), before the penalties */
     if (in->bias_offsets) {
@@ -203,6 +210,16 @@ static int load_penalized_row(const oracle_in_t* in, int64_t r, float* x, int32_
             if (id < 0 || (int64_t)id >= V) return ST_BAD_PARAM;
         }
         for (int32_t j = b0; j < b1; ++j) x[in->bias_ids[j]] = x[in->bias_ids[j]] + in->bias_values[j];
+    }
+    /* min_tokens (the first stage of the vLLM sampler the xbrilliance.ai note
+     * walks through): while a row still owes tokens, its stop tokens are -inf */
+    if (in->stop_offsets) {
+        const int32_t s0 = in->stop_offsets[r], s1 = in->stop_offsets[r + 1];
+        if (s1 - s0 > ORACLE_MAX_STOP) return ST_BAD_PARAM;
+        for (int32_t j = s0; j < s1; ++j)
+            if (in->stop_ids[j] < 0 || (int64_t)in->stop_ids[j] >= V) return ST_BAD_PARAM;
+        if (in->min_tokens_left && in->min_tokens_left[r] > 0)
+            for (int32_t j = s0; j < s1; ++j) x[in->stop_ids[j]] = -INFINITY;
     }
     if (!in->hist_offsets) {
         apply_mask(in, r, x);
@@ -389,6 +406,8 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
                   uint64_t global_seed, uint64_t philox_offset,
                   const uint32_t* vocab_mask, int64_t mask_stride,
                   const int32_t* bias_offsets, const int32_t* bias_ids, const float* bias_values,
+                  const int32_t* min_tokens_left, const int32_t* stop_offsets, const int32_t* stop_ids,
+                  int sanitize_nan,
                   const int64_t* rows, int64_t n_out,
                   int32_t* out_tokens, int32_t* out_status, float* out_probs, float* out_logprobs,
                   double* out_diag, int nthreads)
@@ -399,7 +418,8 @@ int oracle_sample(const void* logits, int dtype, int64_t n_rows, int64_t vocab, 
     oracle_in_t in = {logits, dtype, vocab, row_stride, logit_row, temperature, top_k, top_p, min_p,
                       presence, frequency, repetition, seed, has_seed, stream_id,
                       hist_offsets, hist_ids, global_seed, philox_offset, vocab_mask, mask_stride,
-                      bias_offsets, bias_ids, bias_values};
+                      bias_offsets, bias_ids, bias_values, min_tokens_left, stop_offsets, stop_ids,
+                      sanitize_nan};
     const int64_t n = rows ? n_out : n_rows;
     int failed = 0;
     (void)nthreads;
@@ -436,7 +456,8 @@ int oracle_penalized_logits(const void* logits, int dtype, int64_t vocab, int64_
                             const int32_t* hist_offsets, const int32_t* hist_ids,
                             const uint32_t* vocab_mask, int64_t mask_stride,
                             const int32_t* bias_offsets, const int32_t* bias_ids, const float* bias_values,
-                            int64_t out_row, float* out_x)
+                            const int32_t* min_tokens_left, const int32_t* stop_offsets, const int32_t* stop_ids,
+                            int sanitize_nan, int64_t out_row, float* out_x)
 {
     oracle_in_t in;
     memset(&in, 0, sizeof in);
@@ -453,6 +474,8 @@ int oracle_penalized_logits(const void* logits, int dtype, int64_t vocab, int64_
     in.hist_offsets = hist_offsets; in.hist_ids = hist_ids;
     in.vocab_mask = vocab_mask; in.mask_stride = mask_stride;
     in.bias_offsets = bias_offsets; in.bias_ids = bias_ids; in.bias_values = bias_values;
+    in.min_tokens_left = min_tokens_left; in.stop_offsets = stop_offsets; in.stop_ids = stop_ids;
+    in.sanitize_nan = sanitize_nan;
     int st = load_penalized_row(&in, out_row, out_x, count, presence, frequency, repetition);
     free(count);
     free(lr);

@@ -90,6 +90,10 @@ class SamplerBatch:
     bias_offsets: Optional[np.ndarray] = None  # [n_rows + 1] int32: logit_bias entries of row r are
     bias_ids: Optional[np.ndarray] = None      # bias_ids / bias_values[bias_offsets[r] .. [r + 1])
     bias_values: Optional[np.ndarray] = None
+    min_tokens_left: Optional[np.ndarray] = None  # [n_rows] int32: > 0 bans the row's stop tokens
+    stop_offsets: Optional[np.ndarray] = None     # [n_rows + 1] int32 CSR over stop_ids
+    stop_ids: Optional[np.ndarray] = None
+    sanitize_nan: bool = False                    # NaN logits read as -inf (else status 1)
     notes: dict = field(default_factory=dict)
 
     @property
@@ -317,6 +321,23 @@ def logit_bias(seed: int, n: int, v: int, max_per_row: int = 64, scale: float = 
     vals[rng.random(ids.size) < 0.05] = -np.inf
     vals[rng.random(ids.size) < 0.02] = np.float32(50.0)
     return offs, ids, vals
+
+
+def min_tokens(seed: int, n: int, v: int, max_stops: int = 4, owe: float = 0.5):
+    """Per-row min_tokens state (tokens still owed, stop-token lists in CSR
+    form): 1..max_stops stop tokens per row (the last ids of the vocabulary,
+    where chat models keep their end-of-turn tokens, plus a random one), and a
+    fraction ``owe`` of the rows still owing 1..16 tokens (the others 0)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = rng.integers(1, max_stops + 1, size=n)
+    offs = np.zeros(n + 1, np.int32)
+    offs[1:] = np.cumsum(lens)
+    ids = np.empty(int(offs[-1]), np.int32)
+    for r in range(n):
+        L = int(lens[r])
+        ids[offs[r]:offs[r + 1]] = np.concatenate([v - 1 - np.arange(L - 1), rng.integers(0, v, 1)])
+    left = np.where(rng.random(n) < owe, rng.integers(1, 17, size=n), 0).astype(np.int32)
+    return left, offs, ids
 
 
 ABLATION_STAGES = ("plain", "topkp", "minp", "penalties")
