@@ -15,7 +15,9 @@ point; `roofline` is for the sampling kernel; `cpu_baseline` = the CPU oracle
 on a bounded sample at one thread and at every core; `ablation` times the
 per-family workloads (plain -> +top-k/top-p -> +min-p -> +penalties);
 `logprob_outputs` times the same step with the per-row logprob outputs
-(sampled token + top 5, scaled and unscaled).
+(sampled token + top 5, scaled and unscaled); `extensions` with a
+vocabulary mask, with logit_bias lists, with a min_tokens ban and with NaN
+sanitising.
 `--impl reference` times the CPU oracle itself (the only reference this
 sampler has), one row per step. Several GPUs run independent replicas (rows
 are independent: no collective).
@@ -375,7 +377,7 @@ def host_call_us(sampler, arg_blocks, stream, n=200):
 
 
 class LogprobReplayer(Replayer):
-    """Replays of sampler_sample_ex calls (top_n logprobs per row)."""
+    """Replays of sampler_sample_ex calls (logprob outputs or another extension)."""
 
     def __init__(self, torch, sampler, arg_blocks, stream, lp_kw):
         super().__init__(torch, sampler, arg_blocks, stream)
@@ -413,6 +415,50 @@ def run_logprob_outputs(torch, sampler, rep, batch, dev, top_n, seconds):
         torch.cuda.synchronize()
         lr.run(lr.R * 2)
         out["unscaled" if unscaled else "scaled"] = stats_us(sustained(lr, seconds))
+    return out
+
+
+def run_extensions(torch, pkg, wdev, batch, dev, local, seconds):
+    """Median step time of the same batch with each sampler_sample_ex extension:
+    a grammar-style vocabulary mask (about 10 % of tokens allowed per row), 64
+    logit_bias entries per row, 16 stop tokens banned on every row (min_tokens),
+    and NaN sanitising over logits with 0.1 % NaN."""
+    out = {}
+    n, V = batch.n_rows, batch.vocab
+    words = (V + 31) // 32
+    mask = workloads.vocab_mask(7, n, V, allowed=0.1, full_rows=0)
+    offs = np.arange(0, 64 * n + 1, 64, dtype=np.int32)
+    rng = np.random.Generator(np.random.PCG64(8))
+    ids = rng.integers(0, V, size=int(offs[-1])).astype(np.int32)
+    vals = (rng.standard_normal(ids.size) * 5).astype(np.float32)
+    left = np.ones(n, np.int32)
+    soffs = np.arange(0, 16 * n + 1, 16, dtype=np.int32)
+    sids = rng.integers(0, V, size=16 * n).astype(np.int32)
+    x = batch.logits.copy()
+    at = rng.random(x.shape) < 0.001
+    x[at] = np.uint16(0x7FC0) if batch.dtype == "bf16" else np.float32(np.nan)
+    cases = (("vocab_mask_10pct", dict(vocab_mask=mask), n * words * 4),
+             ("logit_bias_64", dict(bias_offsets=offs, bias_ids=ids, bias_values=vals),
+              offs.nbytes + ids.nbytes + vals.nbytes),
+             ("min_tokens_16_stops", dict(min_tokens_left=left, stop_offsets=soffs, stop_ids=sids),
+              left.nbytes + soffs.nbytes + sids.nbytes),
+             ("sanitize_nan_0.1pct", dict(logits=x, sanitize_nan=True), 0))
+    for name, kw, extra in cases:
+        b = batch.with_(**kw)
+        s, d, rep, copies, _ = prepare(torch, pkg, wdev, b, dev, local)
+        lr = LogprobReplayer(torch, s, rep.args, rep.stream, wdev.ext_kw(d))
+        with torch.cuda.stream(rep.stream):
+            for a in rep.args:
+                s.sample_ex_args(a, stream=rep.stream.cuda_stream, **wdev.ext_kw(d))
+        torch.cuda.synchronize()
+        lr.run(lr.R * 2)
+        st = stats_us(sustained(lr, seconds))
+        st["extra_bytes_per_step"] = int(extra)
+        st["exact_path_rows"] = s.stat(0, reset=True)
+        out[name] = st
+        s.close()
+        del d, rep, lr
+        torch.cuda.empty_cache()
     return out
 
 
@@ -520,8 +566,10 @@ def run_ours(args):
                "one_thread": {"value": rps1, "unit": UNIT, "sample": f"{nrows1} rows ({el1:.1f} s)"}}
     abl = None
     lpo = None
+    ext = None
     if not args.no_ablation and args.workload == "mixed":
         lpo = run_logprob_outputs(torch, sampler, rep, batch, dev, 5, args.ablation_seconds)
+        ext = run_extensions(torch, pkg, wdev, batch, dev, local, args.ablation_seconds)
         abl = run_ablation(torch, pkg, wdev, dev, local, args.ablation_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -543,6 +591,7 @@ def run_ours(args):
         "clocks": clk,
         "ablation": abl,
         "logprob_outputs": lpo,
+        "extensions": ext,
         "kernel_hash": kernel_hash(),
         "first_tokens": tokens[:8].tolist(),
     }

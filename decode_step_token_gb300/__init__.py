@@ -12,7 +12,8 @@ from typing import Optional
 
 from . import _binding as abi
 from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHORT_WAITS, SAMPLER_DTYPE_BF16,
-                       SAMPLER_DTYPE_F32, SAMPLER_MAX_TOP_N, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
+                       SAMPLER_DTYPE_F32, SAMPLER_MAX_BIAS, SAMPLER_MAX_STOP, SAMPLER_MAX_TOP_N,
+                       SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
                        load_library, sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
                        sampler_destroy, sampler_ext_t, sampler_sample, sampler_sample_host,
                        sampler_sample_ex, sampler_sample_noalloc, sampler_status_string,
@@ -20,7 +21,8 @@ from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHO
 
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
            "sampler_sample_host", "sampler_sample_noalloc", "sampler_sample_ex", "sampler_destroy",
-           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "sampler_ext_t",
+           "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "SAMPLER_MAX_BIAS",
+           "SAMPLER_MAX_STOP", "sampler_ext_t",
            "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
 
 
@@ -126,11 +128,14 @@ class Sampler:
                        out_token_logprob=None, out_top_ids=None, out_top_logprobs=None,
                        vocab_mask=None, mask_stride: Optional[int] = None,
                        bias_offsets=None, bias_ids=None, bias_values=None,
-                       stream: Optional[int] = None) -> None:
+                       min_tokens_left=None, stop_offsets=None, stop_ids=None,
+                       sanitize_nan: bool = False, stream: Optional[int] = None) -> None:
         """sampler_sample_ex: the step plus per-row logprob outputs (device tensors:
         out_token_logprob [N] fp32, out_top_ids / out_top_logprobs [N, top_n]
-        int32 / fp32), a vocabulary bitmask (device [N, words] int32/uint32) and
-        logit_bias lists (device CSR: offsets [N + 1], ids, fp32 values)."""
+        int32 / fp32), a vocabulary bitmask (device [N, words] int32/uint32),
+        logit_bias lists (device CSR: offsets [N + 1], ids, fp32 values), the
+        min_tokens ban (device int32: tokens owed [N], stop-token CSR offsets
+        [N + 1] and ids) and NaN sanitising."""
         if stream is None:
             import torch
             stream = torch.cuda.current_stream(self.device).cuda_stream
@@ -138,7 +143,9 @@ class Sampler:
             mask_stride = int(vocab_mask.shape[-1])
         ext = sampler_ext_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob), _ptr(out_top_ids),
                             _ptr(out_top_logprobs), _ptr(vocab_mask), int(mask_stride or 0),
-                            _ptr(bias_offsets), _ptr(bias_ids), _ptr(bias_values))
+                            _ptr(bias_offsets), _ptr(bias_ids), _ptr(bias_values),
+                            _ptr(min_tokens_left), _ptr(stop_offsets), _ptr(stop_ids),
+                            1 if sanitize_nan else 0)
         rc = sampler_sample_ex(self._h, args, ext, stream)
         if rc != SAMPLER_OK:
             raise SamplerError(rc, "sampler_sample_ex")

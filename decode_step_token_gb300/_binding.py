@@ -43,6 +43,7 @@ SAMPLER_STAT_EXACT_ROWS = 0
 SAMPLER_NOALLOC_MAX_ROWS = 64
 SAMPLER_MAX_TOP_N = 16
 SAMPLER_MAX_BIAS = 64
+SAMPLER_MAX_STOP = 16
 
 
 class sampler_config_t(ctypes.Structure):
@@ -101,6 +102,10 @@ class sampler_ext_t(ctypes.Structure):
         ("bias_offsets", _P),
         ("bias_ids", _P),
         ("bias_values", _P),
+        ("min_tokens_left", _P),
+        ("stop_offsets", _P),
+        ("stop_ids", _P),
+        ("sanitize_nan", ctypes.c_int32),
     ]
 
 

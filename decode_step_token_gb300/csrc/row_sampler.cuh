@@ -100,6 +100,12 @@ struct KernelParams {
     const int32_t* bias_offsets;
     const int32_t* bias_ids;
     const float* bias_values;
+    // min_tokens of sampler_sample_ex (slice kernel only): a row that still owes
+    // tokens has its stop tokens (CSR by output row) at -inf
+    const int32_t* min_tokens_left;
+    const int32_t* stop_offsets;
+    const int32_t* stop_ids;
+    int32_t sanitize_nan;  // NaN logits read as -inf (slice kernel only)
 };
 
 // ------------------------------------------------------------------ records

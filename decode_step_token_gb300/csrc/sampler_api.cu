@@ -205,7 +205,7 @@ int noalloc_grant_smem(int dev, int dtype, size_t smem)
 
 extern "C" {
 
-uint32_t sampler_abi_version(void) { return (1u << 16) | 2u; }
+uint32_t sampler_abi_version(void) { return (1u << 16) | 3u; }
 
 int sampler_get_stat(sampler_t h, int which, uint64_t* value, int reset)
 {
@@ -326,7 +326,9 @@ int sampler_sample_ex(sampler_t h, const sampler_args_t* a, const sampler_ext_t*
         if (ext->top_n > 0 && (!ext->out_top_ids || !ext->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
         if (ext->vocab_mask && ext->mask_stride < (a->vocab + 31) / 32) return SAMPLER_ERR_UNSUPPORTED;
         if (ext->bias_offsets && (!ext->bias_ids || !ext->bias_values)) return SAMPLER_ERR_NULL_ARG;
-        if (!ext->out_token_logprob && ext->top_n == 0 && !ext->vocab_mask && !ext->bias_offsets)
+        if (ext->stop_offsets && !ext->stop_ids) return SAMPLER_ERR_NULL_ARG;
+        if (!ext->out_token_logprob && ext->top_n == 0 && !ext->vocab_mask && !ext->bias_offsets &&
+            !ext->stop_offsets && !ext->sanitize_nan)
             ext = nullptr;  // nothing asked
     }
     if (a->n_rows == 0) return SAMPLER_OK;

@@ -14,7 +14,8 @@ static_assert(slc::kMaxRows <= slc::kT, "one thread per row classifies the batch
 static_assert(slc::kHead < slc::kMaxSmem, "shared-memory head");
 
 static_assert(kSliceMaxRows == slc::kMaxRows && kSliceMaxSlices == slc::kMaxSlices, "slice limits");
-static_assert(slc::kMaxTopN == SAMPLER_MAX_TOP_N && slc::kMaxBias == SAMPLER_MAX_BIAS, "extension limits");
+static_assert(slc::kMaxTopN == SAMPLER_MAX_TOP_N && slc::kMaxBias == SAMPLER_MAX_BIAS &&
+                  slc::kMaxStop == SAMPLER_MAX_STOP, "extension limits");
 static_assert(kSliceHdrBytes == sizeof(slc::SliceHdr) && kSliceBodyBytes == sizeof(slc::SliceBody),
               "slice record sizes");
 static_assert(kSliceCntStride == slc::kCntStride, "counter stride");
@@ -107,6 +108,10 @@ int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGe
         k.bias_offsets = lp->bias_offsets;
         k.bias_ids = lp->bias_ids;
         k.bias_values = lp->bias_values;
+        k.min_tokens_left = lp->min_tokens_left;
+        k.stop_offsets = lp->stop_offsets;
+        k.stop_ids = lp->stop_ids;
+        k.sanitize_nan = lp->sanitize_nan ? 1 : 0;
     }
     p.n_rows = int(a->n_rows);
     p.G = g.G;

@@ -59,6 +59,19 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
             }
         }
     }
+    ri.ban = 0;
+    if (kp.stop_offsets) {  // min_tokens: at most kMaxStop stop tokens, every id in the vocabulary
+        const int s0 = kp.stop_offsets[r], s1 = kp.stop_offsets[r + 1];
+        if (s1 - s0 > kMaxStop || s1 < s0) {
+            bad = true;
+        } else {
+            for (int j = s0; j < s1; ++j) {
+                const int id = kp.stop_ids[j];
+                if (id < 0 || int64_t(id) >= V) bad = true;
+            }
+            if (s1 > s0 && kp.min_tokens_left && kp.min_tokens_left[r] > 0) ri.ban = 1;
+        }
+    }
     const bool greedy = T < 1e-5f;
     ri.T = greedy ? 1.0f : T;
     ri.invT = 1.0f / ri.T;
@@ -84,7 +97,7 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     ri.s2o = kp.lp_unscaled ? 1.4426950408889634f : ri.s2;
     ri.need_zo = (ri.lp && (kp.lp_unscaled || ri.cls != kClsTrunc)) ? 1 : 0;
     if (ri.lp && kp.top_n > 0) ri.mt = uint8_t(max(int(ri.mt), kp.top_n));
-    ri.pad2 = ri.pad3 = 0;
+    ri.pad3 = 0;
     ri.r = r;
     return ri;
 }
@@ -198,16 +211,29 @@ __device__ __forceinline__ void unit_max(const SliceView<InT>& sv, float& mx, in
     amax = __reduce_min_sync(0xffffffffu, li);
 }
 
-// ---------------------------------------------------------------- logit_bias
-// Row r's logit of token v after its bias entries (one fp32 addition each, in
-// list order) and its vocabulary mask: one thread's view, for the few tokens
-// read again one by one.
+// ---------------------------------------------------------------- logit_bias, min_tokens
+// Whether the row takes tokens apart from its staged logits: biased tokens, and
+// stop tokens banned while the row owes tokens.
+__device__ __forceinline__ bool has_extras(const KernelParams& kp, const RowInfo& ri)
+{
+    return kp.bias_offsets != nullptr || ri.ban;
+}
+
+// Row r's logit of token v after NaN sanitising, its bias entries (one fp32
+// addition each, in list order), its min_tokens ban and its vocabulary mask:
+// one thread's view, for the few tokens read again one by one.
 template <typename InT>
 __device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowInfo& ri, int v)
 {
     float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    if (kp.sanitize_nan && x != x) x = -INFINITY;
     if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
         return -INFINITY;
+    if (ri.ban) {
+        const int s1 = kp.stop_offsets[ri.r + 1];
+        for (int j = kp.stop_offsets[ri.r]; j < s1; ++j)
+            if (kp.stop_ids[j] == v) return -INFINITY;
+    }
     if (kp.bias_offsets) {
         const int b1 = kp.bias_offsets[ri.r + 1];
         for (int j = kp.bias_offsets[ri.r]; j < b1; ++j)
@@ -216,22 +242,27 @@ __device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowI
     return x;
 }
 
-// The row's biased tokens in [lo, hi) with their biased, masked logits (each
-// token once), written to xi / xv; returns how many (at most kMaxBias). Warp-wide.
+// The row's biased and banned tokens in [lo, hi) with their final logits (each
+// token once), written to xi / xv; returns how many (at most kMaxExtras).
+// Warp-wide.
 template <typename InT>
 __device__ __noinline__ int row_extras(const KernelParams& kp, const RowInfo& ri, int lo, int hi, int32_t* xi,
                                        float* xv)
 {
     const int lane = threadIdx.x & 31;
-    const int b0 = kp.bias_offsets[ri.r];
-    const int L = kp.bias_offsets[ri.r + 1] - b0;
+    const int b0 = kp.bias_offsets ? kp.bias_offsets[ri.r] : 0;
+    const int Lb = kp.bias_offsets ? kp.bias_offsets[ri.r + 1] - b0 : 0;
+    const int s0 = ri.ban ? kp.stop_offsets[ri.r] : 0;
+    const int L = Lb + (ri.ban ? kp.stop_offsets[ri.r + 1] - s0 : 0);
+    // entry e of the bias list followed by the banned stop tokens
+    auto id_at = [&](int e) { return e < Lb ? kp.bias_ids[b0 + e] : kp.stop_ids[s0 + (e - Lb)]; };
     int cnt = 0;
 #pragma unroll 1
     for (int e0 = 0; e0 < L; e0 += 32) {
         const int e = e0 + lane;
-        const int id = e < L ? kp.bias_ids[b0 + e] : -1;
+        const int id = e < L ? id_at(e) : -1;
         bool first = e < L && id >= lo && id < hi;
-        for (int j = 0; first && j < e; ++j) first = kp.bias_ids[b0 + j] != id;  // its first entry
+        for (int j = 0; first && j < e; ++j) first = id_at(j) != id;  // its first entry
         float x = 0.0f;
         if (first) x = biased_logit<InT>(kp, ri, id);
         const uint32_t bal = __ballot_sync(0xffffffffu, first);
@@ -1061,9 +1092,9 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
     // x >= tB exactly when x is not -inf and its key reaches B
     const float tB = B < 0x00800000u ? -FLT_MAX : key2f(B);
     const typename Vec<InT>::Thr t2 = Vec<InT>::thr(tB);
-    // logit_bias: the row's biased tokens are taken apart (their raw logits
-    // skipped below, their biased values appended at the end)
-    const int nx = P.k.bias_offsets ? row_extras<InT>(P.k, ri, 0, V, xi, xv) : 0;
+    // logit_bias / min_tokens: the row's biased and banned tokens are taken
+    // apart (their raw logits skipped below, their values appended at the end)
+    const int nx = has_extras(P.k, ri) ? row_extras<InT>(P.k, ri, 0, V, xi, xv) : 0;
     int C = C0;
 #pragma unroll 1
     for (int base = 0; base < total; base += 32 * U) {
@@ -1085,6 +1116,7 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
                     v[u] = __ldg(reinterpret_cast<const uint4*>(g) + j);
                 else
                     v[u] = load_vec_slow<InT>(g, j, n);
+                if (P.k.sanitize_nan) v[u] = Vec<InT>::sanitized(v[u]);
                 if (P.k.vocab_mask) {
                     const int tk = c0 + j * E;
                     const uint32_t w = __ldg(P.k.vocab_mask + size_t(ri.r) * size_t(P.k.mask_stride) + (tk >> 5));
@@ -1426,12 +1458,13 @@ __device__ __forceinline__ int cta_excl_scan(int v, int& total, SliceShared& sh)
     return before + s - v;
 }
 
-// Token v of the row: masked, and biased from the CTA's table (set up by
-// cta_bias_setup) when the row carries logit_bias.
+// Token v of the row: sanitised, masked, and taken from the CTA's table (set
+// up by cta_bias_setup) when the row carries logit_bias or a min_tokens ban.
 template <typename InT>
 __device__ __forceinline__ float row_x(const KernelParams& kp, const RowInfo& ri, int v, const SliceShared& sh)
 {
-    const float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
+    if (kp.sanitize_nan && x != x) x = -INFINITY;
     if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
         return -INFINITY;
     if (sh.bx_n && ((sh.bx_bits[v >> 5] >> (v & 31)) & 1u))
@@ -1440,14 +1473,14 @@ __device__ __forceinline__ float row_x(const KernelParams& kp, const RowInfo& ri
     return x;
 }
 
-// The row's logit_bias for the CTA's exact path: its biased tokens (warp 0)
-// and their bitmap in the idle staging slots.
+// The row's logit_bias and min_tokens ban for the CTA's exact path: its biased
+// and banned tokens (warp 0) and their bitmap in the idle staging slots.
 template <typename InT>
 __device__ __forceinline__ void cta_bias_setup(SliceShared& sh, unsigned char* slots, const KernelParams& kp,
                                                const RowInfo& ri)
 {
     const int tid = threadIdx.x, V = int(kp.vocab);
-    if (!kp.bias_offsets) {
+    if (!has_extras(kp, ri)) {
         if (tid == 0) sh.bx_n = 0;
         __syncthreads();
         return;
@@ -1696,40 +1729,51 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
     sv.nvec = (n_el + E - 1) / E;
     sv.n = n_el;
     sv.c0 = c0;
-    if (kp.vocab_mask && !extra) {
-        // the row's vocabulary mask: staged vectors are masked in place once,
-        // the others (a ragged tail, an unaligned slice) as they are read
-        sv.mw = kp.vocab_mask + size_t(r) * size_t(kp.mask_stride);
-        uint4* smv = reinterpret_cast<uint4*>(const_cast<unsigned char*>(slot));
+    // The extensions rewrite the unit in place, so a unit that has one is staged
+    // whole: the vectors the bulk copy left out (a ragged tail, an unaligned
+    // slice) are loaded into the slot too (it holds the whole unit).
+    const bool has_x = !extra && (kp.sanitize_nan || kp.vocab_mask || has_extras(kp, ri));
+    uint4* smv = reinterpret_cast<uint4*>(const_cast<unsigned char*>(slot));
+    if (has_x && sv.nb < sv.nvec) {
+        for (int j = sv.nb + lane; j < sv.nvec; j += 32) smv[j] = sv.vec(j);
+        __syncwarp();
+        sv.nb = sv.nvec;
+    }
+    if (has_x && kp.sanitize_nan) {  // NaN sanitising: NaN becomes -inf
+#pragma unroll 4
+        for (int j = lane; j < sv.nb; j += 32) {
+            const uint4 v = smv[j], c = Vec<InT>::sanitized(v);
+            if ((v.x ^ c.x) | (v.y ^ c.y) | (v.z ^ c.z) | (v.w ^ c.w)) smv[j] = c;
+        }
+        __syncwarp();
+    }
+    if (has_x && kp.vocab_mask) {  // the row's vocabulary mask
+        const uint32_t* mw = kp.vocab_mask + size_t(r) * size_t(kp.mask_stride);
 #pragma unroll 4
         for (int j = lane; j < sv.nb; j += 32) {
             const int t0 = c0 + j * E;
-            const uint32_t bits = (__ldg(sv.mw + (t0 >> 5)) >> (t0 & 31)) & ((1u << E) - 1u);
+            const uint32_t bits = (__ldg(mw + (t0 >> 5)) >> (t0 & 31)) & ((1u << E) - 1u);
             if (bits != (1u << E) - 1u) smv[j] = Vec<InT>::masked(smv[j], bits);
         }
         __syncwarp();
     }
     int nx = 0;
-    if (kp.bias_offsets && !extra) {
-        // logit_bias: the unit's biased tokens are taken apart with their biased
-        // values; the view reads them as -inf (patched in the staged vectors)
+    if (has_x && has_extras(kp, ri)) {
+        // logit_bias / min_tokens: the unit's biased and banned tokens are taken
+        // apart with their final values and read as -inf in the slot
         nx = row_extras<InT>(kp, ri, c0, c0 + n_el, xi, xv);
-        uint32_t* smw = reinterpret_cast<uint32_t*>(const_cast<unsigned char*>(slot));
+        uint32_t* smw = reinterpret_cast<uint32_t*>(smv);
         for (int i = lane; i < nx; i += 32) {
             const int o = xi[i] - c0;
-            if (o / E < sv.nb) {
-                if (sizeof(InT) == 2) {
-                    const int sh = 16 * (o & 1);
-                    atomicOr(&smw[o >> 1], 0xFF80u << sh);
-                    atomicAnd(&smw[o >> 1], ~(0x007Fu << sh));
-                } else {
-                    smw[o] = 0xFF800000u;
-                }
+            if (sizeof(InT) == 2) {
+                const int sh = 16 * (o & 1);
+                atomicOr(&smw[o >> 1], 0xFF80u << sh);
+                atomicAnd(&smw[o >> 1], ~(0x007Fu << sh));
+            } else {
+                smw[o] = 0xFF800000u;
             }
         }
         __syncwarp();
-        sv.xi = xi;
-        sv.nx = nx;
     }
     SliceHdr hdr;
     hdr.mx = -INFINITY;

@@ -68,6 +68,8 @@ constexpr int kLCap = 48;               // list entries one record holds
 constexpr int kKComplete = 32;          // top-k rows up to this k list each unit's top k
 constexpr int kMaxTopN = 16;            // largest top_n of the logprob outputs
 constexpr int kMaxBias = 64;            // logit_bias entries a row may carry
+constexpr int kMaxStop = 16;            // stop tokens a row may carry (min_tokens)
+constexpr int kMaxExtras = kMaxBias + kMaxStop;  // tokens taken apart from the staged logits
 constexpr int kTQCap = 320;             // vectors a truncated unit queues (more: the list overflows)
 constexpr int kKCap = 128;              // largest top-k the lists settle
 constexpr int kReCap = 16;              // slices a finishing warp may read again
@@ -133,7 +135,8 @@ struct alignas(16) RowInfo {
     uint8_t need_z, m, mt, greedy;
     uint8_t lp;    // logprob outputs requested
     uint8_t need_zo;  // the units keep the row's softmax mass at the outputs' temperature
-    uint8_t pad2, pad3;
+    uint8_t ban;   // min_tokens: the row's stop tokens are -inf
+    uint8_t pad3;
     int32_t r;     // the output row
 };
 
@@ -141,8 +144,8 @@ struct alignas(16) WarpScratch {
     uint16_t q[kSlotBytes / 16];        // plain units: vectors the cheap bound let through;
                                         // truncated units: (vector << 8 | mask) words
     uint4 qw[2 * 32];                   // Philox words of the first 32 queued vectors
-    int32_t xi[kMaxBias];               // logit_bias: the unit's biased tokens ...
-    float xv[kMaxBias];                 // ... and their biased (masked) logits
+    int32_t xi[kMaxExtras];             // logit_bias / min_tokens: the unit's biased and
+    float xv[kMaxExtras];               // banned tokens, and their final logits
     uint32_t n;                         // candidates listed
     uint32_t nre;                       // slices to read again
     uint16_t re[kReCap];
@@ -162,10 +165,10 @@ struct alignas(16) SliceShared {
     unsigned long long red_k[2 * kW];
     unsigned long long sel_prefix, sel_wabove, sel_target;
     double red_d[kW];
-    // logit_bias on the exact path: the row's biased tokens, their values, and
-    // a bitmap of them (in the idle staging slots)
-    int32_t bx_i[kMaxBias];
-    float bx_v[kMaxBias];
+    // logit_bias / min_tokens on the exact path: the row's biased and banned
+    // tokens, their values, and a bitmap of them (in the idle staging slots)
+    int32_t bx_i[kMaxExtras];
+    float bx_v[kMaxExtras];
     int32_t bx_n;
     uint32_t* bx_bits;
     unsigned long long lp_list[kMaxTopN];
@@ -215,6 +218,17 @@ struct Vec<uint16_t> {
     {
         return make_uint4(mask_word(v.x, bits), mask_word(v.y, bits >> 2), mask_word(v.z, bits >> 4),
                           mask_word(v.w, bits >> 6));
+    }
+    // NaN elements become -inf
+    __device__ static __forceinline__ uint32_t sanitize_word(uint32_t w)
+    {
+        const uint32_t nan = (((w & 0x7FFFu) > 0x7F80u) ? 0x0000FFFFu : 0u) |
+                             (((w & 0x7FFF0000u) > 0x7F800000u) ? 0xFFFF0000u : 0u);
+        return (w & ~nan) | (0xFF80FF80u & nan);
+    }
+    __device__ static __forceinline__ uint4 sanitized(const uint4& v)
+    {
+        return make_uint4(sanitize_word(v.x), sanitize_word(v.y), sanitize_word(v.z), sanitize_word(v.w));
     }
     using Acc = uint4;
     __device__ static __forceinline__ Acc acc_init() { return neg_inf(); }
@@ -281,6 +295,14 @@ struct Vec<float> {
         return make_uint4((bits & 1u) ? v.x : 0xFF800000u, (bits & 2u) ? v.y : 0xFF800000u,
                           (bits & 4u) ? v.z : 0xFF800000u, (bits & 8u) ? v.w : 0xFF800000u);
     }
+    __device__ static __forceinline__ uint32_t sanitize_word(uint32_t w)
+    {
+        return (w & 0x7FFFFFFFu) > 0x7F800000u ? 0xFF800000u : w;
+    }
+    __device__ static __forceinline__ uint4 sanitized(const uint4& v)
+    {
+        return make_uint4(sanitize_word(v.x), sanitize_word(v.y), sanitize_word(v.z), sanitize_word(v.w));
+    }
     using Acc = float4;
     __device__ static __forceinline__ Acc acc_init() { return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY); }
     __device__ static __forceinline__ float fmax_nan(float a, float b)
@@ -327,14 +349,10 @@ template <typename InT>
 struct SliceView {
     const uint4* sm;
     const InT* g;    // first element of the slice in global memory
-    int nb;          // staged vectors (already masked)
+    int nb;          // staged vectors (with the row's extensions applied)
     int nvec;        // vectors covering the slice
     int n;           // elements in the slice
     int c0;          // first token of the slice
-    const uint32_t* mw = nullptr;  // vocabulary mask words (NULL: none) ...
-    int mbase = 0;                 // ... mw[0] being word mbase of the row's mask
-    const int32_t* xi = nullptr;   // biased tokens, read as -inf here (their biased
-    int nx = 0;                    // values are taken apart)
 
     __device__ __forceinline__ uint4 vec(int j) const
     {
@@ -352,24 +370,7 @@ struct SliceView {
                 w[q] = i < n ? reinterpret_cast<const uint32_t*>(g)[i] : 0xFF800000u;
             }
         }
-        uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
-        if (mw) v = Vec<InT>::masked(v, mask_bits(j));
-        if (nx) {
-            uint32_t keep = (1u << E) - 1u;
-            for (int q = 0; q < nx; ++q) {
-                const int e = xi[q] - (c0 + j * E);
-                if (e >= 0 && e < E) keep &= ~(1u << e);
-            }
-            v = Vec<InT>::masked(v, keep);
-        }
-        return v;
-    }
-    // the allowed-token bits of vector j (bit e: element e)
-    __device__ __forceinline__ uint32_t mask_bits(int j) const
-    {
-        constexpr int E = Vec<InT>::E;
-        const int t0 = c0 + j * E;
-        return (mw[(t0 >> 5) - mbase] >> (t0 & 31)) & ((1u << E) - 1u);
+        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
 

@@ -259,10 +259,27 @@ int sampler_sample_noalloc(const sampler_args_t* args, sampler_stream_t stream);
  * manual lists logit_bias among the sampler's inputs without defining it; this
  * is the reading taken.
  *
+ * min_tokens: while output row r still owes tokens (min_tokens_left[r] > 0),
+ * its stop tokens stop_ids[j], j in [stop_offsets[r], stop_offsets[r + 1]),
+ * are -inf (after logit_bias, before the penalties and the mask), so the row
+ * cannot end yet. This is the first stage of the sampler's fixed order in the
+ * xbrilliance.ai note on sampling cost ("what sampling does in one decode
+ * step"); the note names the stage without defining it, and this is the usual
+ * reading. At most SAMPLER_MAX_STOP stop tokens per row; more, or an id outside
+ * [0, vocab), is SAMPLER_ROW_BAD_PARAM whether or not the row owes tokens.
+ * NULL min_tokens_left: no row owes tokens.
+ *
+ * NaN sanitising (sanitize_nan != 0): a NaN logit reads as -inf, so it is
+ * never picked and weighs nothing, instead of failing its row with
+ * SAMPLER_ROW_NONFINITE (the manual's SGLANG_SANITIZE_NAN_LOGITS switch, in
+ * its MLX help text). +inf stays an error; a row with nothing but NaN and -inf
+ * reports SAMPLER_ROW_ALL_NEG_INF.
+ *
  * Every pointer is a device pointer on the handle's device.
  */
 #define SAMPLER_MAX_TOP_N 16
 #define SAMPLER_MAX_BIAS 64
+#define SAMPLER_MAX_STOP 16
 typedef struct {
     int32_t top_n;                /* 0 .. SAMPLER_MAX_TOP_N */
     int32_t unscaled;             /* 0: log_softmax(x / T) over the kept set; 1: log_softmax(x) */
@@ -274,6 +291,10 @@ typedef struct {
     const int32_t* bias_offsets;  /* [N + 1] CSR offsets of the logit_bias entries; NULL = none */
     const int32_t* bias_ids;      /* [bias_offsets[N]] tokens */
     const float* bias_values;     /* [bias_offsets[N]] values */
+    const int32_t* min_tokens_left;  /* [N] tokens each row still owes; NULL = none */
+    const int32_t* stop_offsets;  /* [N + 1] CSR offsets of the stop tokens; NULL = none */
+    const int32_t* stop_ids;      /* [stop_offsets[N]] tokens */
+    int32_t sanitize_nan;         /* 1: NaN logits read as -inf */
 } sampler_ext_t;
 
 /* sampler_sample plus the extensions of `ext` (NULL: none). Offered on the

@@ -45,28 +45,24 @@ def test_python_binding_uses_the_abi_names(lib):
 
 def test_struct_layouts_match_the_header(tmp_path):
     import decode_step_token_gb300 as d
+    structs = [("sampler_args_t", d.sampler_args_t), ("sampler_config_t", d.sampler_config_t),
+               ("sampler_ext_t", d.sampler_ext_t)]
     src = tmp_path / "layout.c"
-    fields_a = [f[0] for f in d.sampler_args_t._fields_]
-    fields_c = [f[0] for f in d.sampler_config_t._fields_]
     body = ['#include <stdio.h>', '#include <stddef.h>', '#include "sampler.h"', "int main(void){"]
-    body.append('printf("%zu %zu\\n", sizeof(sampler_args_t), sizeof(sampler_config_t));')
-    for f in fields_a:
-        body.append(f'printf("%zu\\n", offsetof(sampler_args_t, {f}));')
-    for f in fields_c:
-        body.append(f'printf("%zu\\n", offsetof(sampler_config_t, {f}));')
+    for name, st in structs:
+        body.append(f'printf("%zu\\n", sizeof({name}));')
+        for f in st._fields_:
+            body.append(f'printf("%zu\\n", offsetof({name}, {f[0]}));')
     body.append("return 0;}")
     src.write_text("\n".join(body))
     exe = tmp_path / "layout"
     subprocess.run(["gcc", f"-I{os.path.dirname(HEADER)}", str(src), "-o", str(exe)], check=True)
-    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
-                                           check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(d.sampler_args_t)
-    assert vals[1] == ctypes.sizeof(d.sampler_config_t)
-    offs = vals[2:]
-    for f, o in zip(fields_a, offs[:len(fields_a)]):
-        assert getattr(d.sampler_args_t, f).offset == o, f
-    for f, o in zip(fields_c, offs[len(fields_a):]):
-        assert getattr(d.sampler_config_t, f).offset == o, f
+    vals = iter(int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                               check=True).stdout.split())
+    for name, st in structs:
+        assert next(vals) == ctypes.sizeof(st), name
+        for f in st._fields_:
+            assert getattr(st, f[0]).offset == next(vals), (name, f[0])
 
 
 def test_host_checks_without_a_gpu(lib):

@@ -65,6 +65,10 @@ def to_device(batch, device="cuda:0", want_probs: Optional[bool] = None, copies:
         "bias_offsets": t(batch.bias_offsets),
         "bias_ids": t(batch.bias_ids),
         "bias_values": t(batch.bias_values),
+        "min_tokens_left": t(batch.min_tokens_left),
+        "stop_offsets": t(batch.stop_offsets),
+        "stop_ids": t(batch.stop_ids),
+        "sanitize_nan": bool(batch.sanitize_nan),
     }
     return d
 
@@ -87,9 +91,17 @@ def sample_args(sampler, batch, d, copy_index: int = 0, philox_offset: Optional[
 
 
 def ext_kw(d):
-    """The mask and logit_bias arguments of sample_ex_args for device buffers `d`."""
+    """The mask, logit_bias, min_tokens and NaN-sanitising arguments of
+    sample_ex_args for device buffers `d`."""
     return dict(vocab_mask=d["vocab_mask"], bias_offsets=d["bias_offsets"], bias_ids=d["bias_ids"],
-                bias_values=d["bias_values"])
+                bias_values=d["bias_values"], min_tokens_left=d["min_tokens_left"],
+                stop_offsets=d["stop_offsets"], stop_ids=d["stop_ids"], sanitize_nan=d["sanitize_nan"])
+
+
+def wants_ext(d) -> bool:
+    """Whether the batch carries an extension only sampler_sample_ex takes."""
+    return (d["vocab_mask"] is not None or d["bias_offsets"] is not None or d["stop_offsets"] is not None
+            or d["sanitize_nan"])
 
 
 class GpuResult:
@@ -103,7 +115,7 @@ def run(sampler, batch, want_probs: Optional[bool] = None, device="cuda:0",
     import torch
 
     d = to_device(batch, device, want_probs, logits_offset_elems=logits_offset_elems)
-    if d["vocab_mask"] is not None or d["bias_offsets"] is not None:
+    if wants_ext(d):
         sampler.sample_ex_args(sample_args(sampler, batch, d), **ext_kw(d))
     else:
         sampler.sample_args(sample_args(sampler, batch, d))
