@@ -422,7 +422,7 @@ def run_extensions(torch, pkg, wdev, batch, dev, local, seconds):
     """Median step time of the same batch with each sampler_sample_ex extension:
     a grammar-style vocabulary mask (about 10 % of tokens allowed per row), 64
     logit_bias entries per row, 16 stop tokens banned on every row (min_tokens),
-    and NaN sanitising over logits with 0.1 % NaN."""
+    and NaN sanitising over the same logits and over logits with 0.1 % NaN."""
     out = {}
     n, V = batch.n_rows, batch.vocab
     words = (V + 31) // 32
@@ -442,6 +442,7 @@ def run_extensions(torch, pkg, wdev, batch, dev, local, seconds):
               offs.nbytes + ids.nbytes + vals.nbytes),
              ("min_tokens_16_stops", dict(min_tokens_left=left, stop_offsets=soffs, stop_ids=sids),
               left.nbytes + soffs.nbytes + sids.nbytes),
+             ("sanitize_nan_no_nan", dict(sanitize_nan=True), 0),
              ("sanitize_nan_0.1pct", dict(logits=x, sanitize_nan=True), 0))
     for name, kw, extra in cases:
         b = batch.with_(**kw)

@@ -48,30 +48,12 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     if (!(ri.minp >= 0.0f && ri.minp <= 1.0f)) bad = true;
     if (!isfinite(pres) || !isfinite(freq)) bad = true;
     if (!(rep > 0.0f) || isinf(rep)) bad = true;
-    if (kp.bias_offsets) {  // logit_bias: at most kMaxBias entries, every id in the vocabulary
-        const int b0 = kp.bias_offsets[r], b1 = kp.bias_offsets[r + 1];
-        if (b1 - b0 > kMaxBias || b1 < b0) {
-            bad = true;
-        } else {
-            for (int j = b0; j < b1; ++j) {
-                const int id = kp.bias_ids[j];
-                if (id < 0 || int64_t(id) >= V) bad = true;
-            }
-        }
-    }
+    // min_tokens: the row's stop tokens are banned while it owes tokens (the
+    // lists' limits are checked warp-wide by ext_lists_ok)
     ri.ban = 0;
-    if (kp.stop_offsets) {  // min_tokens: at most kMaxStop stop tokens, every id in the vocabulary
-        const int s0 = kp.stop_offsets[r], s1 = kp.stop_offsets[r + 1];
-        if (s1 - s0 > kMaxStop || s1 < s0) {
-            bad = true;
-        } else {
-            for (int j = s0; j < s1; ++j) {
-                const int id = kp.stop_ids[j];
-                if (id < 0 || int64_t(id) >= V) bad = true;
-            }
-            if (s1 > s0 && kp.min_tokens_left && kp.min_tokens_left[r] > 0) ri.ban = 1;
-        }
-    }
+    if (kp.stop_offsets && kp.min_tokens_left && kp.min_tokens_left[r] > 0 &&
+        kp.stop_offsets[r + 1] > kp.stop_offsets[r])
+        ri.ban = 1;
     const bool greedy = T < 1e-5f;
     ri.T = greedy ? 1.0f : T;
     ri.invT = 1.0f / ri.T;
@@ -169,7 +151,23 @@ __device__ __forceinline__ float lane_max_val(const SliceView<InT>& sv, uint32_t
     typename Vec<InT>::Acc a = Vec<InT>::acc_init();
 #pragma unroll 2
     for (int j = lane; j < sv.nvec; j += 32) Vec<InT>::acc_add(a, sv.vec(j));
-    const float m = Vec<InT>::acc_max(a);
+    float m = Vec<InT>::acc_max(a);
+    if (sv.san) {
+        // NaN sanitising (the unit is staged whole): a lane that met a NaN makes
+        // its NaNs -inf in the slot and takes its maximum again
+        if (m != m) {
+            uint4* smv = const_cast<uint4*>(sv.sm);
+            a = Vec<InT>::acc_init();
+#pragma unroll 1
+            for (int j = lane; j < sv.nvec; j += 32) {
+                const uint4 c = Vec<InT>::sanitized(smv[j]);
+                smv[j] = c;
+                Vec<InT>::acc_add(a, c);
+            }
+            m = Vec<InT>::acc_max(a);
+        }
+        __syncwarp();
+    }
     const bool nan = m != m;
     f = flags_of(nan, m);
     return nan ? -INFINITY : m;
@@ -212,11 +210,11 @@ __device__ __forceinline__ void unit_max(const SliceView<InT>& sv, float& mx, in
 }
 
 // ---------------------------------------------------------------- logit_bias, min_tokens
-// Whether the row takes tokens apart from its staged logits: biased tokens, and
-// stop tokens banned while the row owes tokens.
-__device__ __forceinline__ bool has_extras(const KernelParams& kp, const RowInfo& ri)
+// Whether the row carries logit_bias or stop-token lists (row_extras checks
+// them and takes the biased and banned tokens apart from the staged logits).
+__device__ __forceinline__ bool has_extras(const KernelParams& kp)
 {
-    return kp.bias_offsets != nullptr || ri.ban;
+    return kp.bias_offsets != nullptr || kp.stop_offsets != nullptr;
 }
 
 // Row r's logit of token v after NaN sanitising, its bias entries (one fp32
@@ -243,35 +241,89 @@ __device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowI
 }
 
 // The row's biased and banned tokens in [lo, hi) with their final logits (each
-// token once), written to xi / xv; returns how many (at most kMaxExtras).
-// Warp-wide.
+// token once), written to xi / xv; returns how many (at most kMaxExtras), or
+// -1 when the row's lists break the limits (more than kMaxBias / kMaxStop
+// entries, an id outside the vocabulary). Warp-wide.
 template <typename InT>
 __device__ __noinline__ int row_extras(const KernelParams& kp, const RowInfo& ri, int lo, int hi, int32_t* xi,
                                        float* xv)
 {
+    constexpr int K = (kMaxExtras + 31) / 32;  // entries per lane
     const int lane = threadIdx.x & 31;
+    const int64_t V = kp.vocab;
     const int b0 = kp.bias_offsets ? kp.bias_offsets[ri.r] : 0;
     const int Lb = kp.bias_offsets ? kp.bias_offsets[ri.r + 1] - b0 : 0;
-    const int s0 = ri.ban ? kp.stop_offsets[ri.r] : 0;
-    const int L = Lb + (ri.ban ? kp.stop_offsets[ri.r + 1] - s0 : 0);
-    // entry e of the bias list followed by the banned stop tokens
-    auto id_at = [&](int e) { return e < Lb ? kp.bias_ids[b0 + e] : kp.stop_ids[s0 + (e - Lb)]; };
+    const int s0 = kp.stop_offsets ? kp.stop_offsets[ri.r] : 0;
+    const int Ls = kp.stop_offsets ? kp.stop_offsets[ri.r + 1] - s0 : 0;
+    if (Lb < 0 || Lb > kMaxBias || Ls < 0 || Ls > kMaxStop) return -1;
+    const int L = Lb + Ls;
+    // Lane l holds entries l, l + 32, ... of the bias list followed by the stop
+    // tokens, and for those in [lo, hi) the token's logit and mask bit: every
+    // load is issued before any is used.
+    int id[K];
+    float bv[K], x[K];
+    bool ok[K];
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int e = lane + 32 * k;
+        id[k] = e < Lb ? kp.bias_ids[b0 + e] : e < L ? kp.stop_ids[s0 + (e - Lb)] : -1;
+        bv[k] = e < Lb ? kp.bias_values[b0 + e] : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int e = lane + 32 * k;
+        bad |= e < L && (id[k] < 0 || int64_t(id[k]) >= V);
+        if (e >= Lb && !ri.ban) id[k] = -1;  // stop tokens ban nothing once the row owes none
+    }
+    if (__any_sync(0xffffffffu, bad)) return -1;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const bool in = id[k] >= lo && id[k] < hi;
+        x[k] = in ? ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + id[k]) : 0.0f;
+        ok[k] = !in || !kp.vocab_mask ||
+                ((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (id[k] >> 5)) >> (id[k] & 31)) & 1u);
+    }
+    // the tokens in range, each at its first entry, in list order
     int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        uint32_t todo = __ballot_sync(0xffffffffu, id[k] >= lo && id[k] < hi);
 #pragma unroll 1
-    for (int e0 = 0; e0 < L; e0 += 32) {
-        const int e = e0 + lane;
-        const int id = e < L ? id_at(e) : -1;
-        bool first = e < L && id >= lo && id < hi;
-        for (int j = 0; first && j < e; ++j) first = id_at(j) != id;  // its first entry
-        float x = 0.0f;
-        if (first) x = biased_logit<InT>(kp, ri, id);
-        const uint32_t bal = __ballot_sync(0xffffffffu, first);
-        if (first) {
-            const int at = cnt + __popc(bal & ((1u << lane) - 1u));
-            xi[at] = id;
-            xv[at] = x;
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1u;
+            const int v = __shfl_sync(0xffffffffu, id[k], src);
+            uint32_t mt[K];
+            bool first = true;
+#pragma unroll
+            for (int kk = 0; kk < K; ++kk) {
+                mt[kk] = __ballot_sync(0xffffffffu, id[kk] == v);
+                if (kk < k && mt[kk]) first = false;
+            }
+            if (mt[k] & ((1u << src) - 1u)) first = false;
+            if (!first) continue;
+            // the token's value: its logit plus its bias entries in list order;
+            // -inf when a stop-token entry bans it or its mask bit is clear
+            float acc = __shfl_sync(0xffffffffu, x[k], src);
+            if (kp.sanitize_nan && acc != acc) acc = -INFINITY;
+            bool banned = !__shfl_sync(0xffffffffu, ok[k], src);
+#pragma unroll
+            for (int kk = 0; kk < K; ++kk) {
+#pragma unroll 1
+                for (uint32_t m = mt[kk]; m; m &= m - 1u) {
+                    const int j = __ffs(m) - 1;
+                    const float b = __shfl_sync(0xffffffffu, bv[kk], j);
+                    if (j + 32 * kk < Lb) acc = acc + b;
+                    else banned = true;
+                }
+            }
+            if (lane == 0) {
+                xi[cnt] = v;
+                xv[cnt] = banned ? -INFINITY : acc;
+            }
+            ++cnt;
         }
-        cnt += __popc(bal);
     }
     __syncwarp();
     return cnt;
@@ -1094,7 +1146,7 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
     const typename Vec<InT>::Thr t2 = Vec<InT>::thr(tB);
     // logit_bias / min_tokens: the row's biased and banned tokens are taken
     // apart (their raw logits skipped below, their values appended at the end)
-    const int nx = has_extras(P.k, ri) ? row_extras<InT>(P.k, ri, 0, V, xi, xv) : 0;
+    const int nx = has_extras(P.k) ? max(0, row_extras<InT>(P.k, ri, 0, V, xi, xv)) : 0;
     int C = C0;
 #pragma unroll 1
     for (int base = 0; base < total; base += 32 * U) {
@@ -1480,7 +1532,7 @@ __device__ __forceinline__ void cta_bias_setup(SliceShared& sh, unsigned char* s
                                                const RowInfo& ri)
 {
     const int tid = threadIdx.x, V = int(kp.vocab);
-    if (!has_extras(kp, ri)) {
+    if (!has_extras(kp)) {
         if (tid == 0) sh.bx_n = 0;
         __syncthreads();
         return;
@@ -1488,7 +1540,7 @@ __device__ __forceinline__ void cta_bias_setup(SliceShared& sh, unsigned char* s
     uint32_t* bits = reinterpret_cast<uint32_t*>(slots);
     for (int w = tid; w < (V + 31) / 32; w += kT) bits[w] = 0u;
     if (tid < 32) {
-        const int n = row_extras<InT>(kp, ri, 0, V, sh.bx_i, sh.bx_v);
+        const int n = max(0, row_extras<InT>(kp, ri, 0, V, sh.bx_i, sh.bx_v));
         if (tid == 0) {
             sh.bx_n = n;
             sh.bx_bits = bits;
@@ -1701,8 +1753,9 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
 
 // ---------------------------------------------------------------- one unit
 // Wait for the warp's slot, summarise the unit into its record (row r, slice s).
+// Returns false, with nothing recorded, when the row's parameters are bad.
 template <typename InT>
-__device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo& ri, uint64_t* bar,
+__device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo& ri, uint64_t* bar,
                                              const unsigned char* slot, uint16_t* q, uint4* qw, int32_t* xi,
                                              float* xv, uint32_t parity, int r, int s, uint32_t off_lo,
                                              uint32_t off_hi)
@@ -1711,6 +1764,26 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
     const int lane = threadIdx.x & 31;
     const KernelParams& kp = P.k;
     const int G = P.G;
+    const int c0 = s * P.W;
+    const int n_el = min(P.W, int(kp.vocab) - c0);
+    // While the copy is in flight: the unit's biased and banned tokens with
+    // their final values (logit_bias / min_tokens), and its vocabulary-mask
+    // words (into the queue scratch, free until the summary).
+    int nx = 0;
+    uint32_t* mws = reinterpret_cast<uint32_t*>(q);
+    if (ri.cls != kClsErr) {
+        if (has_extras(kp)) nx = row_extras<InT>(kp, ri, c0, c0 + n_el, xi, xv);
+        if (kp.vocab_mask && nx >= 0) {
+            const uint32_t* mrow = kp.vocab_mask + size_t(r) * size_t(kp.mask_stride) + (c0 >> 5);
+            const int nw = ((c0 + n_el - 1) >> 5) - (c0 >> 5) + 1;
+            uint32_t w[kMaskWords / 32];
+#pragma unroll
+            for (int i = 0; i < kMaskWords / 32; ++i) w[i] = 32 * i + lane < nw ? __ldg(mrow + 32 * i + lane) : 0u;
+#pragma unroll
+            for (int i = 0; i < kMaskWords / 32; ++i)
+                if (32 * i + lane < nw) mws[32 * i + lane] = w[i];
+        }
+    }
     uint32_t extra = 0;
     // when the wait gives up, the unit is marked and the copy is still awaited
     // (with a longer bound) before the slot is reused
@@ -1719,9 +1792,7 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
         mbar_wait_bounded(bar, parity, kDrainPolls);
     }
     SLC_MARK(3);
-    if (ri.cls == kClsErr) return;
-    const int c0 = s * P.W;
-    const int n_el = min(P.W, int(kp.vocab) - c0);
+    if (ri.cls == kClsErr || nx < 0) return false;
     SliceView<InT> sv;
     sv.sm = reinterpret_cast<const uint4*>(slot);
     sv.g = slice_ptr<InT>(kp, ri.lrow, c0);
@@ -1731,37 +1802,27 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
     sv.c0 = c0;
     // The extensions rewrite the unit in place, so a unit that has one is staged
     // whole: the vectors the bulk copy left out (a ragged tail, an unaligned
-    // slice) are loaded into the slot too (it holds the whole unit).
-    const bool has_x = !extra && (kp.sanitize_nan || kp.vocab_mask || has_extras(kp, ri));
+    // slice) are loaded into the slot too (it holds the whole unit). NaN
+    // sanitising is left to the first lane-maximum pass (a lane that meets a
+    // NaN cleans its vectors).
+    const bool has_x = !extra && (kp.sanitize_nan || kp.vocab_mask || nx > 0);
     uint4* smv = reinterpret_cast<uint4*>(const_cast<unsigned char*>(slot));
     if (has_x && sv.nb < sv.nvec) {
         for (int j = sv.nb + lane; j < sv.nvec; j += 32) smv[j] = sv.vec(j);
-        __syncwarp();
         sv.nb = sv.nvec;
     }
-    if (has_x && kp.sanitize_nan) {  // NaN sanitising: NaN becomes -inf
-#pragma unroll 4
-        for (int j = lane; j < sv.nb; j += 32) {
-            const uint4 v = smv[j], c = Vec<InT>::sanitized(v);
-            if ((v.x ^ c.x) | (v.y ^ c.y) | (v.z ^ c.z) | (v.w ^ c.w)) smv[j] = c;
-        }
-        __syncwarp();
-    }
+    __syncwarp();
+    sv.san = has_x && kp.sanitize_nan;
     if (has_x && kp.vocab_mask) {  // the row's vocabulary mask
-        const uint32_t* mw = kp.vocab_mask + size_t(r) * size_t(kp.mask_stride);
 #pragma unroll 4
         for (int j = lane; j < sv.nb; j += 32) {
-            const int t0 = c0 + j * E;
-            const uint32_t bits = (__ldg(mw + (t0 >> 5)) >> (t0 & 31)) & ((1u << E) - 1u);
+            const int t = j * E + (c0 & 31);
+            const uint32_t bits = (mws[t >> 5] >> (t & 31)) & ((1u << E) - 1u);
             if (bits != (1u << E) - 1u) smv[j] = Vec<InT>::masked(smv[j], bits);
         }
         __syncwarp();
     }
-    int nx = 0;
-    if (has_x && has_extras(kp, ri)) {
-        // logit_bias / min_tokens: the unit's biased and banned tokens are taken
-        // apart with their final values and read as -inf in the slot
-        nx = row_extras<InT>(kp, ri, c0, c0 + n_el, xi, xv);
+    if (has_x && nx) {  // the biased and banned tokens read as -inf in the slot
         uint32_t* smw = reinterpret_cast<uint32_t*>(smv);
         for (int i = lane; i < nx; i += 32) {
             const int o = xi[i] - c0;
@@ -1818,6 +1879,7 @@ __device__ __forceinline__ void process_unit(const SliceParams& P, const RowInfo
             *reinterpret_cast<uint4*>(&body->ga) =
                 make_uint4(uint32_t(g.a), uint32_t(g.a >> 32), uint32_t(g.b), uint32_t(g.b >> 32));
     }
+    return true;
 }
 
 // Finish row r (this warp's arrival completed it), and its logprob outputs when
@@ -1915,11 +1977,11 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
         first = false;
         SLC_MARK(2);
         SLC_UCLS(ri.cls);
-        process_unit<InT>(P, ri, bar, slot, ws.q, ws.qw, ws.xi, ws.xv, parity, r, s, off_lo, off_hi);
+        const bool ok = process_unit<InT>(P, ri, bar, slot, ws.q, ws.qw, ws.xi, ws.xv, parity, r, s, off_lo, off_hi);
         SLC_MARK(5);
         parity ^= 1u;
         const int un = u + stride;
-        if (ri.cls == kClsErr) {
+        if (!ok) {
             if (s == 0 && lane == 0) write_out(kp, r, -1, kRowBadParam);
         } else {
             // the arrival is a release (publishing this unit's record) and an acquire

@@ -76,6 +76,7 @@ constexpr int kReCap = 16;              // slices a finishing warp may read agai
 constexpr int kRankSortMax = 256;       // candidates sorted by counting ranks (more: bitonic)
 constexpr int kSlotBytes = 10240;       // a warp's staging slot
 constexpr int kMinUnit = 2048;          // smallest unit, in elements (unless the row is narrower)
+constexpr int kMaskWords = (kSlotBytes / 2 / 32 + 2 + 31) / 32 * 32;  // mask words a unit spans, rounded up to 32
 constexpr uint32_t kOverflow = 0xFFFFFFFFu;
 constexpr uint32_t kDrainPolls = 1u << 26;  // polls granted to a copy after a wait gave up
 // Each row's arrival counter sits in its own 128-byte line: G warps add to every
@@ -183,6 +184,8 @@ constexpr size_t kMaxSmem = 227 * 1024;
 static_assert(kSmemBytes <= kMaxSmem, "shared memory per CTA");
 static_assert(kSlotBytes >= 1024 * 8, "a free slot holds 1024 candidates");
 static_assert(kTQCap * 4 <= int(sizeof(WarpScratch::q)) && kTQCap > kLCap, "truncated-unit queue");
+static_assert(kMaskWords * 4 <= int(sizeof(WarpScratch::q)) && kMaskWords >= kSlotBytes / 2 / 32 + 2,
+              "a unit's mask words fit the queue scratch");
 
 // ---------------------------------------------------------------- small helpers
 __device__ __forceinline__ void warp_max_idx(float& m, int& i)
@@ -353,6 +356,7 @@ struct SliceView {
     int nvec;        // vectors covering the slice
     int n;           // elements in the slice
     int c0;          // first token of the slice
+    bool san = false;  // NaN sanitising: the first lane-maximum pass cleans the (whole) staged unit
 
     __device__ __forceinline__ uint4 vec(int j) const
     {
