@@ -13,7 +13,9 @@ from typing import Optional
 from . import _binding as abi
 from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHORT_WAITS, SAMPLER_DTYPE_BF16,
                        SAMPLER_DTYPE_F32, SAMPLER_MAX_BIAS, SAMPLER_MAX_STOP, SAMPLER_MAX_TOP_N,
-                       SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
+                       SAMPLER_LM_HEAD_MAX_ROWS, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
+                       SAMPLER_STAT_EXACT_ROWS, SAMPLER_STAT_LM_HEAD_TIMEOUTS, sampler_lm_head_t,
+                       sampler_lm_head_sample,
                        load_library, sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
                        sampler_destroy, sampler_ext_t, sampler_sample, sampler_sample_host,
                        sampler_sample_ex, sampler_sample_noalloc, sampler_status_string,
@@ -22,8 +24,21 @@ from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHO
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
            "sampler_sample_host", "sampler_sample_noalloc", "sampler_sample_ex", "sampler_destroy",
            "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "SAMPLER_MAX_BIAS",
-           "SAMPLER_MAX_STOP", "sampler_ext_t",
+           "SAMPLER_MAX_STOP", "sampler_ext_t", "sampler_lm_head_t", "sampler_lm_head_sample",
+           "SAMPLER_LM_HEAD_MAX_ROWS", "SAMPLER_STAT_EXACT_ROWS", "SAMPLER_STAT_LM_HEAD_TIMEOUTS",
            "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
+
+
+def _make_ext(top_n: int = 0, unscaled: bool = False, out_token_logprob=None, out_top_ids=None,
+              out_top_logprobs=None, vocab_mask=None, mask_stride: Optional[int] = None, bias_offsets=None,
+              bias_ids=None, bias_values=None, min_tokens_left=None, stop_offsets=None, stop_ids=None,
+              sanitize_nan: bool = False) -> sampler_ext_t:
+    if vocab_mask is not None and mask_stride is None:
+        mask_stride = int(vocab_mask.shape[-1])
+    return sampler_ext_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob), _ptr(out_top_ids),
+                         _ptr(out_top_logprobs), _ptr(vocab_mask), int(mask_stride or 0),
+                         _ptr(bias_offsets), _ptr(bias_ids), _ptr(bias_values),
+                         _ptr(min_tokens_left), _ptr(stop_offsets), _ptr(stop_ids), 1 if sanitize_nan else 0)
 
 
 class SamplerError(RuntimeError):
@@ -136,19 +151,33 @@ class Sampler:
         logit_bias lists (device CSR: offsets [N + 1], ids, fp32 values), the
         min_tokens ban (device int32: tokens owed [N], stop-token CSR offsets
         [N + 1] and ids) and NaN sanitising."""
+        ext = _make_ext(top_n, unscaled, out_token_logprob, out_top_ids, out_top_logprobs, vocab_mask,
+                        mask_stride, bias_offsets, bias_ids, bias_values, min_tokens_left, stop_offsets,
+                        stop_ids, sanitize_nan)
+        rc = sampler_sample_ex(self._h, args, ext, self._stream(stream))
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_sample_ex")
+
+    def lm_head_sample_args(self, args: sampler_args_t, hidden, weight, hidden_dim: Optional[int] = None,
+                            hidden_stride: Optional[int] = None, weight_stride: Optional[int] = None,
+                            stream: Optional[int] = None, **ext_kw) -> None:
+        """sampler_lm_head_sample: logits = hidden x weight^T (device bf16 tensors
+        hidden [rows, K], weight [V, K]) written to args.logits, then the step on
+        them; ext_kw as for sample_ex_args."""
+        K = int(hidden_dim if hidden_dim is not None else hidden.shape[-1])
+        lm = sampler_lm_head_t(_ptr(hidden), _ptr(weight), K,
+                               int(hidden_stride if hidden_stride is not None else hidden.stride(0)),
+                               int(weight_stride if weight_stride is not None else weight.stride(0)))
+        ext = _make_ext(**ext_kw) if ext_kw else None
+        rc = sampler_lm_head_sample(self._h, lm, args, ext, self._stream(stream))
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_lm_head_sample")
+
+    def _stream(self, stream: Optional[int]) -> int:
         if stream is None:
             import torch
             stream = torch.cuda.current_stream(self.device).cuda_stream
-        if vocab_mask is not None and mask_stride is None:
-            mask_stride = int(vocab_mask.shape[-1])
-        ext = sampler_ext_t(int(top_n), 1 if unscaled else 0, _ptr(out_token_logprob), _ptr(out_top_ids),
-                            _ptr(out_top_logprobs), _ptr(vocab_mask), int(mask_stride or 0),
-                            _ptr(bias_offsets), _ptr(bias_ids), _ptr(bias_values),
-                            _ptr(min_tokens_left), _ptr(stop_offsets), _ptr(stop_ids),
-                            1 if sanitize_nan else 0)
-        rc = sampler_sample_ex(self._h, args, ext, stream)
-        if rc != SAMPLER_OK:
-            raise SamplerError(rc, "sampler_sample_ex")
+        return stream
 
     def stat(self, which: int = 0, reset: bool = False) -> int:
         """A device diagnostic counter (synchronizes the device)."""

@@ -38,8 +38,10 @@ SAMPLER_CREATE_SHORT_WAITS = 4
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
             "sampler_status_string", "sampler_abi_version", "sampler_get_stat",
-            "sampler_sample_noalloc", "sampler_sample_ex")
+            "sampler_sample_noalloc", "sampler_sample_ex", "sampler_lm_head_sample")
 SAMPLER_STAT_EXACT_ROWS = 0
+SAMPLER_STAT_LM_HEAD_TIMEOUTS = 1
+SAMPLER_LM_HEAD_MAX_ROWS = 256
 SAMPLER_NOALLOC_MAX_ROWS = 64
 SAMPLER_MAX_TOP_N = 16
 SAMPLER_MAX_BIAS = 64
@@ -109,6 +111,16 @@ class sampler_ext_t(ctypes.Structure):
     ]
 
 
+class sampler_lm_head_t(ctypes.Structure):
+    _fields_ = [
+        ("hidden", _P),
+        ("weight", _P),
+        ("hidden_dim", ctypes.c_int64),
+        ("hidden_stride", ctypes.c_int64),
+        ("weight_stride", ctypes.c_int64),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -139,6 +151,9 @@ def load_library(path: str = LIB):
             lib.sampler_sample_noalloc.restype = ctypes.c_int
             lib.sampler_sample_ex.argtypes = [_P, ctypes.POINTER(sampler_args_t), ctypes.POINTER(sampler_ext_t), _P]
             lib.sampler_sample_ex.restype = ctypes.c_int
+            lib.sampler_lm_head_sample.argtypes = [_P, ctypes.POINTER(sampler_lm_head_t), ctypes.POINTER(sampler_args_t),
+                                                   ctypes.POINTER(sampler_ext_t), _P]
+            lib.sampler_lm_head_sample.restype = ctypes.c_int
             lib.sampler_abi_version.argtypes = []
             lib.sampler_abi_version.restype = ctypes.c_uint32
             _lib = lib
@@ -164,6 +179,11 @@ def sampler_sample_ex(h, args: sampler_args_t, ext, stream: int) -> int:
     """ext: a sampler_ext_t or None."""
     return load_library().sampler_sample_ex(h, ctypes.byref(args), ctypes.byref(ext) if ext is not None else None,
                                             _P(stream))
+
+
+def sampler_lm_head_sample(h, lm, args: sampler_args_t, ext, stream: int) -> int:
+    return load_library().sampler_lm_head_sample(h, ctypes.byref(lm), ctypes.byref(args),
+                                                 ctypes.byref(ext) if ext is not None else None, _P(stream))
 
 
 def sampler_sample_noalloc(args: sampler_args_t, stream: int) -> int:

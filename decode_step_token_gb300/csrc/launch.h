@@ -51,9 +51,30 @@ bool slice_geometry(int64_t n_rows, int64_t vocab, int esize, int sms, SliceGeom
 int slice_prepare(int dtype, size_t smem);
 
 // Enqueue one slice-kernel launch. max_polls bounds each wait on a staging copy.
-// ext: the step's extensions (NULL: none)
+// ext: the step's extensions (NULL: none). pdl: launched as the programmatic
+// dependent of the kernel before it on the stream (it waits for that grid
+// before it reads the logits).
 int slice_launch(const sampler_args_t* a, const sampler_ext_t* ext, const SliceGeometry& g,
-                 const SliceWorkspace& ws, uint32_t max_polls, cudaStream_t stream);
+                 const SliceWorkspace& ws, uint32_t max_polls, bool pdl, cudaStream_t stream);
+
+// ---------------------------------------------------------------- LM-head GEMM
+constexpr int kLmHeadMaxRows = 256;  // hidden rows of one launch (the MMA's N)
+
+struct LmHeadPlan {
+    int NT;              // rows rounded up to 16
+    int stages;          // operand stages in shared memory
+    uint32_t tmem_cols;  // tensor-memory columns (two accumulators)
+    int tiles;           // 128-row weight tiles
+    int kchunks;         // 64-wide K stages per tile
+    int ctas;            // persistent grid
+    size_t smem;
+};
+
+bool lm_head_plan(int64_t rows, int64_t vocab, int64_t hidden_dim, int sms, LmHeadPlan* plan);
+int lm_head_prepare(size_t smem);
+// logits [rows, ldl] bf16 = hidden x weight^T; timeouts counts CTAs whose wait gave up.
+int lm_head_launch(const sampler_lm_head_t* g, void* logits, int64_t ldl, int64_t rows, int64_t vocab,
+                   const LmHeadPlan& plan, unsigned long long* timeouts, cudaStream_t stream);
 
 // ---------------------------------------------------------------- fork-group kernel
 // Everything the slice kernel does not take.

@@ -1,8 +1,8 @@
 // sampler_api.cu -- the C ABI of libsampler.so (declared in include/sampler.h):
 // argument checks, the choice of kernel, the handle's workspace, the
-// allocation-free entry point, and the host-buffer entry that stages through
-// the handle's device buffers. The kernels live in slice_kernel.cu and
-// group_kernel.cu.
+// allocation-free entry point, the host-buffer entry that stages through the
+// handle's device buffers, and the LM-head entry. The kernels live in
+// slice_kernel.cu, group_kernel.cu and lm_head_kernel.cu.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -49,6 +49,7 @@ struct sampler_s {
     size_t slice_smem_set[2];  // dynamic shared memory already granted per dtype
     // fork-group kernel
     size_t grp_smem_set[4];
+    size_t lmh_smem_set;     // LM-head GEMM
     size_t grp_occ_smem[4];  // shared memory of the cached cluster occupancy below
     int grp_occ[4];          // co-resident clusters of the fork-group kernel
     unsigned long long* stats;  // device counters (diagnostics)
@@ -86,8 +87,10 @@ int launch_group(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
 }
 
 // lp: the step's extensions, offered on the slice kernel only (the caller has
-// checked that the call takes it)
-int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const sampler_ext_t* lp = nullptr)
+// checked that the call takes it). pdl: a slice-kernel launch is the
+// programmatic dependent of the kernel enqueued before it.
+int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const sampler_ext_t* lp = nullptr,
+           bool pdl = false)
 {
     dst::SliceGeometry g;
     if (slice_takes(a) && a->n_rows <= h->slice_rows &&
@@ -97,7 +100,7 @@ int launch(sampler_t h, const sampler_args_t* a, cudaStream_t stream, const samp
             if (dst::slice_prepare(a->dtype, g.smem) != SAMPLER_OK) return SAMPLER_ERR_CUDA;
             h->slice_smem_set[slot] = g.smem;
         }
-        return dst::slice_launch(a, lp, g, h->slice_ws, h->max_polls, stream);
+        return dst::slice_launch(a, lp, g, h->slice_ws, h->max_polls, pdl, stream);
     }
     if (lp) return SAMPLER_ERR_UNSUPPORTED;
     return launch_group(h, a, stream);
@@ -317,25 +320,72 @@ int sampler_sample(sampler_t h, const sampler_args_t* a, sampler_stream_t stream
     return launch(h, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int sampler_sample_ex(sampler_t h, const sampler_args_t* a, const sampler_ext_t* ext, sampler_stream_t stream)
+namespace {
+
+// Host checks of a step's extensions; *use is NULL when nothing is asked.
+int check_ext(const sampler_args_t* a, const sampler_ext_t* ext, const sampler_ext_t** use)
+{
+    *use = nullptr;
+    if (!ext) return SAMPLER_OK;
+    if (ext->top_n < 0 || ext->top_n > SAMPLER_MAX_TOP_N) return SAMPLER_ERR_UNSUPPORTED;
+    if (ext->top_n > 0 && (!ext->out_top_ids || !ext->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
+    if (ext->vocab_mask && ext->mask_stride < (a->vocab + 31) / 32) return SAMPLER_ERR_UNSUPPORTED;
+    if (ext->bias_offsets && (!ext->bias_ids || !ext->bias_values)) return SAMPLER_ERR_NULL_ARG;
+    if (ext->stop_offsets && !ext->stop_ids) return SAMPLER_ERR_NULL_ARG;
+    if (ext->out_token_logprob || ext->top_n > 0 || ext->vocab_mask || ext->bias_offsets || ext->stop_offsets ||
+        ext->sanitize_nan)
+        *use = ext;
+    return SAMPLER_OK;
+}
+
+}  // namespace
+
+int sampler_sample_ex(sampler_t h, const sampler_args_t* a, const sampler_ext_t* ext_in, sampler_stream_t stream)
 {
     int rc = check_args(h, a);
     if (rc != SAMPLER_OK) return rc;
-    if (ext) {
-        if (ext->top_n < 0 || ext->top_n > SAMPLER_MAX_TOP_N) return SAMPLER_ERR_UNSUPPORTED;
-        if (ext->top_n > 0 && (!ext->out_top_ids || !ext->out_top_logprobs)) return SAMPLER_ERR_NULL_ARG;
-        if (ext->vocab_mask && ext->mask_stride < (a->vocab + 31) / 32) return SAMPLER_ERR_UNSUPPORTED;
-        if (ext->bias_offsets && (!ext->bias_ids || !ext->bias_values)) return SAMPLER_ERR_NULL_ARG;
-        if (ext->stop_offsets && !ext->stop_ids) return SAMPLER_ERR_NULL_ARG;
-        if (!ext->out_token_logprob && ext->top_n == 0 && !ext->vocab_mask && !ext->bias_offsets &&
-            !ext->stop_offsets && !ext->sanitize_nan)
-            ext = nullptr;  // nothing asked
-    }
+    const sampler_ext_t* ext = nullptr;
+    rc = check_ext(a, ext_in, &ext);
+    if (rc != SAMPLER_OK) return rc;
     if (a->n_rows == 0) return SAMPLER_OK;
     DeviceGuard guard;
     if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
     if (ext && !slice_would_take(h, a)) return SAMPLER_ERR_UNSUPPORTED;
     return launch(h, a, reinterpret_cast<cudaStream_t>(stream), ext);
+}
+
+int sampler_lm_head_sample(sampler_t h, const sampler_lm_head_t* lm, const sampler_args_t* a,
+                           const sampler_ext_t* ext_in, sampler_stream_t stream_)
+{
+    int rc = check_args(h, a);
+    if (rc != SAMPLER_OK) return rc;
+    if (!lm) return SAMPLER_ERR_NULL_ARG;
+    const sampler_ext_t* ext = nullptr;
+    rc = check_ext(a, ext_in, &ext);
+    if (rc != SAMPLER_OK) return rc;
+    if (a->n_rows == 0) return SAMPLER_OK;
+    if (a->dtype != SAMPLER_DTYPE_BF16) return SAMPLER_ERR_BAD_DTYPE;
+    if (!lm->hidden || !lm->weight) return SAMPLER_ERR_NULL_ARG;
+    if (lm->hidden_dim < 1 || lm->hidden_stride < lm->hidden_dim || lm->weight_stride < lm->hidden_dim ||
+        lm->hidden_stride % 8 != 0 || lm->weight_stride % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(lm->hidden) % 16 != 0 || reinterpret_cast<uintptr_t>(lm->weight) % 16 != 0)
+        return SAMPLER_ERR_BAD_SHAPE;
+    const int64_t rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
+    if (rows > SAMPLER_LM_HEAD_MAX_ROWS) return SAMPLER_ERR_TOO_LARGE;
+    DeviceGuard guard;
+    if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    if (ext && !slice_would_take(h, a)) return SAMPLER_ERR_UNSUPPORTED;
+    dst::LmHeadPlan plan;
+    if (!dst::lm_head_plan(rows, a->vocab, lm->hidden_dim, h->num_sms, &plan)) return SAMPLER_ERR_TOO_LARGE;
+    if (h->lmh_smem_set < plan.smem) {
+        if (dst::lm_head_prepare(plan.smem) != SAMPLER_OK) return SAMPLER_ERR_CUDA;
+        h->lmh_smem_set = plan.smem;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    rc = dst::lm_head_launch(lm, const_cast<void*>(a->logits), a->row_stride, rows, a->vocab, plan,
+                             h->stats + SAMPLER_STAT_LM_HEAD_TIMEOUTS, stream);
+    if (rc != SAMPLER_OK) return rc;
+    return launch(h, a, stream, ext, true);
 }
 
 int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
@@ -365,7 +415,7 @@ int sampler_sample_noalloc(const sampler_args_t* a, sampler_stream_t stream_)
     ws.hdr = d.scratch + kNoAllocCounterBytes;
     ws.body = d.scratch + kNoAllocCounterBytes + kNoAllocHdrBytes;
     ws.stats = nullptr;
-    return dst::slice_launch(a, nullptr, g, ws, kMaxPolls, stream);
+    return dst::slice_launch(a, nullptr, g, ws, kMaxPolls, false, stream);
 }
 
 int sampler_sample_host(sampler_t h, const sampler_args_t* a, sampler_stream_t stream_)

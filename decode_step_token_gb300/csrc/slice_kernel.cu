@@ -72,7 +72,7 @@ int slice_prepare(int dtype, size_t smem)
 }
 
 int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGeometry& g,
-                 const SliceWorkspace& ws, uint32_t max_polls, cudaStream_t stream)
+                 const SliceWorkspace& ws, uint32_t max_polls, bool pdl, cudaStream_t stream)
 {
     slc::SliceParams p;
     std::memset(&p, 0, sizeof p);
@@ -122,6 +122,7 @@ int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGe
     p.cnt = ws.cnt;
     p.stats = ws.stats;
     p.max_polls = max_polls;
+    p.pdl = pdl ? 1 : 0;
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -129,6 +130,13 @@ int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGe
     cfg.blockDim = dim3(slc::kT);
     cfg.dynamicSmemBytes = g.smem;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     void* fn = a->dtype == SAMPLER_DTYPE_BF16 ? kernel_of<uint16_t>() : kernel_of<float>();
     void* args[] = {&p};
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;

@@ -1921,12 +1921,14 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
     SLC_MARK(0);
     // slot s of the CTA stages its units blockIdx.x + s * NC (+ k * stride):
     // round-robin over CTAs first. The copy of its first unit goes out before
-    // anything else.
+    // anything else, unless the kernel is the programmatic dependent of the
+    // grid that writes the logits: then it goes out once that grid is done,
+    // after the set-up below.
+    const int u0 = int(blockIdx.x) + wid * NC;
     if (lane == 0) {
-        const int u0 = int(blockIdx.x) + wid * NC;
         mbar_init(&sh.full[wid], 1);
         fence_mbar_init();
-        if (u0 < P.n_units) issue_unit<InT>(P, &sh.full[wid], smem + kHead + size_t(wid) * kSlotBytes, u0);
+        if (!P.pdl && u0 < P.n_units) issue_unit<InT>(P, &sh.full[wid], smem + kHead + size_t(wid) * kSlotBytes, u0);
     }
     if (tid == 0) sh.n_exact = 0;
     const uint64_t off = kp.philox_offset_dev ? *kp.philox_offset_dev : kp.philox_offset;
@@ -1962,6 +1964,11 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
 #pragma unroll
         for (int q = 0; q < int(sizeof(RowInfo) / 4); ++q) w0[q] = __shfl_sync(0xffffffffu, wmine[q], sidx);
         memcpy(&ri0, w0, sizeof(RowInfo));
+    }
+    if (P.pdl) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (lane == 0 && u0 < P.n_units)
+            issue_unit<InT>(P, &sh.full[wid], smem + kHead + size_t(wid) * kSlotBytes, u0);
     }
     unsigned char* slot = smem + kHead + size_t(sidx) * kSlotBytes;
     uint64_t* bar = &sh.full[sidx];

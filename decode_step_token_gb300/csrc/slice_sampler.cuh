@@ -121,6 +121,7 @@ struct SliceParams {
     uint32_t* cnt;       // [n_rows * kCntStride] arrivals (one per line); zero between launches
     unsigned long long* stats;  // [0]: rows finished by the exact path (may be NULL)
     uint32_t max_polls;  // bound of each wait on a staging copy
+    int32_t pdl;         // launched as a programmatic dependent: wait for the grid before it
 };
 
 struct alignas(16) RowInfo {

@@ -306,6 +306,42 @@ typedef struct {
 int sampler_sample_ex(sampler_t h, const sampler_args_t* args, const sampler_ext_t* ext,
                       sampler_stream_t stream);
 
+/*
+ * The LM head and the sampler of one decode step (sampler_lm_head_sample).
+ *
+ * The xbrilliance.ai note on sampling cost (section "what sampling does in one
+ * decode step") has the LM head produce the [num_seqs, vocab_size] logits as
+ * matmul(hidden_states, embedding.t()) and pass them to the sampler. This call
+ * does both: first, on the tensor cores,
+ *     logits[i, v] = bf16(sum_k hidden[i, k] * weight[v, k])   (fp32 sums,
+ *                                                             round to nearest even)
+ * for i < n_logit_rows (n_rows when 0) into args->logits (bf16, row_stride
+ * elements apart), then the step of sampler_sample_ex on those logits. When
+ * the small-batch kernel takes the step it is launched as the GEMM's
+ * programmatic dependent: its set-up overlaps the GEMM's tail and it waits for
+ * the GEMM before it reads the logits. The GEMM's waits are bounded; a CTA
+ * whose wait gives up leaves its logits unwritten and counts itself in
+ * SAMPLER_STAT_LM_HEAD_TIMEOUTS.
+ *
+ * hidden: [n_logit_rows, hidden_stride] bf16, one row per logits row; weight:
+ * [vocab, weight_stride] bf16, one row per token (an untied LM head or the
+ * tied embedding). Both 16-byte aligned, strides multiples of 8 elements and
+ * >= hidden_dim, else SAMPLER_ERR_BAD_SHAPE. args->dtype must be
+ * SAMPLER_DTYPE_BF16 (SAMPLER_ERR_BAD_DTYPE); at most SAMPLER_LM_HEAD_MAX_ROWS
+ * logits rows (SAMPLER_ERR_TOO_LARGE). ext as for sampler_sample_ex.
+ */
+#define SAMPLER_LM_HEAD_MAX_ROWS 256
+typedef struct {
+    const void* hidden;       /* [n_logit_rows, hidden_stride] bf16 */
+    const void* weight;       /* [vocab, weight_stride] bf16 */
+    int64_t hidden_dim;       /* K >= 1 */
+    int64_t hidden_stride;    /* elements between hidden rows */
+    int64_t weight_stride;    /* elements between weight rows */
+} sampler_lm_head_t;
+
+int sampler_lm_head_sample(sampler_t h, const sampler_lm_head_t* lm, const sampler_args_t* args,
+                           const sampler_ext_t* ext, sampler_stream_t stream);
+
 /* Release the handle and its device memory. NULL is a no-op. */
 void sampler_destroy(sampler_t h);
 
@@ -317,8 +353,10 @@ const char* sampler_status_string(int code);
  *                            per-slice candidate lists could not settle (top-k
  *                            above 128, a top-p cut past the lists, too many
  *                            candidates), finished by its slower exact path.
+ *   SAMPLER_STAT_LM_HEAD_TIMEOUTS  CTAs of the LM-head GEMM whose bounded wait
+ *                            gave up (their logits were left unwritten).
  * Writes the count to *value and clears it when reset != 0. */
-enum { SAMPLER_STAT_EXACT_ROWS = 0 };
+enum { SAMPLER_STAT_EXACT_ROWS = 0, SAMPLER_STAT_LM_HEAD_TIMEOUTS = 1 };
 int sampler_get_stat(sampler_t h, int which, uint64_t* value, int reset);
 
 /* ABI version of this header: (major << 16) | minor. */

@@ -9,7 +9,8 @@ The arithmetic lives in ``sampler_oracle.c`` (plain C, double precision after
 the fp32 penalties, full sort per row, explicit cumulative sums, its own
 Philox4x32-10). This module compiles it on first use with gcc and marshals
 numpy arrays through ctypes. ``batch_paths`` restates the pages' batch-wide
-path predicates, which the per-row design does not use.
+path predicates, which the per-row design does not use. ``lm_head_logits`` is
+the LM head's matrix product written out in double precision.
 """
 from __future__ import annotations
 
@@ -288,3 +289,24 @@ def logprob_outputs(batch, result: OracleResult, top_n: int, unscaled: bool = Fa
             ids[j, q] = v
             lps[j, q] = lp[v]
     return LogprobOutputs(tok, ids, lps)
+
+
+# ---------------------------------------------------------------- LM head
+def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float64 (exact: bf16 is the top half of a float32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def lm_head_logits(hidden_bits: np.ndarray, weight_bits: np.ndarray, cols: Optional[np.ndarray] = None):
+    """The LM head of the xbrilliance.ai note's decode step (section
+    "解码一步里采样做什么": the logits are matmul(hidden_states, embedding.t())):
+    logits[i, v] = sum_k hidden[i, k] * weight[v, k], from bf16 inputs, in
+    float64 (every product of two bf16 values is exact in double; the sum's
+    rounding is ~1e-16 relative). Also returns sum_k |hidden[i, k] * weight[v, k]|,
+    the scale of the rounding error a lower-precision sum may make.
+    ``cols``: only those vocabulary rows (the returned columns follow its order).
+    """
+    h = _bf16_to_f64(hidden_bits)
+    w = _bf16_to_f64(weight_bits if cols is None else weight_bits[cols])
+    return h @ w.T, np.abs(h) @ np.abs(w).T

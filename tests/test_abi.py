@@ -46,7 +46,7 @@ def test_python_binding_uses_the_abi_names(lib):
 def test_struct_layouts_match_the_header(tmp_path):
     import decode_step_token_gb300 as d
     structs = [("sampler_args_t", d.sampler_args_t), ("sampler_config_t", d.sampler_config_t),
-               ("sampler_ext_t", d.sampler_ext_t)]
+               ("sampler_ext_t", d.sampler_ext_t), ("sampler_lm_head_t", d.sampler_lm_head_t)]
     src = tmp_path / "layout.c"
     body = ['#include <stdio.h>', '#include <stddef.h>', '#include "sampler.h"', "int main(void){"]
     for name, st in structs:

@@ -51,6 +51,8 @@ __all__ = [
     "logit_bias",
     "ablation",
     "ABLATION_STAGES",
+    "min_tokens",
+    "lm_head",
     "WORKLOADS",
     "make",
 ]
@@ -385,3 +387,24 @@ WORKLOADS = {
 
 def make(name: str) -> SamplerBatch:
     return WORKLOADS[name]()
+
+
+def lm_head(seed: int = 6, n: int = 64, v: int = 128000, k: int = 4096, *, weight: bool = True):
+    """An LM-head decode step: hidden states [n, k] ~ N(0, 1) and an LM-head
+    weight [v, k] ~ N(0, (2 / sqrt(k))^2), both rounded to bf16 (bits), so that
+    the logits are ~ N(0, 4) like the mixed batch's; and the sampler parameters
+    of the mixed batch (32 rows T=0.8, 16 rows top_k=50 top_p=0.9, 16 greedy at
+    n = 64) with a placeholder for the logits the LM head writes.
+    ``weight=False`` skips the weight (the caller draws it on the device)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    hidden = to_bf16_bits(rng.standard_normal((n, k), dtype=np.float32))
+    w = None
+    if weight:
+        w = to_bf16_bits(rng.standard_normal((v, k), dtype=np.float32) * np.float32(2.0 / np.sqrt(k)))
+    kinds = np.array([0] * (n // 2) + [1] * (n // 4) + [2] * (n - n // 2 - n // 4))
+    rng.shuffle(kinds)
+    t = np.where(kinds == 0, 0.8, np.where(kinds == 1, 1.0, 0.0))
+    b = SamplerBatch("lm_head", np.zeros((n, v), np.uint16), "bf16", v, n, _f32(t),
+                     top_k=np.where(kinds == 1, 50, -1).astype(np.int32),
+                     top_p=_f32(np.where(kinds == 1, 0.9, 1.0)), notes={"kinds": kinds})
+    return hidden, w, b

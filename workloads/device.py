@@ -149,3 +149,42 @@ def run_logprobs(sampler, batch, top_n: int, unscaled: bool = False, device="cud
     return GpuLogprobResult(d["out_tokens"].cpu().numpy(), d["out_status"].cpu().numpy(),
                             tok_lp.cpu().numpy() if tok_lp is not None else None,
                             ids.cpu().numpy()[:, :top_n], lps.cpu().numpy()[:, :top_n])
+
+
+class GpuLmHeadResult:
+    def __init__(self, logits, tokens, status):
+        self.logits, self.tokens, self.status = logits, tokens, status
+        self.probs = self.logprobs = None
+
+
+def bf16_device(bits, device="cuda:0", stride: Optional[int] = None):
+    """Host bf16 bits [rows, k] -> a device int16 tensor [rows, stride] (k <= stride;
+    the padding holds NaN bits, which the product must never read)."""
+    import torch
+
+    rows, k = bits.shape
+    stride = k if stride is None else stride
+    t = torch.full((rows, stride), 0x7FC0, dtype=torch.int16, device=device)
+    t[:, :k] = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    return t
+
+
+def run_lm_head(sampler, hidden, weight, batch, device="cuda:0", hidden_stride: Optional[int] = None,
+                weight_stride: Optional[int] = None, sentinel: int = 0x7F81, **ext) -> GpuLmHeadResult:
+    """One synchronous sampler_lm_head_sample call. `hidden` / `weight`: host bf16
+    bits or device int16 tensors; batch.logits (its shape gives the row stride) is
+    filled with `sentinel` bits on the device and receives the logits. Results
+    (the logits buffer as bf16 bits, tokens, status) back on the host."""
+    import torch
+
+    K = int(hidden.shape[1])
+    h = hidden if isinstance(hidden, torch.Tensor) else bf16_device(hidden, device, hidden_stride)
+    w = weight if isinstance(weight, torch.Tensor) else bf16_device(weight, device, weight_stride)
+    d = to_device(batch, device, False)
+    d["logits"][0].view(torch.int16).fill_(sentinel - 0x10000 if sentinel >= 0x8000 else sentinel)
+    args = sample_args(sampler, batch, d)
+    sampler.lm_head_sample_args(args, h, w, hidden_dim=K, hidden_stride=int(h.stride(0)),
+                                weight_stride=int(w.stride(0)), **ext)
+    torch.cuda.synchronize()
+    logits = d["logits"][0].view(torch.int16).cpu().numpy().view(np.uint16)
+    return GpuLmHeadResult(logits, d["out_tokens"].cpu().numpy(), d["out_status"].cpu().numpy())
