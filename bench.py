@@ -17,7 +17,8 @@ per-family workloads (plain -> +top-k/top-p -> +min-p -> +penalties);
 `logprob_outputs` times the same step with the per-row logprob outputs
 (sampled token + top 5, scaled and unscaled); `extensions` with a
 vocabulary mask, with logit_bias lists, with a min_tokens ban and with NaN
-sanitising.
+sanitising; `lm_head` the LM-head GEMM (tcgen05) before the sampler, alone,
+chained, and against cuBLAS.
 `--impl reference` times the CPU oracle itself (the only reference this
 sampler has), one row per step. Several GPUs run independent replicas (rows
 are independent: no collective).
@@ -463,6 +464,78 @@ def run_extensions(torch, pkg, wdev, batch, dev, local, seconds):
     return out
 
 
+class FnReplayer(Replayer):
+    """CUDA graphs of R calls of fn(stream) (same run() / sustained() interface)."""
+
+    def __init__(self, torch, fn, stream, R):
+        super().__init__(torch, None, [None] * R, stream)
+        self.fn = fn
+
+    def graph(self, r):
+        if r not in self.graphs:
+            torch = self.torch
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g, stream=self.stream):
+                    for _ in range(r):
+                        self.fn(torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            self.graphs[r] = g
+        return self.graphs[r]
+
+
+def run_lm_head(torch, pkg, wdev, dev, local, seconds, n=64, V=128000, K=4096):
+    """The LM-head step: logits = hidden x weight^T (bf16, K = 4096, weight 1 GB,
+    larger than L2) on the tcgen05 GEMM, then the mixed batch's sampling on
+    them. Times the GEMM alone, the sampler alone on its logits (L2-warm), the
+    two in plain stream order, the two chained by sampler_lm_head_sample
+    (programmatic dependent launch), cuBLAS (torch.matmul) alone and followed
+    by the sampler."""
+    import workloads
+
+    hidden_bits, _, b = workloads.lm_head(6, n, V, K, weight=False)
+    gen = torch.Generator(device=dev).manual_seed(6)
+    w = (torch.randn((V, K), generator=gen, device=dev) * (2.0 / np.sqrt(K))).to(torch.bfloat16)
+    torch.cuda.empty_cache()
+    h = torch.from_numpy(hidden_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    sampler = pkg.Sampler(max_rows=n, max_vocab=V, device=local)
+    d = wdev.to_device(b, dev, False)
+    args = wdev.sample_args(sampler, b, d)
+    logits = d["logits"][0]
+    stream = torch.cuda.Stream(device=dev)
+    variants = {
+        "gemm": lambda st: sampler.lm_head(h, w, logits, stream=st),
+        "sampler": lambda st: sampler.sample_args(args, st),
+        "chained": lambda st: sampler.lm_head_sample_args(args, h, w, stream=st),
+        "cublas_gemm": lambda st: torch.matmul(h, w.t(), out=logits),
+    }
+    variants["gemm_then_sampler"] = lambda st: (variants["gemm"](st), variants["sampler"](st))
+    variants["cublas_then_sampler"] = lambda st: (variants["cublas_gemm"](st), variants["sampler"](st))
+    out = {"n_rows": n, "vocab": V, "hidden_dim": K}
+    with torch.cuda.stream(stream):
+        for f in variants.values():  # first calls outside capture (kernel attributes, cuBLAS handles)
+            f(stream.cuda_stream)
+    torch.cuda.synchronize()
+    for name, f in variants.items():
+        rep = FnReplayer(torch, f, stream, 8)
+        rep.run(16)
+        out[name] = stats_us(sustained(rep, seconds))
+    gemm_bytes = V * K * 2 + n * K * 2 + n * V * 2
+    peak, kind = measured_peaks()
+    t = out["gemm"]["median_us"] * 1e-6
+    out["gemm_roofline"] = {"bound": "hbm", "algorithmic_bytes": gemm_bytes, "achieved": gemm_bytes / t / 1e9,
+                            "peak": peak, "unit": "GB/s", "frac": gemm_bytes / t / 1e9 / peak,
+                            "peak_source": f"{kind} hbm_gbs", "tflops": 2.0 * n * V * K / t / 1e12}
+    # what the programmatic dependent launch saves against the same two kernels in
+    # plain stream order (the sampler alone re-reads logits that stay in L2)
+    out["chained_saving_us"] = out["gemm_then_sampler"]["median_us"] - out["chained"]["median_us"]
+    out["timeouts"] = sampler.stat(1)
+    sampler.close()
+    del w, h, d
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ablation(torch, pkg, wdev, dev, local, seconds):
     """Median step time of each per-family workload (plain -> +top-k/top-p ->
     +min-p -> +penalties) at N=64, V=128000 bf16."""
@@ -568,10 +641,12 @@ def run_ours(args):
     abl = None
     lpo = None
     ext = None
+    lmh = None
     if not args.no_ablation and args.workload == "mixed":
         lpo = run_logprob_outputs(torch, sampler, rep, batch, dev, 5, args.ablation_seconds)
         ext = run_extensions(torch, pkg, wdev, batch, dev, local, args.ablation_seconds)
         abl = run_ablation(torch, pkg, wdev, dev, local, args.ablation_seconds)
+        lmh = run_lm_head(torch, pkg, wdev, dev, local, args.ablation_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
@@ -593,6 +668,7 @@ def run_ours(args):
         "ablation": abl,
         "logprob_outputs": lpo,
         "extensions": ext,
+        "lm_head": lmh,
         "kernel_hash": kernel_hash(),
         "first_tokens": tokens[:8].tolist(),
     }

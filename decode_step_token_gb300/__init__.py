@@ -15,7 +15,7 @@ from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHO
                        SAMPLER_DTYPE_F32, SAMPLER_MAX_BIAS, SAMPLER_MAX_STOP, SAMPLER_MAX_TOP_N,
                        SAMPLER_LM_HEAD_MAX_ROWS, SAMPLER_NOALLOC_MAX_ROWS, SAMPLER_OK,
                        SAMPLER_STAT_EXACT_ROWS, SAMPLER_STAT_LM_HEAD_TIMEOUTS, sampler_lm_head_t,
-                       sampler_lm_head_sample,
+                       sampler_lm_head_sample, sampler_lm_head,
                        load_library, sampler_abi_version, sampler_args_t, sampler_config_t, sampler_create,
                        sampler_destroy, sampler_ext_t, sampler_sample, sampler_sample_host,
                        sampler_sample_ex, sampler_sample_noalloc, sampler_status_string,
@@ -24,7 +24,7 @@ from ._binding import (EXPORTED, SAMPLER_CREATE_HOST_STAGING, SAMPLER_CREATE_SHO
 __all__ = ["Sampler", "SamplerError", "load_library", "sampler_create", "sampler_sample",
            "sampler_sample_host", "sampler_sample_noalloc", "sampler_sample_ex", "sampler_destroy",
            "sampler_status_string", "SAMPLER_NOALLOC_MAX_ROWS", "SAMPLER_MAX_TOP_N", "SAMPLER_MAX_BIAS",
-           "SAMPLER_MAX_STOP", "sampler_ext_t", "sampler_lm_head_t", "sampler_lm_head_sample",
+           "SAMPLER_MAX_STOP", "sampler_ext_t", "sampler_lm_head_t", "sampler_lm_head_sample", "sampler_lm_head",
            "SAMPLER_LM_HEAD_MAX_ROWS", "SAMPLER_STAT_EXACT_ROWS", "SAMPLER_STAT_LM_HEAD_TIMEOUTS",
            "sampler_abi_version", "sampler_args_t", "sampler_config_t", "EXPORTED"]
 
@@ -172,6 +172,23 @@ class Sampler:
         rc = sampler_lm_head_sample(self._h, lm, args, ext, self._stream(stream))
         if rc != SAMPLER_OK:
             raise SamplerError(rc, "sampler_lm_head_sample")
+
+    def lm_head(self, hidden, weight, logits, rows: Optional[int] = None, vocab: Optional[int] = None,
+                hidden_dim: Optional[int] = None, hidden_stride: Optional[int] = None,
+                weight_stride: Optional[int] = None, logits_stride: Optional[int] = None,
+                stream: Optional[int] = None) -> None:
+        """sampler_lm_head: logits = hidden x weight^T (device bf16 tensors hidden
+        [rows, K], weight [V, K], logits [rows, stride])."""
+        K = int(hidden_dim if hidden_dim is not None else hidden.shape[-1])
+        lm = sampler_lm_head_t(_ptr(hidden), _ptr(weight), K,
+                               int(hidden_stride if hidden_stride is not None else hidden.stride(0)),
+                               int(weight_stride if weight_stride is not None else weight.stride(0)))
+        rc = sampler_lm_head(self._h, lm, _ptr(logits),
+                             int(logits_stride if logits_stride is not None else logits.stride(0)),
+                             int(rows if rows is not None else hidden.shape[0]),
+                             int(vocab if vocab is not None else weight.shape[0]), self._stream(stream))
+        if rc != SAMPLER_OK:
+            raise SamplerError(rc, "sampler_lm_head")
 
     def _stream(self, stream: Optional[int]) -> int:
         if stream is None:

@@ -38,7 +38,7 @@ SAMPLER_CREATE_SHORT_WAITS = 4
 
 EXPORTED = ("sampler_create", "sampler_sample", "sampler_sample_host", "sampler_destroy",
             "sampler_status_string", "sampler_abi_version", "sampler_get_stat",
-            "sampler_sample_noalloc", "sampler_sample_ex", "sampler_lm_head_sample")
+            "sampler_sample_noalloc", "sampler_sample_ex", "sampler_lm_head_sample", "sampler_lm_head")
 SAMPLER_STAT_EXACT_ROWS = 0
 SAMPLER_STAT_LM_HEAD_TIMEOUTS = 1
 SAMPLER_LM_HEAD_MAX_ROWS = 256
@@ -154,6 +154,9 @@ def load_library(path: str = LIB):
             lib.sampler_lm_head_sample.argtypes = [_P, ctypes.POINTER(sampler_lm_head_t), ctypes.POINTER(sampler_args_t),
                                                    ctypes.POINTER(sampler_ext_t), _P]
             lib.sampler_lm_head_sample.restype = ctypes.c_int
+            lib.sampler_lm_head.argtypes = [_P, ctypes.POINTER(sampler_lm_head_t), _P, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, _P]
+            lib.sampler_lm_head.restype = ctypes.c_int
             lib.sampler_abi_version.argtypes = []
             lib.sampler_abi_version.restype = ctypes.c_uint32
             _lib = lib
@@ -184,6 +187,11 @@ def sampler_sample_ex(h, args: sampler_args_t, ext, stream: int) -> int:
 def sampler_lm_head_sample(h, lm, args: sampler_args_t, ext, stream: int) -> int:
     return load_library().sampler_lm_head_sample(h, ctypes.byref(lm), ctypes.byref(args),
                                                  ctypes.byref(ext) if ext is not None else None, _P(stream))
+
+
+def sampler_lm_head(h, lm, logits: int, logits_stride: int, rows: int, vocab: int, stream: int) -> int:
+    return load_library().sampler_lm_head(h, ctypes.byref(lm), _P(logits), logits_stride, rows, vocab,
+                                          _P(stream))
 
 
 def sampler_sample_noalloc(args: sampler_args_t, stream: int) -> int:

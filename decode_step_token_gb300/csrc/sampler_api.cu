@@ -354,6 +354,46 @@ int sampler_sample_ex(sampler_t h, const sampler_args_t* a, const sampler_ext_t*
     return launch(h, a, reinterpret_cast<cudaStream_t>(stream), ext);
 }
 
+namespace {
+
+int check_lm(const sampler_lm_head_t* lm)
+{
+    if (!lm || !lm->hidden || !lm->weight) return SAMPLER_ERR_NULL_ARG;
+    if (lm->hidden_dim < 1 || lm->hidden_stride < lm->hidden_dim || lm->weight_stride < lm->hidden_dim ||
+        lm->hidden_stride % 8 != 0 || lm->weight_stride % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(lm->hidden) % 16 != 0 || reinterpret_cast<uintptr_t>(lm->weight) % 16 != 0)
+        return SAMPLER_ERR_BAD_SHAPE;
+    return SAMPLER_OK;
+}
+
+// Enqueue the LM-head GEMM (the caller has checked lm and set the device).
+int launch_lm_head(sampler_t h, const sampler_lm_head_t* lm, void* logits, int64_t ldl, int64_t rows, int64_t vocab,
+                   cudaStream_t stream)
+{
+    dst::LmHeadPlan plan;
+    if (!dst::lm_head_plan(rows, vocab, lm->hidden_dim, h->num_sms, &plan)) return SAMPLER_ERR_TOO_LARGE;
+    if (h->lmh_smem_set < plan.smem) {
+        if (dst::lm_head_prepare(plan.smem) != SAMPLER_OK) return SAMPLER_ERR_CUDA;
+        h->lmh_smem_set = plan.smem;
+    }
+    return dst::lm_head_launch(lm, logits, ldl, rows, vocab, plan, h->stats + SAMPLER_STAT_LM_HEAD_TIMEOUTS, stream);
+}
+
+}  // namespace
+
+int sampler_lm_head(sampler_t h, const sampler_lm_head_t* lm, void* logits, int64_t ldl, int64_t rows,
+                    int64_t vocab, sampler_stream_t stream)
+{
+    if (!h || !logits) return SAMPLER_ERR_NULL_ARG;
+    int rc = check_lm(lm);
+    if (rc != SAMPLER_OK) return rc;
+    if (rows < 1 || vocab < 1 || ldl < vocab) return SAMPLER_ERR_BAD_SHAPE;
+    if (rows > SAMPLER_LM_HEAD_MAX_ROWS || vocab > h->max_vocab) return SAMPLER_ERR_TOO_LARGE;
+    DeviceGuard guard;
+    if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
+    return launch_lm_head(h, lm, logits, ldl, rows, vocab, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int sampler_lm_head_sample(sampler_t h, const sampler_lm_head_t* lm, const sampler_args_t* a,
                            const sampler_ext_t* ext_in, sampler_stream_t stream_)
 {
@@ -365,25 +405,15 @@ int sampler_lm_head_sample(sampler_t h, const sampler_lm_head_t* lm, const sampl
     if (rc != SAMPLER_OK) return rc;
     if (a->n_rows == 0) return SAMPLER_OK;
     if (a->dtype != SAMPLER_DTYPE_BF16) return SAMPLER_ERR_BAD_DTYPE;
-    if (!lm->hidden || !lm->weight) return SAMPLER_ERR_NULL_ARG;
-    if (lm->hidden_dim < 1 || lm->hidden_stride < lm->hidden_dim || lm->weight_stride < lm->hidden_dim ||
-        lm->hidden_stride % 8 != 0 || lm->weight_stride % 8 != 0 ||
-        reinterpret_cast<uintptr_t>(lm->hidden) % 16 != 0 || reinterpret_cast<uintptr_t>(lm->weight) % 16 != 0)
-        return SAMPLER_ERR_BAD_SHAPE;
+    rc = check_lm(lm);
+    if (rc != SAMPLER_OK) return rc;
     const int64_t rows = a->n_logit_rows > 0 ? a->n_logit_rows : a->n_rows;
     if (rows > SAMPLER_LM_HEAD_MAX_ROWS) return SAMPLER_ERR_TOO_LARGE;
     DeviceGuard guard;
     if (cudaSetDevice(h->device) != cudaSuccess) return SAMPLER_ERR_CUDA;
     if (ext && !slice_would_take(h, a)) return SAMPLER_ERR_UNSUPPORTED;
-    dst::LmHeadPlan plan;
-    if (!dst::lm_head_plan(rows, a->vocab, lm->hidden_dim, h->num_sms, &plan)) return SAMPLER_ERR_TOO_LARGE;
-    if (h->lmh_smem_set < plan.smem) {
-        if (dst::lm_head_prepare(plan.smem) != SAMPLER_OK) return SAMPLER_ERR_CUDA;
-        h->lmh_smem_set = plan.smem;
-    }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    rc = dst::lm_head_launch(lm, const_cast<void*>(a->logits), a->row_stride, rows, a->vocab, plan,
-                             h->stats + SAMPLER_STAT_LM_HEAD_TIMEOUTS, stream);
+    rc = launch_lm_head(h, lm, const_cast<void*>(a->logits), a->row_stride, rows, a->vocab, stream);
     if (rc != SAMPLER_OK) return rc;
     return launch(h, a, stream, ext, true);
 }

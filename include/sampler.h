@@ -342,6 +342,13 @@ typedef struct {
 int sampler_lm_head_sample(sampler_t h, const sampler_lm_head_t* lm, const sampler_args_t* args,
                            const sampler_ext_t* ext, sampler_stream_t stream);
 
+/* The LM head alone: logits[i, v] for i < rows, v < vocab, computed as by
+ * sampler_lm_head_sample, into `logits` (bf16, logits_stride >= vocab elements
+ * apart). rows in [1, SAMPLER_LM_HEAD_MAX_ROWS], vocab <= the handle's
+ * max_vocab (SAMPLER_ERR_TOO_LARGE); lm checked as above. */
+int sampler_lm_head(sampler_t h, const sampler_lm_head_t* lm, void* logits, int64_t logits_stride, int64_t rows,
+                    int64_t vocab, sampler_stream_t stream);
+
 /* Release the handle and its device memory. NULL is a no-op. */
 void sampler_destroy(sampler_t h);
 

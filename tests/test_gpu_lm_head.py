@@ -160,3 +160,16 @@ def test_refusals(sampler):
         sampler.lm_head_sample_args(dev.sample_args(sampler, big, db), dev.bf16_device(big_h), w)
     assert e.value.code == -3
     assert sampler.stat(dd.SAMPLER_STAT_LM_HEAD_TIMEOUTS) == 0
+
+
+def test_logits_only_entry(sampler):
+    import torch
+
+    hidden, weight, b = workloads.lm_head(87, 40, 7000, 384)
+    g = dev.run_lm_head(sampler, hidden, weight, b)
+    out = torch.zeros((40, 7008), dtype=torch.int16, device="cuda:0")
+    sampler.lm_head(dev.bf16_device(hidden), dev.bf16_device(weight), out, vocab=7000)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[:, :7000], g.logits)
+    assert np.all(got[:, 7000:] == 0)
