@@ -739,10 +739,21 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-rotate", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--lm-head-only", action="store_true",
+                    help="run only the LM-head leg (GEMM, sampler, chained, cuBLAS) and print its JSON")
+    ap.add_argument("--hidden-dim", type=int, default=4096, help="K of the LM-head leg")
     args = ap.parse_args()
     if args.steps < 1:
         ap.error("--steps must be at least 1")
-    if args.impl == "reference":
+    if args.lm_head_only:
+        import torch
+
+        import decode_step_token_gb300 as pkg
+        from workloads import device as wdev
+
+        print(json.dumps(run_lm_head(torch, pkg, wdev, "cuda:0", 0, args.ablation_seconds, K=args.hidden_dim)),
+              flush=True)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
