@@ -53,7 +53,7 @@ SUSTAINED_S = 0.5
 
 # the translation unit of the small-batch (slice) kernel and what it includes: the
 # kernel the roofline and the committed ncu counters are about
-SLICE_SOURCES = ("slice_kernel.cu", "slice_kernel.cuh", "slice_sampler.cuh", "row_sampler.cuh", "philox.cuh",
+SLICE_SOURCES = ("slice_kernel.cu", "slice_kernel_ext.cu", "slice_kernel.cuh", "slice_sampler.cuh", "row_sampler.cuh", "philox.cuh",
                  "ptx.cuh", "launch.h")
 
 

@@ -1,8 +1,8 @@
 """Build libsampler.so in-tree with nvcc for sm_103a (GB300).
 
-The library has four translation units (the C ABI's host code, the slice
-kernel, the fork-group kernel, the LM-head GEMM); they compile in parallel and
-link into one shared object.
+The library has five translation units (the C ABI's host code, the slice
+kernel and its variant with the extensions, the fork-group kernel, the LM-head
+GEMM); they compile in parallel and link into one shared object.
 """
 from __future__ import annotations
 
@@ -20,7 +20,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [*ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC"]
-UNITS = ("sampler_api.cu", "slice_kernel.cu", "group_kernel.cu", "lm_head_kernel.cu")
+UNITS = ("sampler_api.cu", "slice_kernel.cu", "slice_kernel_ext.cu", "group_kernel.cu", "lm_head_kernel.cu")
 
 
 def sources() -> list:

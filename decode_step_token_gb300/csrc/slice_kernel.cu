@@ -1,10 +1,16 @@
-// slice_kernel.cu -- instantiation, geometry and launch of the slice kernel
-// (design in slice_sampler.cuh).
+// slice_kernel.cu -- geometry and launch of the slice kernel (design in
+// slice_sampler.cuh), and its variant without the extensions of
+// sampler_sample_ex (the one with them is built in slice_kernel_ext.cu).
 #include <algorithm>
 #include <cstring>
 
 #include "launch.h"
+
+#define SLC_EXT 0
+#define SLC_VARIANT base
 #include "slice_kernel.cuh"
+#undef SLC_EXT
+#undef SLC_VARIANT
 
 namespace dst {
 
@@ -24,15 +30,20 @@ namespace {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-template <typename InT>
-void* kernel_of() { return reinterpret_cast<void*>(&slc::slice_kernel<InT>); }
+// The kernel for the logits' type, with or without the extensions.
+void* kernel_of(int dtype, bool ext)
+{
+    if (ext) return slice_ext_kernel(dtype);
+    return dtype == SAMPLER_DTYPE_BF16 ? reinterpret_cast<void*>(&slc::base::slice_kernel<uint16_t>)
+                                       : reinterpret_cast<void*>(&slc::base::slice_kernel<float>);
+}
 
 }  // namespace
 
 bool kernels_loadable()
 {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel_of<float>()) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, kernel_of(SAMPLER_DTYPE_F32, false)) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -65,9 +76,10 @@ bool slice_geometry(int64_t N, int64_t V, int esize, int sms, SliceGeometry* g)
 
 int slice_prepare(int dtype, size_t smem)
 {
-    void* fn = dtype == SAMPLER_DTYPE_BF16 ? kernel_of<uint16_t>() : kernel_of<float>();
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-        return SAMPLER_ERR_CUDA;
+    for (bool ext : {false, true})
+        if (cudaFuncSetAttribute(kernel_of(dtype, ext), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess)
+            return SAMPLER_ERR_CUDA;
     return SAMPLER_OK;
 }
 
@@ -137,7 +149,7 @@ int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGe
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    void* fn = a->dtype == SAMPLER_DTYPE_BF16 ? kernel_of<uint16_t>() : kernel_of<float>();
+    void* fn = kernel_of(a->dtype, lp != nullptr);
     void* args[] = {&p};
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;
     return SAMPLER_OK;

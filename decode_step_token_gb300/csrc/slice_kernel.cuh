@@ -4,7 +4,15 @@
 // summary, its arrival and, when it completes a row, that row's finish. The
 // only CTA-wide step is the exact path at the end, for rows the candidate
 // lists could not settle.
-#pragma once
+//
+// Included once per kernel variant: SLC_EXT 1 builds the variant that takes
+// the extensions of sampler_sample_ex (logprob outputs, vocabulary mask,
+// logit_bias, min_tokens, NaN sanitising) into namespace SLC_VARIANT; SLC_EXT 0
+// compiles their code out, which keeps the kernel text of the plain step at
+// about half the size (its finishing code runs from a cold instruction cache).
+#if !defined(SLC_EXT) || !defined(SLC_VARIANT)
+#error "define SLC_EXT (0 or 1) and SLC_VARIANT before including slice_kernel.cuh"
+#endif
 
 #include "slice_sampler.cuh"
 
@@ -18,6 +26,16 @@
 
 namespace dst {
 namespace slc {
+namespace SLC_VARIANT {
+
+// ---------------------------------------------------------------- extension switches
+// Constant false in the variant without extensions, so that their code drops out.
+__device__ __forceinline__ bool row_lp(const RowInfo& ri) { return SLC_EXT && ri.lp; }
+__device__ __forceinline__ const uint32_t* mask_of(const KernelParams& kp)
+{
+    return SLC_EXT ? kp.vocab_mask : nullptr;
+}
+__device__ __forceinline__ bool sanitizing(const KernelParams& kp) { return SLC_EXT && kp.sanitize_nan; }
 
 // ---------------------------------------------------------------- set-up
 // Every lane of the warp reads the same row (one request each, the same words).
@@ -51,7 +69,7 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     // min_tokens: the row's stop tokens are banned while it owes tokens (the
     // lists' limits are checked warp-wide by ext_lists_ok)
     ri.ban = 0;
-    if (kp.stop_offsets && kp.min_tokens_left && kp.min_tokens_left[r] > 0 &&
+    if (SLC_EXT && kp.stop_offsets && kp.min_tokens_left && kp.min_tokens_left[r] > 0 &&
         kp.stop_offsets[r + 1] > kp.stop_offsets[r])
         ri.ban = 1;
     const bool greedy = T < 1e-5f;
@@ -68,7 +86,7 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     ri.mt = uint8_t(ri.do_topk && ri.k <= kKComplete ? ri.k : ri.m);
     ri.greedy = greedy ? 1 : 0;
     const bool trunc = ri.do_topk || ri.do_topp || ri.do_minp;
-    ri.lp = (kp.out_tok_lp != nullptr || kp.top_n > 0) ? 1 : 0;
+    ri.lp = (SLC_EXT && (kp.out_tok_lp != nullptr || kp.top_n > 0)) ? 1 : 0;
     if (bad) ri.cls = kClsErr;
     else if (greedy) ri.cls = (ri.lp && trunc) ? kClsTrunc : kClsGreedy;  // outputs over the kept set at T := 1
     else if (!trunc) ri.cls = kClsPlain;
@@ -141,6 +159,23 @@ __device__ __forceinline__ int vec_find(const uint4& v, float m)
     return pos;
 }
 
+// NaN sanitising of the vectors a lane reads (the unit is staged whole): NaN
+// becomes -inf in the slot; returns the lane's new maximum.
+template <typename InT>
+__device__ __noinline__ float lane_sanitize(const SliceView<InT>& sv)
+{
+    const int lane = threadIdx.x & 31;
+    uint4* smv = const_cast<uint4*>(sv.sm);
+    typename Vec<InT>::Acc a = Vec<InT>::acc_init();
+#pragma unroll 1
+    for (int j = lane; j < sv.nvec; j += 32) {
+        const uint4 c = Vec<InT>::sanitized(smv[j]);
+        smv[j] = c;
+        Vec<InT>::acc_add(a, c);
+    }
+    return Vec<InT>::acc_max(a);
+}
+
 // Lane maximum and the flags of the part of the unit a lane reads: one packed,
 // NaN-propagating maximum per vector. A lane that met a NaN reports -inf (its
 // flags mark the row).
@@ -152,20 +187,10 @@ __device__ __forceinline__ float lane_max_val(const SliceView<InT>& sv, uint32_t
 #pragma unroll 2
     for (int j = lane; j < sv.nvec; j += 32) Vec<InT>::acc_add(a, sv.vec(j));
     float m = Vec<InT>::acc_max(a);
-    if (sv.san) {
+    if (SLC_EXT && sv.san) {
         // NaN sanitising (the unit is staged whole): a lane that met a NaN makes
         // its NaNs -inf in the slot and takes its maximum again
-        if (m != m) {
-            uint4* smv = const_cast<uint4*>(sv.sm);
-            a = Vec<InT>::acc_init();
-#pragma unroll 1
-            for (int j = lane; j < sv.nvec; j += 32) {
-                const uint4 c = Vec<InT>::sanitized(smv[j]);
-                smv[j] = c;
-                Vec<InT>::acc_add(a, c);
-            }
-            m = Vec<InT>::acc_max(a);
-        }
+        if (m != m) m = lane_sanitize<InT>(sv);
         __syncwarp();
     }
     const bool nan = m != m;
@@ -214,7 +239,7 @@ __device__ __forceinline__ void unit_max(const SliceView<InT>& sv, float& mx, in
 // them and takes the biased and banned tokens apart from the staged logits).
 __device__ __forceinline__ bool has_extras(const KernelParams& kp)
 {
-    return kp.bias_offsets != nullptr || kp.stop_offsets != nullptr;
+    return SLC_EXT && (kp.bias_offsets != nullptr || kp.stop_offsets != nullptr);
 }
 
 // Row r's logit of token v after NaN sanitising, its bias entries (one fp32
@@ -224,15 +249,15 @@ template <typename InT>
 __device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowInfo& ri, int v)
 {
     float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
-    if (kp.sanitize_nan && x != x) x = -INFINITY;
-    if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
+    if (sanitizing(kp) && x != x) x = -INFINITY;
+    if (mask_of(kp) && !((__ldg(mask_of(kp) + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
         return -INFINITY;
-    if (ri.ban) {
+    if (SLC_EXT && ri.ban) {
         const int s1 = kp.stop_offsets[ri.r + 1];
         for (int j = kp.stop_offsets[ri.r]; j < s1; ++j)
             if (kp.stop_ids[j] == v) return -INFINITY;
     }
-    if (kp.bias_offsets) {
+    if (SLC_EXT && kp.bias_offsets) {
         const int b1 = kp.bias_offsets[ri.r + 1];
         for (int j = kp.bias_offsets[ri.r]; j < b1; ++j)
             if (kp.bias_ids[j] == v) x = x + kp.bias_values[j];
@@ -281,8 +306,8 @@ __device__ __noinline__ int row_extras(const KernelParams& kp, const RowInfo& ri
     for (int k = 0; k < K; ++k) {
         const bool in = id[k] >= lo && id[k] < hi;
         x[k] = in ? ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + id[k]) : 0.0f;
-        ok[k] = !in || !kp.vocab_mask ||
-                ((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (id[k] >> 5)) >> (id[k] & 31)) & 1u);
+        ok[k] = !in || !mask_of(kp) ||
+                ((__ldg(mask_of(kp) + size_t(ri.r) * size_t(kp.mask_stride) + (id[k] >> 5)) >> (id[k] & 31)) & 1u);
     }
     // the tokens in range, each at its first entry, in list order
     int cnt = 0;
@@ -306,7 +331,7 @@ __device__ __noinline__ int row_extras(const KernelParams& kp, const RowInfo& ri
             // the token's value: its logit plus its bias entries in list order;
             // -inf when a stop-token entry bans it or its mask bit is clear
             float acc = __shfl_sync(0xffffffffu, x[k], src);
-            if (kp.sanitize_nan && acc != acc) acc = -INFINITY;
+            if (sanitizing(kp) && acc != acc) acc = -INFINITY;
             bool banned = !__shfl_sync(0xffffffffu, ok[k], src);
 #pragma unroll
             for (int kk = 0; kk < K; ++kk) {
@@ -1080,7 +1105,7 @@ static __device__ __noinline__ bool cut_and_pick(const SliceParams& P, const Row
     }
     if (lane == 0) write_out(P.k, r, token, kRowOk);
     tok_out = token;
-    if (ri.lp && !P.k.lp_unscaled) {
+    if (row_lp(ri) && !P.k.lp_unscaled) {
         // the kept set's mass at the outputs' temperature, and the token's logit
         double z = 0.0;
         float xt = 0.0f;
@@ -1168,10 +1193,10 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
                     v[u] = __ldg(reinterpret_cast<const uint4*>(g) + j);
                 else
                     v[u] = load_vec_slow<InT>(g, j, n);
-                if (P.k.sanitize_nan) v[u] = Vec<InT>::sanitized(v[u]);
-                if (P.k.vocab_mask) {
+                if (sanitizing(P.k)) v[u] = Vec<InT>::sanitized(v[u]);
+                if (mask_of(P.k)) {
                     const int tk = c0 + j * E;
-                    const uint32_t w = __ldg(P.k.vocab_mask + size_t(ri.r) * size_t(P.k.mask_stride) + (tk >> 5));
+                    const uint32_t w = __ldg(mask_of(P.k) + size_t(ri.r) * size_t(P.k.mask_stride) + (tk >> 5));
                     v[u] = Vec<InT>::masked(v[u], (w >> (tk & 31)) & ((1u << E) - 1u));
                 }
             }
@@ -1279,7 +1304,7 @@ static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScrat
     tok = -1;
     if (st) {
         if (lane == 0) write_out(P.k, r, -1, st);
-        if (ri.lp) lp_write_error(P.k, r);
+        if (row_lp(ri)) lp_write_error(P.k, r);
         return true;
     }
     // the min-p threshold on the logit: m + T ln(min_p), rounded up to fp32
@@ -1516,8 +1541,8 @@ template <typename InT>
 __device__ __forceinline__ float row_x(const KernelParams& kp, const RowInfo& ri, int v, const SliceShared& sh)
 {
     float x = ElemTraits<InT>::load(kp.logits, int64_t(ri.lrow) * kp.row_stride + v);
-    if (kp.sanitize_nan && x != x) x = -INFINITY;
-    if (kp.vocab_mask && !((__ldg(kp.vocab_mask + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
+    if (sanitizing(kp) && x != x) x = -INFINITY;
+    if (mask_of(kp) && !((__ldg(mask_of(kp) + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
         return -INFINITY;
     if (sh.bx_n && ((sh.bx_bits[v >> 5] >> (v & 31)) & 1u))
         for (int q = 0; q < sh.bx_n; ++q)
@@ -1659,7 +1684,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
     }
     // the pick (greedy rows: the maximum, lowest index) and the kept set's mass
     // and size at the outputs' temperature (logprob outputs over the kept set)
-    const bool lp_kept = ri.lp && !kp.lp_unscaled && ri.cls == kClsTrunc;
+    const bool lp_kept = row_lp(ri) && !kp.lp_unscaled && ri.cls == kClsTrunc;
     const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
     K2 t{0ull, 0ull};
     double z = 0.0;
@@ -1668,7 +1693,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
         const float x = row_x<InT>(kp, ri, v, sh);
         if (!(x > -INFINITY)) continue;
         const bool kept = !(hb && !in_prefix(f2key(x), v, bk, bi)) && !(ri.do_minp && !(x >= xthr));
-        if (ri.lp && (kept || !lp_kept)) {
+        if (row_lp(ri) && (kept || !lp_kept)) {
             z += double(exp2f((x - m) * ri.s2o));
             ++nk;
         }
@@ -1681,7 +1706,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
         sh.red_k[2 * wid] = t.a;
         sh.red_k[2 * wid + 1] = t.b;
     }
-    if (ri.lp) {
+    if (row_lp(ri)) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
         nk = __reduce_add_sync(0xffffffffu, nk);
@@ -1706,7 +1731,7 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
         }
     }
     __syncthreads();
-    if (!ri.lp) return;
+    if (!row_lp(ri)) return;
     // logprob outputs: the first n of the kept set (or of the row) in (value desc,
     // index asc) order, from the n-th of that order; the kept set is a prefix of it
     double zt = 0.0;
@@ -1752,6 +1777,50 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
 }
 
 // ---------------------------------------------------------------- one unit
+// A unit with an extension, once its copy has landed: staged whole (the vectors
+// the bulk copy left out, a ragged tail or an unaligned slice, are loaded into
+// the slot, which holds the whole unit), then rewritten in place: the mask
+// (mws: the unit's mask words, word 0 holding token c0) turns disallowed tokens
+// to -inf, and so do the nx biased and banned tokens xi (their values are taken
+// apart). Out of line: the step without extensions keeps its code compact.
+template <typename InT>
+__device__ __noinline__ void stage_extensions(SliceView<InT>& sv, bool masked, const uint32_t* mws,
+                                              const int32_t* xi, int nx)
+{
+    constexpr int E = Vec<InT>::E;
+    const int lane = threadIdx.x & 31;
+    const int c0 = sv.c0;
+    uint4* smv = const_cast<uint4*>(sv.sm);
+    if (sv.nb < sv.nvec) {
+        for (int j = sv.nb + lane; j < sv.nvec; j += 32) smv[j] = sv.vec(j);
+        sv.nb = sv.nvec;
+    }
+    __syncwarp();
+    if (masked) {
+#pragma unroll 4
+        for (int j = lane; j < sv.nb; j += 32) {
+            const int t = j * E + (c0 & 31);
+            const uint32_t bits = (mws[t >> 5] >> (t & 31)) & ((1u << E) - 1u);
+            if (bits != (1u << E) - 1u) smv[j] = Vec<InT>::masked(smv[j], bits);
+        }
+        __syncwarp();
+    }
+    if (nx) {
+        uint32_t* smw = reinterpret_cast<uint32_t*>(smv);
+        for (int i = lane; i < nx; i += 32) {
+            const int o = xi[i] - c0;
+            if (sizeof(InT) == 2) {
+                const int sh = 16 * (o & 1);
+                atomicOr(&smw[o >> 1], 0xFF80u << sh);
+                atomicAnd(&smw[o >> 1], ~(0x007Fu << sh));
+            } else {
+                smw[o] = 0xFF800000u;
+            }
+        }
+        __syncwarp();
+    }
+}
+
 // Wait for the warp's slot, summarise the unit into its record (row r, slice s).
 // Returns false, with nothing recorded, when the row's parameters are bad.
 template <typename InT>
@@ -1773,8 +1842,8 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
     uint32_t* mws = reinterpret_cast<uint32_t*>(q);
     if (ri.cls != kClsErr) {
         if (has_extras(kp)) nx = row_extras<InT>(kp, ri, c0, c0 + n_el, xi, xv);
-        if (kp.vocab_mask && nx >= 0) {
-            const uint32_t* mrow = kp.vocab_mask + size_t(r) * size_t(kp.mask_stride) + (c0 >> 5);
+        if (mask_of(kp) && nx >= 0) {
+            const uint32_t* mrow = mask_of(kp) + size_t(r) * size_t(kp.mask_stride) + (c0 >> 5);
             const int nw = ((c0 + n_el - 1) >> 5) - (c0 >> 5) + 1;
             uint32_t w[kMaskWords / 32];
 #pragma unroll
@@ -1805,36 +1874,9 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
     // slice) are loaded into the slot too (it holds the whole unit). NaN
     // sanitising is left to the first lane-maximum pass (a lane that meets a
     // NaN cleans its vectors).
-    const bool has_x = !extra && (kp.sanitize_nan || kp.vocab_mask || nx > 0);
-    uint4* smv = reinterpret_cast<uint4*>(const_cast<unsigned char*>(slot));
-    if (has_x && sv.nb < sv.nvec) {
-        for (int j = sv.nb + lane; j < sv.nvec; j += 32) smv[j] = sv.vec(j);
-        sv.nb = sv.nvec;
-    }
-    __syncwarp();
-    sv.san = has_x && kp.sanitize_nan;
-    if (has_x && kp.vocab_mask) {  // the row's vocabulary mask
-#pragma unroll 4
-        for (int j = lane; j < sv.nb; j += 32) {
-            const int t = j * E + (c0 & 31);
-            const uint32_t bits = (mws[t >> 5] >> (t & 31)) & ((1u << E) - 1u);
-            if (bits != (1u << E) - 1u) smv[j] = Vec<InT>::masked(smv[j], bits);
-        }
-        __syncwarp();
-    }
-    if (has_x && nx) {  // the biased and banned tokens read as -inf in the slot
-        uint32_t* smw = reinterpret_cast<uint32_t*>(smv);
-        for (int i = lane; i < nx; i += 32) {
-            const int o = xi[i] - c0;
-            if (sizeof(InT) == 2) {
-                const int sh = 16 * (o & 1);
-                atomicOr(&smw[o >> 1], 0xFF80u << sh);
-                atomicAnd(&smw[o >> 1], ~(0x007Fu << sh));
-            } else {
-                smw[o] = 0xFF800000u;
-            }
-        }
-        __syncwarp();
+    if (!extra && (sanitizing(kp) || mask_of(kp) || nx > 0)) {
+        stage_extensions<InT>(sv, mask_of(kp) != nullptr, mws, xi, nx);
+        sv.san = sanitizing(kp);
     }
     SliceHdr hdr;
     hdr.mx = -INFINITY;
@@ -1851,7 +1893,7 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
                 hdr.flags |= extras_flags(xv, nx);
                 extras_max(xi, xv, nx, hdr.mx, hdr.amax);
             }
-            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
+            if (row_lp(ri)) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         } else if (ri.cls == kClsPlain) {
             unit_plain<InT>(sv, ri, off_lo, off_hi, q, qw, g, hdr.flags);
             if (nx) {  // the biased tokens, scored exactly
@@ -1866,7 +1908,7 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
                 if (t.b) k2_insert(g, t.b);
             }
             __syncwarp();
-            if (ri.lp) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
+            if (row_lp(ri)) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         } else {
             unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         }
@@ -1900,7 +1942,7 @@ __device__ __noinline__ bool finish_row(const SliceParams& P, WarpScratch& ws, c
         return false;
     }
     // outputs over the whole row (untruncated rows; every row when unscaled)
-    if (ri.lp && (P.k.lp_unscaled || ri.cls != kClsTrunc)) {
+    if (row_lp(ri) && (P.k.lp_unscaled || ri.cls != kClsTrunc)) {
         __syncwarp();
         return finish_lp_row<InT>(P, ws, ri, r, tok, st, scratch, m);
     }
@@ -2032,5 +2074,6 @@ __global__ void __launch_bounds__(kT, 1) slice_kernel(const __grid_constant__ Sl
     }
 }
 
+}  // namespace SLC_VARIANT
 }  // namespace slc
 }  // namespace dst
