@@ -106,7 +106,7 @@ int group_occupancy(int dtype, bool pen, const GroupGeometry& g)
     return nc;
 }
 
-int group_launch(const sampler_args_t* a, const GroupGeometry& gg, int clusters, cudaStream_t stream)
+int group_launch(const sampler_args_t* a, const GroupGeometry& gg, int clusters, uint32_t* work, cudaStream_t stream)
 {
     const bool pen = a->hist_offsets != nullptr;
     grp::GroupParams p;
@@ -148,6 +148,7 @@ int group_launch(const sampler_args_t* a, const GroupGeometry& gg, int clusters,
     p.off_cand = gg.off_cand;
     p.off_cnt = gg.off_cnt;
     p.off_stage = gg.off_stage;
+    p.work = work;
 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];

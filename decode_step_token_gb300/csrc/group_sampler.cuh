@@ -68,6 +68,8 @@ struct GroupParams {
     uint32_t off_cand;
     uint32_t off_cnt;
     uint32_t off_stage;
+    uint32_t* work;     // [2] chunks handed out past the first one per cluster, clusters done;
+                        // zero between launches (the last cluster to finish clears them)
 };
 
 struct alignas(8) ForkOut {  // leader's result for one fork, copied to every CTA
@@ -118,6 +120,7 @@ struct alignas(8) SelState {  // exact path: radix select state
 
 struct alignas(16) GShared {
     uint64_t mbar[kChunks];
+    int32_t next_chunk[2]; // the cluster's next chunk, by iteration parity (written by the leader)
     uint32_t phase;        // parity of the next wait on mbar[]
     int32_t n_forks;
     int32_t r0;

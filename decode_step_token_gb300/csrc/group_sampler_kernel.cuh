@@ -957,7 +957,14 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
     uint32_t stuck_bits = 0;  // barriers whose copies never completed (the CTA stops copying)
     __syncthreads();
 
-    for (int chunk = int(cluster_id_x()); chunk < P.n_chunks; chunk += ncl) {
+    // Chunks of output rows: a cluster's first one is its index; it claims each
+    // next one from the work counter while it serves the current one (at the
+    // end of the chunk's first group, when every CTA of the cluster is known to
+    // run), so that clusters whose groups run long take fewer chunks. The claim
+    // reaches every CTA through the cluster barrier that closes the group.
+    int chunk = int(cluster_id_x());
+    for (int it = 0; chunk < P.n_chunks; ++it) {
+        bool claimed = false;
         const int cr0 = chunk * P.chunk, cr1 = min(P.n_rows, cr0 + P.chunk);
         for (int r0 = cr0; r0 < cr1;) {
             // ---- set-up (warp 0): the group, its bulk copies, its forks' parameters
@@ -1555,9 +1562,25 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
                 K.out_tokens[r0 + tid] = sh.bc.f[tid].token;
                 if (K.out_status) K.out_status[r0 + tid] = sh.bc.f[tid].status;
             }
+            if (!claimed && rank == 0 && tid == 0) {
+                const int nx = ncl + int(atomicAdd(P.work, 1u));
+                for (uint32_t c = 0; c < C; ++c)
+                    dsmem_st_u32(dsmem_map(smem_addr(&sh.next_chunk[it & 1]), c), uint32_t(nx));
+            }
+            claimed = true;
             __syncthreads();
             cluster_sync();
             r0 += g;
+        }
+        chunk = sh.next_chunk[it & 1];
+    }
+    // the last cluster out clears the work counter for the next launch (every
+    // cluster's claims come before its count)
+    if (rank == 0 && tid == 0) {
+        __threadfence();
+        if (atomicAdd(P.work + 1, 1u) == uint32_t(ncl - 1)) {
+            atomicExch(P.work, 0u);
+            atomicExch(P.work + 1, 0u);
         }
     }
     // copies that gave up: wait (bounded) for them to land before the CTA exits

@@ -99,6 +99,7 @@ int group_occupancy(int dtype, bool pen, const GroupGeometry& g);
 
 int group_prepare(int dtype, bool pen, size_t smem);
 
-int group_launch(const sampler_args_t* a, const GroupGeometry& g, int clusters, cudaStream_t stream);
+// work: two zeroed counters of the handle (the kernel leaves them zeroed)
+int group_launch(const sampler_args_t* a, const GroupGeometry& g, int clusters, uint32_t* work, cudaStream_t stream);
 
 }  // namespace dst

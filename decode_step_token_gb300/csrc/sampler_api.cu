@@ -52,6 +52,7 @@ struct sampler_s {
     size_t lmh_smem_set;     // LM-head GEMM
     size_t grp_occ_smem[4];  // shared memory of the cached cluster occupancy below
     int grp_occ[4];          // co-resident clusters of the fork-group kernel
+    uint32_t* grp_work;      // the fork-group kernel's chunk counters (zero between launches)
     unsigned long long* stats;  // device counters (diagnostics)
     // staging for sampler_sample_host
     unsigned char* stage_base;
@@ -83,7 +84,7 @@ int launch_group(sampler_t h, const sampler_args_t* a, cudaStream_t stream)
         h->grp_occ[slot] = nc;
         h->grp_occ_smem[slot] = gg.smem;
     }
-    return dst::group_launch(a, gg, h->grp_occ[slot], stream);
+    return dst::group_launch(a, gg, h->grp_occ[slot], h->grp_work, stream);
 }
 
 // lp: the step's extensions, offered on the slice kernel only (the caller has
@@ -134,6 +135,7 @@ void free_handle(sampler_s* h)
     cudaFree(h->slice_ws.body);
     cudaFree(h->slice_ws.cnt);
     cudaFree(h->stats);
+    cudaFree(h->grp_work);
     cudaFree(h->stage_base);
     delete h;
 }
@@ -280,6 +282,8 @@ int sampler_create(sampler_t* out, const sampler_config_t* cfg)
             cudaMemset(h->slice_ws.cnt, 0, cnt_bytes) != cudaSuccess ||
             cudaMalloc(&h->stats, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
             cudaMemset(h->stats, 0, kNumStats * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaMalloc(&h->grp_work, 2 * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(h->grp_work, 0, 2 * sizeof(uint32_t)) != cudaSuccess ||
             cudaDeviceSynchronize() != cudaSuccess) {
             free_handle(h);
             return SAMPLER_ERR_CUDA;
