@@ -47,13 +47,14 @@ bool kernels_loadable();
 // slice kernel does not take the shape.
 bool slice_geometry(int64_t n_rows, int64_t vocab, int esize, int sms, SliceGeometry* g);
 
-// Grant the kernel (both variants) its dynamic shared memory (once per device
+// Grant the kernel (every variant) its dynamic shared memory (once per device
 // and size).
 int slice_prepare(int dtype, size_t smem);
 
-// The slice kernel's variant with the extensions of sampler_sample_ex, for the
-// logits' type (built in slice_kernel_ext.cu).
-void* slice_ext_kernel(int dtype);
+// The slice kernel's variants with the extensions of sampler_sample_ex, for the
+// logits' type: the filters alone, or (lp) everything (built in
+// slice_kernel_ext.cu).
+void* slice_ext_kernel(int dtype, bool lp);
 
 // Enqueue one slice-kernel launch. max_polls bounds each wait on a staging copy.
 // ext: the step's extensions (NULL: none). pdl: launched as the programmatic

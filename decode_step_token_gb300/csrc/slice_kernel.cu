@@ -1,15 +1,17 @@
 // slice_kernel.cu -- geometry and launch of the slice kernel (design in
 // slice_sampler.cuh), and its variant without the extensions of
-// sampler_sample_ex (the one with them is built in slice_kernel_ext.cu).
+// sampler_sample_ex (the others are built in slice_kernel_ext.cu).
 #include <algorithm>
 #include <cstring>
 
 #include "launch.h"
 
-#define SLC_EXT 0
+#define SLC_FILTERS 0
+#define SLC_LP 0
 #define SLC_VARIANT base
 #include "slice_kernel.cuh"
-#undef SLC_EXT
+#undef SLC_FILTERS
+#undef SLC_LP
 #undef SLC_VARIANT
 
 namespace dst {
@@ -30,10 +32,11 @@ namespace {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// The kernel for the logits' type, with or without the extensions.
-void* kernel_of(int dtype, bool ext)
+// The kernel for the logits' type and the extensions a call asks for (0: none,
+// 1: filters only, 2: logprob outputs, with or without filters).
+void* kernel_of(int dtype, int variant)
 {
-    if (ext) return slice_ext_kernel(dtype);
+    if (variant) return slice_ext_kernel(dtype, variant == 2);
     return dtype == SAMPLER_DTYPE_BF16 ? reinterpret_cast<void*>(&slc::base::slice_kernel<uint16_t>)
                                        : reinterpret_cast<void*>(&slc::base::slice_kernel<float>);
 }
@@ -43,7 +46,7 @@ void* kernel_of(int dtype, bool ext)
 bool kernels_loadable()
 {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel_of(SAMPLER_DTYPE_F32, false)) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, kernel_of(SAMPLER_DTYPE_F32, 0)) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -76,9 +79,9 @@ bool slice_geometry(int64_t N, int64_t V, int esize, int sms, SliceGeometry* g)
 
 int slice_prepare(int dtype, size_t smem)
 {
-    for (bool ext : {false, true})
-        if (cudaFuncSetAttribute(kernel_of(dtype, ext), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
+    for (int variant = 0; variant < 3; ++variant)
+        if (cudaFuncSetAttribute(kernel_of(dtype, variant), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem)) != cudaSuccess)
             return SAMPLER_ERR_CUDA;
     return SAMPLER_OK;
 }
@@ -149,7 +152,8 @@ int slice_launch(const sampler_args_t* a, const sampler_ext_t* lp, const SliceGe
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    void* fn = kernel_of(a->dtype, lp != nullptr);
+    const int variant = !lp ? 0 : (lp->out_token_logprob || lp->top_n > 0) ? 2 : 1;
+    void* fn = kernel_of(a->dtype, variant);
     void* args[] = {&p};
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SAMPLER_ERR_CUDA;
     return SAMPLER_OK;

@@ -5,13 +5,14 @@
 // only CTA-wide step is the exact path at the end, for rows the candidate
 // lists could not settle.
 //
-// Included once per kernel variant: SLC_EXT 1 builds the variant that takes
-// the extensions of sampler_sample_ex (logprob outputs, vocabulary mask,
-// logit_bias, min_tokens, NaN sanitising) into namespace SLC_VARIANT; SLC_EXT 0
-// compiles their code out, which keeps the kernel text of the plain step at
-// about half the size (its finishing code runs from a cold instruction cache).
-#if !defined(SLC_EXT) || !defined(SLC_VARIANT)
-#error "define SLC_EXT (0 or 1) and SLC_VARIANT before including slice_kernel.cuh"
+// Included once per kernel variant, into namespace SLC_VARIANT: SLC_FILTERS 1
+// takes the filters of sampler_sample_ex (vocabulary mask, logit_bias,
+// min_tokens, NaN sanitising), SLC_LP 1 its logprob outputs; 0 compiles that
+// code out. The plain step's variant (both 0) has about half the kernel text of
+// the one with everything (its finishing code runs from a cold instruction
+// cache, so the text it walks through is what it pays for).
+#if !defined(SLC_FILTERS) || !defined(SLC_LP) || !defined(SLC_VARIANT)
+#error "define SLC_FILTERS, SLC_LP (0 or 1) and SLC_VARIANT before including slice_kernel.cuh"
 #endif
 
 #include "slice_sampler.cuh"
@@ -29,13 +30,13 @@ namespace slc {
 namespace SLC_VARIANT {
 
 // ---------------------------------------------------------------- extension switches
-// Constant false in the variant without extensions, so that their code drops out.
-__device__ __forceinline__ bool row_lp(const RowInfo& ri) { return SLC_EXT && ri.lp; }
+// Constant false in the variants without them, so that their code drops out.
+__device__ __forceinline__ bool row_lp(const RowInfo& ri) { return SLC_LP && ri.lp; }
 __device__ __forceinline__ const uint32_t* mask_of(const KernelParams& kp)
 {
-    return SLC_EXT ? kp.vocab_mask : nullptr;
+    return SLC_FILTERS ? kp.vocab_mask : nullptr;
 }
-__device__ __forceinline__ bool sanitizing(const KernelParams& kp) { return SLC_EXT && kp.sanitize_nan; }
+__device__ __forceinline__ bool sanitizing(const KernelParams& kp) { return SLC_FILTERS && kp.sanitize_nan; }
 
 // ---------------------------------------------------------------- set-up
 // Every lane of the warp reads the same row (one request each, the same words).
@@ -69,7 +70,7 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     // min_tokens: the row's stop tokens are banned while it owes tokens (the
     // lists' limits are checked warp-wide by ext_lists_ok)
     ri.ban = 0;
-    if (SLC_EXT && kp.stop_offsets && kp.min_tokens_left && kp.min_tokens_left[r] > 0 &&
+    if (SLC_FILTERS && kp.stop_offsets && kp.min_tokens_left && kp.min_tokens_left[r] > 0 &&
         kp.stop_offsets[r + 1] > kp.stop_offsets[r])
         ri.ban = 1;
     const bool greedy = T < 1e-5f;
@@ -86,7 +87,7 @@ __device__ __forceinline__ RowInfo load_info(const SliceParams& P, int r)
     ri.mt = uint8_t(ri.do_topk && ri.k <= kKComplete ? ri.k : ri.m);
     ri.greedy = greedy ? 1 : 0;
     const bool trunc = ri.do_topk || ri.do_topp || ri.do_minp;
-    ri.lp = (SLC_EXT && (kp.out_tok_lp != nullptr || kp.top_n > 0)) ? 1 : 0;
+    ri.lp = (SLC_LP && (kp.out_tok_lp != nullptr || kp.top_n > 0)) ? 1 : 0;
     if (bad) ri.cls = kClsErr;
     else if (greedy) ri.cls = (ri.lp && trunc) ? kClsTrunc : kClsGreedy;  // outputs over the kept set at T := 1
     else if (!trunc) ri.cls = kClsPlain;
@@ -187,7 +188,7 @@ __device__ __forceinline__ float lane_max_val(const SliceView<InT>& sv, uint32_t
 #pragma unroll 2
     for (int j = lane; j < sv.nvec; j += 32) Vec<InT>::acc_add(a, sv.vec(j));
     float m = Vec<InT>::acc_max(a);
-    if (SLC_EXT && sv.san) {
+    if (SLC_FILTERS && sv.san) {
         // NaN sanitising (the unit is staged whole): a lane that met a NaN makes
         // its NaNs -inf in the slot and takes its maximum again
         if (m != m) m = lane_sanitize<InT>(sv);
@@ -239,7 +240,7 @@ __device__ __forceinline__ void unit_max(const SliceView<InT>& sv, float& mx, in
 // them and takes the biased and banned tokens apart from the staged logits).
 __device__ __forceinline__ bool has_extras(const KernelParams& kp)
 {
-    return SLC_EXT && (kp.bias_offsets != nullptr || kp.stop_offsets != nullptr);
+    return SLC_FILTERS && (kp.bias_offsets != nullptr || kp.stop_offsets != nullptr);
 }
 
 // Row r's logit of token v after NaN sanitising, its bias entries (one fp32
@@ -252,12 +253,12 @@ __device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowI
     if (sanitizing(kp) && x != x) x = -INFINITY;
     if (mask_of(kp) && !((__ldg(mask_of(kp) + size_t(ri.r) * size_t(kp.mask_stride) + (v >> 5)) >> (v & 31)) & 1u))
         return -INFINITY;
-    if (SLC_EXT && ri.ban) {
+    if (SLC_FILTERS && ri.ban) {
         const int s1 = kp.stop_offsets[ri.r + 1];
         for (int j = kp.stop_offsets[ri.r]; j < s1; ++j)
             if (kp.stop_ids[j] == v) return -INFINITY;
     }
-    if (SLC_EXT && kp.bias_offsets) {
+    if (SLC_FILTERS && kp.bias_offsets) {
         const int b1 = kp.bias_offsets[ri.r + 1];
         for (int j = kp.bias_offsets[ri.r]; j < b1; ++j)
             if (kp.bias_ids[j] == v) x = x + kp.bias_values[j];
