@@ -842,13 +842,19 @@ __device__ __forceinline__ void count3_key(uint32_t key, uint32_t c1, uint32_t c
 
 // B for a top-k row: the 16-bit prefix of the k-th largest sketch key over the
 // row (the row holds at least k). sk: kSketch words per slice, meta[b].w of
-// them valid; each lane holds the keys of its slices in registers.
-static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k)
+// them valid. Each lane keeps the 16-bit prefixes of its NS slices' keys two
+// to a register (NS = the fewest that cover G slices, so that no lane counts
+// empty slots) and counts them with paired 16-bit compares, two prefix bits a
+// round: few instructions, since the finishing warp shares its scheduler with
+// units still running.
+template <int NS>
+__device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uint4* meta, int G, int k)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t key[kSPL * kSketch];
+    constexpr int kPairs = kSketch / 2;
+    uint32_t pk[NS][kPairs];
 #pragma unroll
-    for (int i = 0; i < kSPL; ++i) {
+    for (int i = 0; i < NS; ++i) {
         const int b = lane + 32 * i;
         uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
         uint32_t mb = 0;
@@ -859,16 +865,42 @@ static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, const u
         }
         const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-        for (int q = 0; q < kSketch; ++q) key[i * kSketch + q] = uint32_t(q) < mb ? w[q] : 0u;
+        for (int q = 0; q < kPairs; ++q) {
+            const uint32_t a = uint32_t(2 * q) < mb ? w[2 * q] >> 16 : 0u;
+            const uint32_t c = uint32_t(2 * q + 1) < mb ? w[2 * q + 1] >> 16 : 0u;
+            pk[i][q] = a | (c << 16);
+        }
     }
-    return kth_prefix(uint32_t(k), [&](uint32_t c1, uint32_t c2, uint32_t c3, uint32_t(&n)[3]) {
-        // four independent partial counts per threshold (short dependency chains)
-        uint32_t part[4][3] = {};
+    uint32_t p = 0;
+#pragma unroll 1
+    for (int sh = 14; sh >= 0; sh -= 2) {
+        uint32_t n[3];
 #pragma unroll
-        for (int q = 0; q < kSPL * kSketch; ++q) count3_key(key[q], c1, c2, c3, part[q & 3]);
+        for (int j = 0; j < 3; ++j) {
+            // both halves of the threshold hold the candidate prefix (>= 1, so
+            // empty slots, prefix 0, never count)
+            const uint32_t t = (p | (uint32_t(j + 1) << sh)) * 0x00010001u;
+            uint32_t a = 0;  // two 16-bit counts (at most NS * kSketch / 2 each)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) n[j] = part[0][j] + part[1][j] + part[2][j] + part[3][j];
-    });
+            for (int i = 0; i < NS; ++i)
+#pragma unroll
+                for (int q = 0; q < kPairs; ++q) a += __vsetgeu2(pk[i][q], t);
+            n[j] = (a & 0xFFFFu) + (a >> 16);
+        }
+        const uint32_t n1 = __reduce_add_sync(0xffffffffu, n[0]);
+        const uint32_t n2 = __reduce_add_sync(0xffffffffu, n[1]);
+        const uint32_t n3 = __reduce_add_sync(0xffffffffu, n[2]);
+        p |= (n3 >= uint32_t(k) ? 3u : n2 >= uint32_t(k) ? 2u : n1 >= uint32_t(k) ? 1u : 0u) << sh;
+    }
+    return p << 16;
+}
+
+static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k)
+{
+    if (G <= 32) return sketch_bound_n<1>(sk, meta, G, k);
+    if (G <= 64) return sketch_bound_n<2>(sk, meta, G, k);
+    if (G <= 96) return sketch_bound_n<3>(sk, meta, G, k);
+    return sketch_bound_n<kSPL>(sk, meta, G, k);
 }
 
 // Keep, stably and at the front, the words whose key reaches lo; returns how
