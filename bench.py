@@ -51,17 +51,29 @@ KERNEL_DIR = os.path.join(ROOT, "decode_step_token_gb300", "csrc")
 SUSTAINED_S = 0.5
 
 
-# the device code of the small-batch (slice) kernel: the kernel the roofline and
-# the committed ncu counters are about (the host-side headers it also includes
-# declare other kernels' entry points too)
-SLICE_SOURCES = ("slice_kernel.cu", "slice_kernel_ext.cu", "slice_kernel.cuh", "slice_sampler.cuh",
-                 "row_sampler.cuh", "philox.cuh", "ptx.cuh")
+# the device code of the kernel a workload runs: the kernel the roofline and the
+# committed ncu counters are about (the host-side headers the kernels also
+# include declare other kernels' entry points too)
+KERNEL_SOURCES = {
+    "slice": ("slice_kernel.cu", "slice_kernel_ext.cu", "slice_kernel.cuh", "slice_sampler.cuh",
+              "row_sampler.cuh", "philox.cuh", "ptx.cuh"),
+    "group": ("group_kernel.cu", "group_sampler.cuh", "group_sampler_kernel.cuh", "row_sampler.cuh",
+              "philox.cuh", "ptx.cuh"),
+}
 
 
-def kernel_hash() -> str:
-    """Hash of the slice kernel's device sources."""
+def kernel_kind(batch) -> str:
+    """Which kernel the library runs a batch on: the small-batch (slice) kernel for
+    at most 256 rows without history or materialised outputs, else the fork-group
+    kernel."""
+    slice_ok = batch.n_rows <= 256 and batch.hist_offsets is None and not batch.want_probs
+    return "slice" if slice_ok else "group"
+
+
+def kernel_hash(kind: str = "slice") -> str:
+    """Hash of the device sources of one kernel."""
     h = hashlib.sha256()
-    for f in SLICE_SOURCES:
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(KERNEL_DIR, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -93,13 +105,13 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(workload: str):
+def traffic_record(workload: str, kind: str = "slice"):
     """dram bytes per launch of the sampling kernel, from the committed ncu summaries
     (profiles/*.md lines `kernel_hash: ...`, `workload: ...` and
     `dram_bytes_per_launch: ...`), if one was taken on this workload with the
     kernels as they are now."""
     pdir = os.path.join(ROOT, "profiles")
-    want = kernel_hash()
+    want = kernel_hash(kind)
     try:
         names = sorted(os.listdir(pdir))
     except OSError:
@@ -627,7 +639,7 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (ms_step / 1e3) / 1e9
-    tr = traffic_record(batch.name)
+    tr = traffic_record(batch.name, kernel_kind(batch))
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": tr["dram_bytes_per_launch"] if tr else None,
             "traffic_source": (f"ncu capture summarised in profiles/{tr['source']} (same kernel "
@@ -675,7 +687,7 @@ def run_ours(args):
         "logprob_outputs": lpo,
         "extensions": ext,
         "lm_head": lmh,
-        "kernel_hash": kernel_hash(),
+        "kernel_hash": kernel_hash(kernel_kind(batch)),
         "first_tokens": tokens[:8].tolist(),
     }
     print(json.dumps(line), flush=True)
