@@ -24,6 +24,9 @@
 #define SLC_TAG(v)
 #define SLC_UCLS(v)
 #endif
+#ifndef SLC_FIN_INLINE
+#define SLC_FIN_INLINE __forceinline__
+#endif
 
 namespace dst {
 namespace slc {
@@ -640,8 +643,9 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
         const int at = nq + __popc(bal & ((1u << lane) - 1u));
         if (hit && at < kTQCap) q[at] = (uint32_t(j) << 8) | hit;
         nq += __popc(bal);
-        total += __reduce_add_sync(0xffffffffu, uint32_t(__popc(hit)));
+        total += uint32_t(__popc(hit));
     }
+    total = __reduce_add_sync(0xffffffffu, total);
     SLC_MARK(18);
     uint32_t xcount = 0;  // biased tokens that reach tau, listed after the others
     for (int q0 = 0; q0 < nx; q0 += 32) {
@@ -844,15 +848,18 @@ __device__ __forceinline__ void count3_key(uint32_t key, uint32_t c1, uint32_t c
 // row (the row holds at least k). sk: kSketch words per slice, meta[b].w of
 // them valid. Each lane keeps the 16-bit prefixes of its NS slices' keys two
 // to a register (NS = the fewest that cover G slices, so that no lane counts
-// empty slots) and counts them with paired 16-bit compares, two prefix bits a
-// round: few instructions, since the finishing warp shares its scheduler with
-// units still running.
+// empty slots) and counts them with paired 16-bit compares. The answer lies
+// between the smallest and the largest valid prefix (at least k keys reach the
+// smallest), so the search keeps lo (at least k keys reach it) and hi (fewer
+// do) from those two and cuts the range in four each round: few rounds, since
+// the keys of one row span a narrow range of prefixes.
 template <int NS>
 __device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uint4* meta, int G, int k)
 {
     const int lane = threadIdx.x & 31;
     constexpr int kPairs = kSketch / 2;
     uint32_t pk[NS][kPairs];
+    uint32_t pmin = 0xFFFFu, pmax = 0u;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
         const int b = lane + 32 * i;
@@ -870,32 +877,50 @@ __device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uin
             const uint32_t c = uint32_t(2 * q + 1) < mb ? w[2 * q + 1] >> 16 : 0u;
             pk[i][q] = a | (c << 16);
         }
+        // the sketch is in descending order: its first key is the largest, its
+        // last valid one the smallest
+        if (mb) {
+            pmax = max(pmax, w[0] >> 16);
+            pmin = min(pmin, w[min(mb, uint32_t(kSketch)) - 1u] >> 16);
+        }
     }
-    uint32_t p = 0;
+    uint32_t lo = __reduce_min_sync(0xffffffffu, pmin);
+    uint32_t hi = __reduce_max_sync(0xffffffffu, pmax) + 1u;
 #pragma unroll 1
-    for (int sh = 14; sh >= 0; sh -= 2) {
-        uint32_t n[3];
+    while (hi - lo > 1u) {
+        const uint32_t d = hi - lo - 1u;
+        uint32_t t[3], n[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) t[j] = lo + 1u + (d * uint32_t(j + 1)) / 4u;  // in (lo, hi)
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             // both halves of the threshold hold the candidate prefix (>= 1, so
             // empty slots, prefix 0, never count)
-            const uint32_t t = (p | (uint32_t(j + 1) << sh)) * 0x00010001u;
+            const uint32_t tt = t[j] * 0x00010001u;
             uint32_t a = 0;  // two 16-bit counts (at most NS * kSketch / 2 each)
 #pragma unroll
             for (int i = 0; i < NS; ++i)
 #pragma unroll
-                for (int q = 0; q < kPairs; ++q) a += __vsetgeu2(pk[i][q], t);
-            n[j] = (a & 0xFFFFu) + (a >> 16);
+                for (int q = 0; q < kPairs; ++q) a += __vsetgeu2(pk[i][q], tt);
+            n[j] = __reduce_add_sync(0xffffffffu, (a & 0xFFFFu) + (a >> 16));
         }
-        const uint32_t n1 = __reduce_add_sync(0xffffffffu, n[0]);
-        const uint32_t n2 = __reduce_add_sync(0xffffffffu, n[1]);
-        const uint32_t n3 = __reduce_add_sync(0xffffffffu, n[2]);
-        p |= (n3 >= uint32_t(k) ? 3u : n2 >= uint32_t(k) ? 2u : n1 >= uint32_t(k) ? 1u : 0u) << sh;
+        // counts fall as the threshold rises
+        if (n[2] >= uint32_t(k)) {
+            lo = t[2];
+        } else if (n[1] >= uint32_t(k)) {
+            lo = t[1];
+            hi = t[2];
+        } else if (n[0] >= uint32_t(k)) {
+            lo = t[0];
+            hi = t[1];
+        } else {
+            hi = t[0];
+        }
     }
-    return p << 16;
+    return lo << 16;
 }
 
-static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k)
+static __device__ SLC_FIN_INLINE uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k)
 {
     if (G <= 32) return sketch_bound_n<1>(sk, meta, G, k);
     if (G <= 64) return sketch_bound_n<2>(sk, meta, G, k);
@@ -905,7 +930,7 @@ static __device__ __noinline__ uint32_t sketch_bound(const uint32_t* sk, const u
 
 // Keep, stably and at the front, the words whose key reaches lo; returns how
 // many were kept.
-static __device__ __noinline__ int compact_ge(unsigned long long* c, int n, uint32_t lo)
+static __device__ SLC_FIN_INLINE int compact_ge(unsigned long long* c, int n, uint32_t lo)
 {
     const int lane = threadIdx.x & 31;
     int kept = 0;
@@ -926,7 +951,7 @@ static __device__ __noinline__ int compact_ge(unsigned long long* c, int n, uint
 // Keep (at the front, in their order) the candidates whose key's top 16 bits
 // reach those of the k-th largest key: the k largest words and their ties in
 // that 16-bit bin. Returns how many were kept.
-static __device__ __noinline__ int select_top(unsigned long long* c, int n, int k)
+static __device__ SLC_FIN_INLINE int select_top(unsigned long long* c, int n, int k)
 {
     const int lane = threadIdx.x & 31;
     const uint32_t lo = kth_prefix(uint32_t(k), [&](uint32_t c1, uint32_t c2, uint32_t c3, uint32_t(&m)[3]) {
@@ -991,7 +1016,7 @@ __device__ __forceinline__ void lp_write(const KernelParams& kp, int r, const un
 
 // Sort n words in warp-private shared memory, descending (bitonic through
 // shared memory, padded with zeros up to a power of two; the buffer holds it).
-static __device__ __noinline__ void warp_sort_smem(unsigned long long* a, int n)
+static __device__ SLC_FIN_INLINE void warp_sort_smem(unsigned long long* a, int n)
 {
     const int lane = threadIdx.x & 31;
     int np2 = 1;
@@ -1022,7 +1047,7 @@ static __device__ __noinline__ void warp_sort_smem(unsigned long long* a, int n)
 // The first `keep` of n distinct words in descending order, out[rank] = word:
 // each word's rank is the number of larger words, counted by its lane against
 // every word (broadcast reads, four partial counts).
-static __device__ __noinline__ void rank_sort(const unsigned long long* c, int n, unsigned long long* out, int keep)
+static __device__ SLC_FIN_INLINE void rank_sort(const unsigned long long* c, int n, unsigned long long* out, int keep)
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -1064,7 +1089,7 @@ __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v
 // candidates of a row without top-k or min-p (the exact path takes it).
 // hs / meta: the slices' staged headers and (tau, zs, zc, m) words.
 template <typename InT>
-static __device__ __noinline__ bool cut_and_pick(const SliceParams& P, const RowInfo& ri, int r, uint32_t off_lo,
+static __device__ SLC_FIN_INLINE bool cut_and_pick(const SliceParams& P, const RowInfo& ri, int r, uint32_t off_lo,
                                                  uint32_t off_hi, const unsigned long long* cand, int C, float m,
                                                  float xthr, const SliceHdr* hs, const uint4* meta, int& tok_out)
 {
@@ -1289,7 +1314,7 @@ static __device__ __noinline__ int reread_slices(const SliceParams& P, const Row
 // slices that matter in a second round, which become the candidates. Returns
 // false when the row must take the exact path (m out).
 template <typename InT>
-static __device__ __noinline__ bool finish_trunc(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
+static __device__ SLC_FIN_INLINE bool finish_trunc(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
                                                  uint32_t off_lo, uint32_t off_hi, unsigned char* scratch,
                                                  float& m_out, int& tok, int32_t& st_out)
 {
@@ -1961,7 +1986,7 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
 // they are asked; scratch: the warp's idle staging slot. Returns false when the
 // row is left for the exact path (m: the row maximum).
 template <typename InT>
-__device__ __noinline__ bool finish_row(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
+__device__ SLC_FIN_INLINE bool finish_row(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
                                         uint32_t off_lo, uint32_t off_hi, unsigned char* scratch, float& m)
 {
     m = -INFINITY;
