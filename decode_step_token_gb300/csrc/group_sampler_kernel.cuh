@@ -709,7 +709,7 @@ namespace grp {
 // and by fixed-point softmax mass (top-p over the top-k domain) over the staged row.
 // Leaves the fork's bound set and kind Pick.
 template <typename InT>
-__device__ __noinline__ void exact_fork(GShared& sh, const Part& pt, uint32_t rank, uint32_t C, int f)
+__device__ __noinline__ void exact_fork(GShared& sh, Part pt, uint32_t rank, uint32_t C, int f)
 {
     const RowParams rp = sh.rp[f];
     const float m = sh.bc.m;
@@ -737,7 +737,7 @@ __device__ __noinline__ void exact_fork(GShared& sh, const Part& pt, uint32_t ra
 
 // Gumbel-max over the whole part for an untruncated fork: the part's best two.
 template <typename InT>
-__device__ __noinline__ void plain_fork(GShared& sh, const Part& pt, int f)
+__device__ __noinline__ void plain_fork(GShared& sh, Part pt, int f)
 {
     const RowParams rp = sh.rp[f];
     GumbelAcc g;
@@ -795,7 +795,7 @@ __device__ __noinline__ void pick_warp(GShared& sh, int f, const unsigned long l
 
 // A fork whose kept tokens are all listed reads only this CTA's candidate list.
 template <typename InT>
-__device__ __noinline__ void pick_part(GShared& sh, const Part& pt, int f, const unsigned long long* cand,
+__device__ __noinline__ void pick_part(GShared& sh, Part pt, int f, const unsigned long long* cand,
                                        int ncand)
 {
     const RowParams rp = sh.rp[f];
@@ -839,7 +839,7 @@ __device__ __noinline__ void pick_part(GShared& sh, const Part& pt, int f, const
 // fp32 probs / logprobs of fork f over this CTA's part: 16-byte streaming stores
 // where the output row allows, plain stores for the ragged ends.
 template <typename InT>
-__device__ __noinline__ void write_outputs(const GShared& sh, const KernelParams& K, const Part& pt, int r, int f)
+__device__ __noinline__ void write_outputs(const GShared& sh, const KernelParams& K, Part pt, int r, int f)
 {
     const RowParams& rp = sh.rp[f];
     const ForkOut& fo = sh.bc.f[f];

@@ -166,7 +166,7 @@ __device__ __forceinline__ int vec_find(const uint4& v, float m)
 // NaN sanitising of the vectors a lane reads (the unit is staged whole): NaN
 // becomes -inf in the slot; returns the lane's new maximum.
 template <typename InT>
-__device__ __noinline__ float lane_sanitize(const SliceView<InT>& sv)
+__device__ __noinline__ float lane_sanitize(SliceView<InT> sv)
 {
     const int lane = threadIdx.x & 31;
     uint4* smv = const_cast<uint4*>(sv.sm);
@@ -274,7 +274,7 @@ __device__ __forceinline__ float biased_logit(const KernelParams& kp, const RowI
 // -1 when the row's lists break the limits (more than kMaxBias / kMaxStop
 // entries, an id outside the vocabulary). Warp-wide.
 template <typename InT>
-__device__ __noinline__ int row_extras(const KernelParams& kp, const RowInfo& ri, int lo, int hi, int32_t* xi,
+__device__ __noinline__ int row_extras(const KernelParams& kp, RowInfo ri, int lo, int hi, int32_t* xi,
                                        float* xv)
 {
     constexpr int K = (kMaxExtras + 31) / 32;  // entries per lane
@@ -561,7 +561,7 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
 // Sum over the unit of exp2((x - mx) * s2) (Kahan per lane, double across the
 // warp), as a high and a low fp32 part.
 template <typename InT>
-__device__ __noinline__ void unit_mass(const SliceView<InT>& sv, float mx, float s2, float& hi, float& lo,
+__device__ __noinline__ void unit_mass(SliceView<InT> sv, float mx, float s2, float& hi, float& lo,
                                        const float* xv = nullptr, int nx = 0)
 {
     constexpr int E = Vec<InT>::E;
@@ -744,7 +744,7 @@ __device__ __forceinline__ SliceHdr ld_hdr(const SliceHdr* p)
 // Exact (double-precision) Gumbel score of token v of the row, its logit read
 // again and its Philox word recomputed.
 template <typename InT>
-static __device__ __noinline__ double exact_score(const KernelParams& kp, const RowInfo& ri, uint32_t off_lo,
+static __device__ __noinline__ double exact_score(const KernelParams& kp, RowInfo ri, uint32_t off_lo,
                                                   uint32_t off_hi, int v)
 {
     const RowPhilox rp = row_philox(PhiloxKey{ri.key_lo, ri.key_hi}, ri.stream, off_lo, off_hi);
@@ -1214,7 +1214,7 @@ static __device__ __noinline__ uint4 load_vec_slow(const InT* g, int j, int n)
 // per lane in flight, counted, then written at their warp-wide positions.
 // Returns the new count (more than cap when they do not fit).
 template <typename InT>
-static __device__ __noinline__ int reread_slices(const SliceParams& P, const RowInfo& ri, const uint16_t* re,
+static __device__ __noinline__ int reread_slices(const SliceParams& P, RowInfo ri, const uint16_t* re,
                                                  int nre, uint32_t B, unsigned long long* c, int C0, int cap,
                                                  int32_t* xi, float* xv)
 {
@@ -1449,7 +1449,7 @@ static __device__ SLC_FIN_INLINE bool finish_trunc(const SliceParams& P, WarpScr
 // its top n, so a list that did not overflow holds every token of the row's top
 // n in its slice). `token` is the sampled one; st its status.
 template <typename InT>
-static __device__ __noinline__ bool finish_lp_row(const SliceParams& P, WarpScratch& ws, const RowInfo& ri, int r,
+static __device__ __noinline__ bool finish_lp_row(const SliceParams& P, WarpScratch& ws, RowInfo ri, int r,
                                                   int token, int32_t st, unsigned char* scratch, float& m_out)
 {
     const int lane = threadIdx.x & 31;
@@ -1716,7 +1716,7 @@ __device__ void cta_select(SliceShared& sh, const KernelParams& kp, const RowInf
 
 template <typename InT>
 __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots, const SliceParams& P, int r,
-                                           const RowInfo& ri, float m, uint32_t off_lo, uint32_t off_hi)
+                                           RowInfo ri, float m, uint32_t off_lo, uint32_t off_hi)
 {
     const KernelParams& kp = P.k;
     const int V = int(kp.vocab);
@@ -1842,8 +1842,8 @@ __device__ __noinline__ void cta_exact_row(SliceShared& sh, unsigned char* slots
 // to -inf, and so do the nx biased and banned tokens xi (their values are taken
 // apart). Out of line: the step without extensions keeps its code compact.
 template <typename InT>
-__device__ __noinline__ void stage_extensions(SliceView<InT>& sv, bool masked, const uint32_t* mws,
-                                              const int32_t* xi, int nx)
+__device__ __noinline__ int stage_extensions(SliceView<InT> sv, bool masked, const uint32_t* mws,
+                                             const int32_t* xi, int nx)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -1877,6 +1877,7 @@ __device__ __noinline__ void stage_extensions(SliceView<InT>& sv, bool masked, c
         }
         __syncwarp();
     }
+    return sv.nb;
 }
 
 // Wait for the warp's slot, summarise the unit into its record (row r, slice s).
@@ -1933,7 +1934,7 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
     // sanitising is left to the first lane-maximum pass (a lane that meets a
     // NaN cleans its vectors).
     if (!extra && (sanitizing(kp) || mask_of(kp) || nx > 0)) {
-        stage_extensions<InT>(sv, mask_of(kp) != nullptr, mws, xi, nx);
+        sv.nb = stage_extensions<InT>(sv, mask_of(kp) != nullptr, mws, xi, nx);
         sv.san = sanitizing(kp);
     }
     SliceHdr hdr;
