@@ -28,7 +28,8 @@ struct SliceGeometry {
 struct SliceWorkspace {
     void* hdr;       // [rows][G] 16-byte slice headers
     void* body;      // [rows][G] slice bodies
-    uint32_t* cnt;   // [rows * kSliceCntStride] arrival counters (one per 128-byte line), zero between launches
+    uint32_t* cnt;   // [rows * kSliceCntStride] per row: its arrival counter (alone in a 128-byte line)
+                     // and a 256-bin histogram of its truncated units' sketch keys; zero between launches
     unsigned long long* stats;  // may be NULL
 };
 
@@ -38,7 +39,7 @@ constexpr int kSliceMaxRows = 256;
 constexpr int kSliceMaxSlices = 128;
 constexpr size_t kSliceHdrBytes = 16;
 constexpr size_t kSliceBodyBytes = 464;
-constexpr int kSliceCntStride = 32;  // 32-bit words between two rows' counters
+constexpr int kSliceCntStride = 32 + 256;  // 32-bit words between two rows' counters (counter line + histogram)
 
 // True when this library's kernels load on the current device.
 bool kernels_loadable();

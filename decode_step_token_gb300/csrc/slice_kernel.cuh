@@ -558,6 +558,25 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
 }
 
 // ---------------------------------------------------------------- truncated unit
+// Bin of a sketch key in its row's histogram: 1/4 wide over the logits
+// [-32, 32), the outer two bins taking everything beyond.
+__device__ __forceinline__ uint32_t key_bin(uint32_t key)
+{
+    const int b = __float2int_rd(key2f(key) * 4.0f) + kHistBins / 2;
+    return uint32_t(min(max(b, 0), kHistBins - 1));
+}
+
+// 16-bit prefixes that enclose bin b: every key of the bin reaches lo << 16,
+// and a key that reaches hi << 16 lies in a higher bin (inner bins only).
+__device__ __forceinline__ uint32_t bin_lo_prefix(int b)
+{
+    return f2key(float(b - kHistBins / 2) * 0.25f) >> 16;
+}
+__device__ __forceinline__ uint32_t bin_hi_prefix(int b)
+{
+    return (f2key(float(b + 1 - kHistBins / 2) * 0.25f) >> 16) + 1u;
+}
+
 // Sum over the unit of exp2((x - mx) * s2) (Kahan per lane, double across the
 // warp), as a high and a low fp32 part.
 template <typename InT>
@@ -592,7 +611,7 @@ __device__ __noinline__ void unit_mass(SliceView<InT> sv, float mx, float s2, fl
 template <typename InT>
 __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowInfo& ri, SliceHdr& hdr_out,
                                            SliceBody* body, uint32_t* q, const int32_t* xi = nullptr,
-                                           const float* xv = nullptr, int nx = 0)
+                                           const float* xv = nullptr, int nx = 0, uint32_t* hist = nullptr)
 {
     constexpr int E = Vec<InT>::E;
     const int lane = threadIdx.x & 31;
@@ -620,7 +639,10 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     }
     const uint32_t nfin = __popc(__ballot_sync(0xffffffffu, lkey != 0u));
     const uint32_t m = min(uint32_t(ri.m), nfin);
-    if (lkey != 0u && rank < m) body->sketch[rank] = lkey;
+    if (lkey != 0u && rank < m) {
+        body->sketch[rank] = lkey;
+        if (hist) atomicAdd(hist + key_bin(lkey), 1u);  // the row's histogram of sketch keys
+    }
     // (a unit with fewer finite lane maxima than mt lists every finite token: only
     // then is its list sure to hold its top mt)
     const uint32_t at = __ballot_sync(0xffffffffu, nfin >= uint32_t(ri.mt) && rank == uint32_t(ri.mt) - 1u);
@@ -854,7 +876,8 @@ __device__ __forceinline__ void count3_key(uint32_t key, uint32_t c1, uint32_t c
 // do) from those two and cuts the range in four each round: few rounds, since
 // the keys of one row span a narrow range of prefixes.
 template <int NS>
-__device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uint4* meta, int G, int k)
+__device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uint4* meta, int G, int k,
+                                                   const uint32_t* hist)
 {
     const int lane = threadIdx.x & 31;
     constexpr int kPairs = kSketch / 2;
@@ -886,6 +909,38 @@ __device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uin
     }
     uint32_t lo = __reduce_min_sync(0xffffffffu, pmin);
     uint32_t hi = __reduce_max_sync(0xffffffffu, pmax) + 1u;
+    if (hist) {
+        // the bin that holds the k-th largest key, from the top (lane l holds
+        // bins 255 - 8 l down to 248 - 8 l); the answer lies within it
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = hist[kHistBins - 1 - 8 * lane - i];
+            sum += c[i];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const uint32_t at = __ballot_sync(0xffffffffu, incl >= uint32_t(k));
+        int bin = 0;
+        if (at) {
+            const int src = __ffs(at) - 1;
+            uint32_t run = incl - sum;
+            int mine = -1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // the lane's top bin first
+                run += c[i];
+                if (mine < 0 && run >= uint32_t(k)) mine = kHistBins - 1 - 8 * lane - i;
+            }
+            bin = __shfl_sync(0xffffffffu, mine, src);
+            // bin 0 reaches down to -inf, bin 255 up to +inf
+            if (bin > 0) lo = max(lo, bin_lo_prefix(bin));
+            if (bin < kHistBins - 1) hi = min(hi, bin_hi_prefix(bin));
+        }
+    }
 #pragma unroll 1
     while (hi - lo > 1u) {
         const uint32_t d = hi - lo - 1u;
@@ -920,12 +975,13 @@ __device__ __forceinline__ uint32_t sketch_bound_n(const uint32_t* sk, const uin
     return lo << 16;
 }
 
-static __device__ SLC_FIN_INLINE uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k)
+static __device__ SLC_FIN_INLINE uint32_t sketch_bound(const uint32_t* sk, const uint4* meta, int G, int k,
+                                                      const uint32_t* hist = nullptr)
 {
-    if (G <= 32) return sketch_bound_n<1>(sk, meta, G, k);
-    if (G <= 64) return sketch_bound_n<2>(sk, meta, G, k);
-    if (G <= 96) return sketch_bound_n<3>(sk, meta, G, k);
-    return sketch_bound_n<kSPL>(sk, meta, G, k);
+    if (G <= 32) return sketch_bound_n<1>(sk, meta, G, k, hist);
+    if (G <= 64) return sketch_bound_n<2>(sk, meta, G, k, hist);
+    if (G <= 96) return sketch_bound_n<3>(sk, meta, G, k, hist);
+    return sketch_bound_n<kSPL>(sk, meta, G, k, hist);
 }
 
 // Keep, stably and at the front, the words whose key reaches lo; returns how
@@ -1327,7 +1383,13 @@ static __device__ SLC_FIN_INLINE bool finish_trunc(const SliceParams& P, WarpScr
     uint32_t* sk = reinterpret_cast<uint32_t*>(scratch + size_t(G) * 32);  // [G][kSketch]
     unsigned long long* area = reinterpret_cast<unsigned long long*>(sk);  // the lists, over the sketches
     const int cap = int((size_t(kSlotBytes) - size_t(32) * G) / 8);
+    // the row's histogram of sketch keys, at the end of the slot (read before the
+    // lists reach it)
+    uint32_t* hist = P.cnt + size_t(r) * kCntStride + kHistOff;
+    uint32_t* hsm = reinterpret_cast<uint32_t*>(scratch + kSlotBytes - kHistBins * 4);
     // round 1
+    cp_async16(hsm + 8 * lane, hist + 8 * lane);
+    cp_async16(hsm + 8 * lane + 4, hist + 8 * lane + 4);
 #pragma unroll 1
     for (int b = lane; b < G; b += 32) {
         cp_async16(hs + b, hd + b);
@@ -1336,6 +1398,9 @@ static __device__ SLC_FIN_INLINE bool finish_trunc(const SliceParams& P, WarpScr
         cp_async16(sk + b * kSketch + 4, &bd[b].sketch[4]);
     }
     cp_async_commit_wait();
+    // the histogram is zero again for the next launch
+    reinterpret_cast<uint4*>(hist)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(hist)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     SLC_MARK(7);
     uint32_t fl = 0, nkeys = 0, taumax = 0;
@@ -1372,7 +1437,7 @@ static __device__ SLC_FIN_INLINE bool finish_trunc(const SliceParams& P, WarpScr
     uint32_t B;
     if (ri.do_topk) {
         if (ri.k > kKCap || nkeys < uint32_t(ri.k)) return false;
-        B = sketch_bound(sk, meta, G, ri.k);
+        B = sketch_bound(sk, meta, G, ri.k, hsm);
     } else if (ri.do_minp) {
         B = f2key(xthr);
     } else {
@@ -1969,7 +2034,8 @@ __device__ __forceinline__ bool process_unit(const SliceParams& P, const RowInfo
             __syncwarp();
             if (row_lp(ri)) unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
         } else {
-            unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx);
+            unit_trunc<InT>(sv, ri, hdr, body, reinterpret_cast<uint32_t*>(q), xi, xv, nx,
+                            P.cnt + size_t(r) * kCntStride + kHistOff);
         }
     }
     hdr.flags |= extra;

@@ -82,7 +82,9 @@ constexpr uint32_t kDrainPolls = 1u << 26;  // polls granted to a copy after a w
 // Each row's arrival counter sits in its own 128-byte line: G warps add to every
 // counter, and counters sharing a line would serialise their atomics in one L2
 // slice.
-constexpr int kCntStride = 32;
+constexpr int kCntStride = 32 + 256;  // per row: the arrival counter's line, then the sketch-key histogram
+constexpr int kHistOff = 32;          // first histogram word
+constexpr int kHistBins = 256;        // bins of 1/4 over the logits [-32, 32) (the outer two take the rest)
 
 enum : uint8_t { kClsTrunc = 0, kClsPlain = 1, kClsGreedy = 2, kClsErr = 3 };
 
@@ -118,7 +120,7 @@ struct SliceParams {
     int32_t n_units;     // n_rows * G
     SliceHdr* hdr;       // [n_rows][G]
     SliceBody* body;     // [n_rows][G]
-    uint32_t* cnt;       // [n_rows * kCntStride] arrivals (one per line); zero between launches
+    uint32_t* cnt;       // [n_rows * kCntStride] arrivals (one per line) and sketch-key histograms; zero between launches
     unsigned long long* stats;  // [0]: rows finished by the exact path (may be NULL)
     uint32_t max_polls;  // bound of each wait on a staging copy
     int32_t pdl;         // launched as a programmatic dependent: wait for the grid before it
@@ -184,6 +186,7 @@ constexpr size_t kSmemBytes = kHead + size_t(kW) * kSlotBytes;
 constexpr size_t kMaxSmem = 227 * 1024;
 static_assert(kSmemBytes <= kMaxSmem, "shared memory per CTA");
 static_assert(kSlotBytes >= 1024 * 8, "a free slot holds 1024 candidates");
+static_assert(kMaxSlices * 64 + kHistBins * 4 <= kSlotBytes, "a truncated row's finish stages its records and histogram in a slot");
 static_assert(kTQCap * 4 <= int(sizeof(WarpScratch::q)) && kTQCap > kLCap, "truncated-unit queue");
 static_assert(kMaskWords * 4 <= int(sizeof(WarpScratch::q)) && kMaskWords >= kSlotBytes / 2 / 32 + 2,
               "a unit's mask words fit the queue scratch");
