@@ -208,15 +208,16 @@ int sampler_sample_host(sampler_t h, const sampler_args_t* args, sampler_stream_
  * Allocation-free sampling step. None of the pages has a counterpart: the
  * sampler they describe always owns its buffers. This entry point takes no
  * handle and allocates nothing. Its workspace (per-row arrival counters and
- * per-(row, slice) records, 3.6 MiB) is an array in the library's own device
- * memory, one copy per device. It runs the same kernel sampler_sample uses for
- * small batches and returns the same tokens. Every launch leaves the counters
- * at zero, and a row whose wait gave up (SAMPLER_ROW_TIMEOUT) leaves no state
- * behind, so one bad call never affects a later one.
+ * sketch-key histograms, per-(row, slice) records, 3.8 MiB) is an array in the
+ * library's own device memory, one copy per device. It runs the same kernel
+ * sampler_sample uses for small batches and returns the same tokens. Every
+ * launch leaves the counters and histograms at zero, and a row whose wait gave
+ * up (SAMPLER_ROW_TIMEOUT) leaves no state behind, so one bad call never
+ * affects a later one.
  *
  * The first call on a device does a one-time set-up on the current device:
  * it looks up that array's address, reads the SM count and clears the row
- * counters on `stream`. Make that first call before any stream capture.
+ * counters and histograms on `stream`. Make that first call before any stream capture.
  *
  * Arguments as for sampler_sample (device pointers on the current device),
  * with these limits:
