@@ -268,8 +268,13 @@ __device__ __forceinline__ unsigned long long block_incl_scan_u64(unsigned long 
 // term rounded down -- or NaN when all of them fall short. Two rounds of 256 bins:
 // on a log scale of the distance to m, then evenly inside the bin where the target
 // is met. Bins only order the values (larger bin, smaller value).
-// `bins` is 4 x 256 words of shared memory.
-__device__ __noinline__ float tmax_select(GShared& sh, uint32_t* bins, const float* v, int C, float m, float tmin,
+// `bins` is 4 x 256 words of shared memory. The thread's maxima come by value
+// (their first C entries): an array whose address reached this out-of-line
+// function would live in local memory.
+struct TmaxVals {
+    float x[kMaxParts];
+};
+__device__ __noinline__ float tmax_select(GShared& sh, uint32_t* bins, const TmaxVals v, int C, float m, float tmin,
                                           bool mass, float invT, unsigned long long target)
 {
     const int tid = threadIdx.x;
@@ -290,9 +295,10 @@ __device__ __noinline__ float tmax_select(GShared& sh, uint32_t* bins, const flo
         // level 0: bins on a log scale of the distance to m (heavy tails and narrow
         // rows alike spread over them); level 1: even bins inside the chosen bin
         const float inv = hi > lo ? 256.0f / (hi - lo) : 0.0f;
-        for (int c = 0; c < C; ++c) {
-            const float x = v[c];
-            if (!(x > -INFINITY && x >= lo && x <= hi)) continue;
+#pragma unroll
+        for (int c = 0; c < kMaxParts; ++c) {
+            const float x = v.x[c];
+            if (c >= C || !(x > -INFINITY && x >= lo && x <= hi)) continue;
             const int bin = level == 0 ? min(255, int(__log2f(1.0f + (m - x) * invT_bins) * 16.0f))
                                        : min(255, max(0, int((hi - x) * inv)));
             const uint32_t key = f2key(x);
@@ -333,7 +339,7 @@ __device__ __noinline__ void tmax_bounds(GShared& sh, uint32_t C, int g, float m
 {
     const int tid = threadIdx.x;
     const int n = int(C) * kT;
-    float v[kMaxParts];
+    TmaxVals v;
     uint32_t kv[kMaxParts];
 #pragma unroll
     for (int c = 0; c < kMaxParts; ++c)
@@ -341,8 +347,8 @@ __device__ __noinline__ void tmax_bounds(GShared& sh, uint32_t C, int g, float m
     float lo = INFINITY;
 #pragma unroll
     for (int c = 0; c < kMaxParts; ++c) {
-        v[c] = c < int(C) ? key2f(kv[c]) : -INFINITY;
-        if (v[c] > -INFINITY) lo = fminf(lo, v[c]);
+        v.x[c] = c < int(C) ? key2f(kv[c]) : -INFINITY;
+        if (v.x[c] > -INFINITY) lo = fminf(lo, v.x[c]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
@@ -903,10 +909,14 @@ __device__ __noinline__ void write_outputs(const GShared& sh, const KernelParams
 namespace dst {
 namespace grp {
 
-// Leader CTA: concatenate the C candidate lists (counts[c] words in CTA c) into
-// `list`; each thread issues all its remote loads before storing any.
+// Leader CTA: concatenate the C candidate lists (counts.n[c] words in CTA c) into
+// `list`; each thread issues all its remote loads before storing any. The counts
+// come by value and are indexed by constants only, so they stay in registers.
+struct PartCounts {
+    uint32_t n[kMaxParts];
+};
 __device__ __noinline__ void gather_lists(unsigned long long* list, const unsigned long long* cand,
-                                          const uint32_t* counts, uint32_t C, int total)
+                                          const PartCounts counts, uint32_t C, int total)
 {
     constexpr int kU = 16;  // list capacity / kT
     const int tid = threadIdx.x;
@@ -917,9 +927,12 @@ __device__ __noinline__ void gather_lists(unsigned long long* list, const unsign
         w[u] = 0ull;
         if (gi < total) {
             int c = 0, li = gi;
-            for (int cc = 0; cc + 1 < int(C) && li >= int(counts[cc]); ++cc) {
-                li -= int(counts[cc]);
-                c = cc + 1;
+#pragma unroll
+            for (int cc = 0; cc + 1 < kMaxParts; ++cc) {
+                if (c == cc && cc + 1 < int(C) && li >= int(counts.n[cc])) {
+                    li -= int(counts.n[cc]);
+                    c = cc + 1;
+                }
             }
             w[u] = dsmem_ld_u64(dsmem_map(smem_addr(&cand[li]), uint32_t(c)));
         }
@@ -1422,16 +1435,16 @@ __global__ void __launch_bounds__(kT, 2) group_kernel(const __grid_constant__ Gr
                 __syncthreads();
                 cluster_sync();
                 if (rank == 0) {
-                    uint32_t counts[kMaxParts];
+                    PartCounts counts;
                     uint32_t total = 0;
                     bool overflow = false;
 #pragma unroll
                     for (int c = 0; c < kMaxParts; ++c)
-                        counts[c] = c < int(C) ? dsmem_ld_u32(dsmem_map(smem_addr(&sh.part.ncand), uint32_t(c))) : 0u;
+                        counts.n[c] = c < int(C) ? dsmem_ld_u32(dsmem_map(smem_addr(&sh.part.ncand), uint32_t(c))) : 0u;
 #pragma unroll
                     for (int c = 0; c < kMaxParts; ++c) {
-                        overflow |= counts[c] > uint32_t(cap);
-                        total += counts[c];
+                        overflow |= counts.n[c] > uint32_t(cap);
+                        total += counts.n[c];
                     }
                     overflow |= total > uint32_t(P.list_cap);
                     bool need_sort = false;

@@ -285,6 +285,27 @@ def test_exact_path_runs_and_matches(sampler):
     assert sampler.stat(0, reset=True) > 0
 
 
+def test_truncated_rows_repeat_without_exact_path(sampler):
+    """Back-to-back calls with truncated rows on one handle, batches of different
+    sizes interleaved: each truncated unit adds its sketch keys to its row's
+    histogram and the finishing warp clears it, so every call gives the same
+    tokens and no row falls to the exact path (a histogram left over from an
+    earlier call would move the bound past the row's k-th value)."""
+    lat, mix = workloads.latency(32), workloads.mixed()
+    first = {}
+    sampler.stat(0, reset=True)
+    for rep in range(3):
+        for b in (lat, mix, lat):
+            g = dev.run(sampler, b, want_probs=False)
+            assert (g.status == 0).all()
+            if b.name not in first:
+                first[b.name] = g.tokens
+            assert np.array_equal(g.tokens, first[b.name]), (rep, b.name)
+    assert sampler.stat(0, reset=True) == 0
+    o = oracle.sample(lat, want_probs=False, nthreads=16)
+    assert np.array_equal(first[lat.name][~o.ambiguous()], o.tokens[~o.ambiguous()])
+
+
 def test_wait_timeout_status():
     """A handle whose staging waits give up at once reports status 5 on every row
     of a small batch (token -1), and the next call on an ordinary handle is
