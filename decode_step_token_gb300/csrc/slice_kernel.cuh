@@ -559,6 +559,16 @@ __device__ __forceinline__ void unit_plain(const SliceView<InT>& sv, const RowIn
 }
 
 // ---------------------------------------------------------------- truncated unit
+// Position of the n-th set bit (counting from 0) of a mask that has more than n.
+__device__ __forceinline__ int nth_set_lane(uint32_t mask, int n)
+{
+    int pos = 0;
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1)
+        if (__popc(mask & ((1u << (pos + w)) - 1u)) <= n) pos += w;
+    return pos;
+}
+
 // Bin of a sketch key in its row's histogram: 1/4 wide over the logits
 // [-32, 32), the outer two bins taking everything beyond.
 __device__ __forceinline__ uint32_t key_bin(uint32_t key)
@@ -658,10 +668,19 @@ __device__ __forceinline__ void unit_trunc(const SliceView<InT>& sv, const RowIn
     const typename Vec<InT>::Thr t2 = Vec<InT>::thr(t);
     uint32_t total = 0;
     int nq = 0;
+    // only the vectors of the lanes whose maximum reaches tau can hold such tokens
+    // (vector j is lane j % 32's): they are spread over all 32 lanes, work item
+    // w = i * na + a standing for vector i * 32 + (the a-th such lane)
+    const uint32_t act = __ballot_sync(0xffffffffu, lkey >= tau);
+    const int na = __popc(act);
+    const int work = na * ((sv.nvec + 31) >> 5);
+    const float inv_na = na ? 1.0f / float(na) : 0.0f;
 #pragma unroll 1
-    for (int j0 = 0; j0 < sv.nvec; j0 += 32) {
-        const int j = j0 + lane;
-        const uint32_t hit = (j < sv.nvec && lkey >= tau) ? Vec<InT>::mask_ge(sv.vec(j), t2) : 0u;
+    for (int w0 = 0; w0 < work; w0 += 32) {
+        const int w = w0 + lane;
+        const int i = int((float(w) + 0.5f) * inv_na);  // w / na, exact for these sizes
+        const int j = i * 32 + nth_set_lane(act, w - i * na);
+        const uint32_t hit = (w < work && j < sv.nvec) ? Vec<InT>::mask_ge(sv.vec(j), t2) : 0u;
         const uint32_t bal = __ballot_sync(0xffffffffu, hit != 0u);
         const int at = nq + __popc(bal & ((1u << lane) - 1u));
         if (hit && at < kTQCap) q[at] = (uint32_t(j) << 8) | hit;
